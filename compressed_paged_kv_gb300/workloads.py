@@ -1,0 +1,316 @@
+"""Seeded synthetic inputs for the compression / decode-attention hot path.
+
+This module builds INPUTS only: random K/V/Q tensors, block tables, refcounts
+and free stacks with the shapes and structure of the workloads below.  It holds
+none of the method's arithmetic (no scores, no selection, no compaction, no
+attention), so both the CUDA path and the CPU oracle can be fed from it.
+
+Workloads (shapes of the models the Zipage summaries evaluate: Qwen3-8B and
+DeepSeek-R1-Distill-Llama-8B, KV budget 2048 tokens):
+
+  tiny         1 layer, 2/4 heads, d 64, b 16, N_max 8, 2 requests sharing
+               block 0 (refcount 2); K, V, Q i.i.d. N(0,1).
+  qwen3_1l     1 layer, 8/32 heads, d 128, b 16, N_max 128, 64 requests, no
+               sharing; K, V, Q i.i.d. N(0,1).
+  qwen3_36l    36 layers, 256 requests in 32 groups of 8 sharing a 4-block
+               prompt prefix (refcount 8); K AR(1) rho 0.9 + 1% heavy hitters
+               (x8); V, Q N(0,1).
+  long4k       36 layers, N_max 256, 128 requests, K AR(1) rho 0.95, V N(0,1).
+  mixed        32 layers, 512 requests, lengths uniform in [1024, 2048]; 51
+               of them forced to 2048 (they compress); the rest decode.
+
+All tensors are generated in fp32 from torch generators seeded per (tensor,
+layer) from a master seed, then rounded once to bf16.  Physical block ids are
+a seeded permutation, so block tables are not contiguous.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+MASK64 = (1 << 64) - 1
+
+
+def splitmix64(x: int) -> int:
+    """One step of the SplitMix64 generator (Steele, Lea, Flood 2014)."""
+    x = (x + 0x9E3779B97F4A7C15) & MASK64
+    z = x
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & MASK64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & MASK64
+    return z ^ (z >> 31)
+
+
+def derive_seed(master: int, *keys: int) -> int:
+    s = splitmix64(master & MASK64)
+    for k in keys:
+        s = splitmix64(s ^ (k & MASK64))
+    return s & ((1 << 63) - 1)
+
+
+TENSOR_K, TENSOR_V, TENSOR_Q, TENSOR_DQ, TENSOR_TABLE, TENSOR_HH, TENSOR_LEN = range(7)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    L: int
+    Hkv: int
+    Hq: int
+    d: int
+    b: int
+    N: int            # N_max: blocks per request at compression
+    w: int            # observation window
+    lam: float        # lambda
+    R: int            # requests in the batch
+    group: int = 1    # requests per prefix-sharing group
+    prefix_blocks: int = 0
+    rho: float = 0.0  # AR(1) coefficient of K along the sequence (0: i.i.d.)
+    hh_prob: float = 0.0
+    hh_scale: float = 8.0
+    spare_blocks: int = 64
+    mixed: bool = False
+    mixed_compress: int = 0
+    mixed_len_lo: int = 0
+    seed: int = 0
+
+    @property
+    def G(self):
+        return self.Hq // self.Hkv
+
+    @property
+    def T(self):
+        return self.N * self.b
+
+    @property
+    def C(self):
+        return self.T - self.w
+
+    @property
+    def n_keep(self):
+        return (self.N - 1) * self.b - self.w
+
+    def units(self, R=None):
+        return (self.R if R is None else R) * self.L * self.Hkv
+
+    def unit_bytes(self, moved=None):
+        """Algorithmic bytes of one compression unit: K read once for scoring,
+        V read + K write + V write of the moved rows, the window queries."""
+        M = (self.N - 1) * self.b if moved is None else moved
+        row = self.d * 2
+        return self.T * row + 3 * M * row + self.w * self.G * row
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", L=1, Hkv=2, Hq=4, d=64, b=16, N=8, w=8, lam=0.5, R=2, group=2,
+                     prefix_blocks=1, spare_blocks=16, seed=20260000),
+    "qwen3_1l": Workload("qwen3_1l", L=1, Hkv=8, Hq=32, d=128, b=16, N=128, w=8, lam=0.5,
+                         R=64, spare_blocks=64, seed=20260001),
+    "qwen3_36l": Workload("qwen3_36l", L=36, Hkv=8, Hq=32, d=128, b=16, N=128, w=8, lam=0.5,
+                          R=256, group=8, prefix_blocks=4, rho=0.9, hh_prob=0.01,
+                          spare_blocks=1024 + 64, seed=20260002),
+    "long4k": Workload("long4k", L=36, Hkv=8, Hq=32, d=128, b=16, N=256, w=8, lam=0.5, R=128,
+                       rho=0.95, spare_blocks=64, seed=20260003),
+    "mixed": Workload("mixed", L=32, Hkv=8, Hq=32, d=128, b=16, N=128, w=8, lam=0.5, R=512,
+                      mixed=True, mixed_compress=51, mixed_len_lo=1024, spare_blocks=64,
+                      seed=20260004),
+}
+# Index order used by the configuration list this library is measured on.
+WORKLOAD_ORDER = ["tiny", "qwen3_1l", "qwen3_36l", "long4k", "mixed"]
+
+
+def scaled(wl: Workload, **changes) -> Workload:
+    """A copy of a workload with some fields changed (smaller test cases)."""
+    return dataclasses.replace(wl, **changes)
+
+
+def _gen(device, seed):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _normal(shape, device, seed):
+    return torch.randn(shape, generator=_gen(device, seed), device=device, dtype=torch.float32)
+
+
+def _ar1(eps: torch.Tensor, rho: float) -> torch.Tensor:
+    """x_0 = eps_0;  x_t = rho x_{t-1} + sqrt(1-rho^2) eps_t along dim -2.
+    Evaluated in chunks: inside a chunk the recursion is a small lower-
+    triangular matrix product; chunks are chained sequentially."""
+    if rho == 0.0:
+        return eps
+    T = eps.shape[-2]
+    CH = 64
+    s = math.sqrt(1.0 - rho * rho)
+    idx = torch.arange(CH, device=eps.device, dtype=torch.float32)
+    expo = (idx[:, None] - idx[None, :]).clamp(min=0)
+    tri = torch.where(idx[:, None] >= idx[None, :], rho ** expo, torch.zeros_like(expo))
+    decay = rho ** (idx + 1.0)
+    out = torch.empty_like(eps)
+    prev = None
+    for c0 in range(0, T, CH):
+        e = eps[..., c0:c0 + CH, :]
+        n = e.shape[-2]
+        inject = e.clone()
+        if c0 == 0:
+            inject[..., 1:, :] *= s  # x_0 = eps_0 exactly
+        else:
+            inject *= s
+        x = torch.matmul(tri[:n, :n], inject)
+        if prev is not None:
+            x = x + decay[:n, None] * prev[..., None, :]
+        out[..., c0:c0 + n, :] = x
+        prev = x[..., -1, :]
+    return out
+
+
+@dataclasses.dataclass
+class CacheState:
+    """A paged KV cache and its block accounting (all tensors on one device)."""
+    wl: Workload
+    k_pools: list          # L x [num_blocks][Hkv][b][d] bf16
+    v_pools: list
+    block_tables: torch.Tensor  # [rows][max_blocks] int32
+    lengths: torch.Tensor       # [rows] int32
+    refcount: torch.Tensor      # [num_blocks] int32
+    free_ids: torch.Tensor      # [num_blocks] int32 (capacity = num_blocks)
+    free_count: torch.Tensor    # [1] int32
+    window_q: torch.Tensor      # [L][Rc][Hq][w][d] bf16 (compressing requests)
+    decode_q: torch.Tensor      # [L][rows][Hq][d] bf16
+    compress_rows: torch.Tensor  # [Rc] int32: rows that compress
+    decode_rows: torch.Tensor    # [Rd] int32: rows that decode only
+
+    @property
+    def num_blocks(self):
+        return self.refcount.shape[0]
+
+
+def build_cache(wl: Workload, device="cpu", seed=None, with_decode_q=True) -> CacheState:
+    """Builds the cache of a workload: every request's K/V rows written through
+    its block table into per-layer pools, plus the queries of one step."""
+    master = wl.seed if seed is None else seed
+    b, N, d, Hkv, L = wl.b, wl.N, wl.d, wl.Hkv, wl.L
+    R = wl.R
+    gcpu = _gen("cpu", derive_seed(master, TENSOR_LEN))
+    if wl.mixed:
+        lengths = torch.randint(wl.mixed_len_lo, N * b + 1, (R,), generator=gcpu, dtype=torch.int64)
+        perm = torch.randperm(R, generator=gcpu)
+        compress_rows = torch.sort(perm[:wl.mixed_compress]).values
+        lengths[compress_rows] = N * b
+        mask = torch.ones(R, dtype=torch.bool)
+        mask[compress_rows] = False
+        decode_rows = torch.arange(R)[mask]
+    else:
+        lengths = torch.full((R,), N * b, dtype=torch.int64)
+        compress_rows = torch.arange(R)
+        decode_rows = torch.arange(0)
+    nblk = (lengths + b - 1) // b
+
+    # physical block assignment: shared prefix blocks once per group
+    group = max(wl.group, 1)
+    pb = wl.prefix_blocks if group > 1 else 0
+    n_groups = (R + group - 1) // group
+    used = int(nblk.sum().item()) - (R - n_groups) * pb
+    num_blocks = used + wl.spare_blocks
+    gperm = _gen("cpu", derive_seed(master, TENSOR_TABLE))
+    phys = torch.randperm(num_blocks, generator=gperm).to(torch.int32)
+    tables = torch.zeros((R, N), dtype=torch.int32)
+    refcount = torch.zeros(num_blocks, dtype=torch.int32)
+    nxt = 0
+    for gi in range(n_groups):
+        members = list(range(gi * group, min((gi + 1) * group, R)))
+        shared = phys[nxt:nxt + pb]
+        nxt += pb
+        for r in members:
+            tables[r, :pb] = shared
+            own = int(nblk[r].item()) - pb
+            tables[r, pb:pb + own] = phys[nxt:nxt + own]
+            nxt += own
+        if pb:
+            refcount[shared.long()] = len(members)
+    assert nxt == used
+    for r in range(R):
+        own = tables[r, pb:int(nblk[r].item())]
+        refcount[own.long()] += 1
+    free_list = phys[used:].clone()
+    free_ids = torch.full((num_blocks,), -1, dtype=torch.int32)
+    free_ids[:free_list.numel()] = free_list
+    free_count = torch.tensor([free_list.numel()], dtype=torch.int32)
+
+    T = N * b
+    k_pools, v_pools = [], []
+    flat_tables = tables.to(device).long()
+    for l in range(L):
+        eps = _normal((R, Hkv, T, d), device, derive_seed(master, TENSOR_K, l))
+        veps = _normal((R, Hkv, T, d), device, derive_seed(master, TENSOR_V, l))
+        if pb:
+            # prefix tokens are generated once per group (from its first member)
+            P = pb * b
+            lead = (torch.arange(R, device=device) // group) * group
+            eps[:, :, :P] = eps[lead][:, :, :P]
+            veps[:, :, :P] = veps[lead][:, :, :P]
+        K = _ar1(eps, wl.rho)
+        if wl.hh_prob > 0:
+            u = torch.rand((R, Hkv, T), generator=_gen(device, derive_seed(master, TENSOR_HH, l)),
+                           device=device)
+            if pb:
+                P = pb * b
+                lead = (torch.arange(R, device=device) // group) * group
+                u[:, :, :P] = u[lead][:, :, :P]
+            K = torch.where((u < wl.hh_prob)[..., None], K * wl.hh_scale, K)
+        kb = K.to(torch.bfloat16)
+        vb = veps.to(torch.bfloat16)
+        del K, eps, veps
+        kpool = torch.zeros((num_blocks, Hkv, b, d), dtype=torch.bfloat16, device=device)
+        vpool = torch.zeros((num_blocks, Hkv, b, d), dtype=torch.bfloat16, device=device)
+        # [R][Hkv][N][b][d] -> rows of blocks; only the live blocks are written
+        kb = kb.view(R, Hkv, N, b, d).permute(0, 2, 1, 3, 4)
+        vb = vb.view(R, Hkv, N, b, d).permute(0, 2, 1, 3, 4)
+        live = torch.arange(N, device=device)[None, :] < nblk.to(device)[:, None]
+        kpool[flat_tables[live]] = kb[live]
+        vpool[flat_tables[live]] = vb[live]
+        del kb, vb
+        k_pools.append(kpool)
+        v_pools.append(vpool)
+
+    Rc = compress_rows.numel()
+    window_q = torch.empty((L, Rc, wl.Hq, wl.w, d), dtype=torch.bfloat16, device=device)
+    for l in range(L):
+        window_q[l] = _normal((Rc, wl.Hq, wl.w, d), device,
+                              derive_seed(master, TENSOR_Q, l)).to(torch.bfloat16)
+    if with_decode_q:
+        decode_q = torch.empty((L, R, wl.Hq, d), dtype=torch.bfloat16, device=device)
+        for l in range(L):
+            decode_q[l] = _normal((R, wl.Hq, d), device,
+                                  derive_seed(master, TENSOR_DQ, l)).to(torch.bfloat16)
+    else:
+        decode_q = torch.empty(0, dtype=torch.bfloat16, device=device)
+    i32 = dict(dtype=torch.int32, device=device)
+    return CacheState(
+        wl=wl, k_pools=k_pools, v_pools=v_pools, block_tables=tables.to(**i32),
+        lengths=lengths.to(**i32), refcount=refcount.to(**i32), free_ids=free_ids.to(**i32),
+        free_count=free_count.to(**i32), window_q=window_q, decode_q=decode_q,
+        compress_rows=compress_rows.to(**i32), decode_rows=decode_rows.to(**i32))
+
+
+def bf16_bits(t: torch.Tensor):
+    """Raw uint16 bit patterns of a bf16 tensor, as a host numpy array."""
+    import numpy as np
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def snapshot(st: CacheState) -> dict:
+    """Host copy of every mutable piece of a cache state."""
+    return dict(
+        k_pools=[bf16_bits(k) for k in st.k_pools],
+        v_pools=[bf16_bits(v) for v in st.v_pools],
+        block_tables=st.block_tables.cpu().numpy().copy(),
+        lengths=st.lengths.cpu().numpy().copy(),
+        refcount=st.refcount.cpu().numpy().copy(),
+        free_ids=st.free_ids.cpu().numpy().copy(),
+        free_count=int(st.free_count.cpu().item()),
+        window_q=bf16_bits(st.window_q),
+        compress_rows=st.compress_rows.cpu().numpy().copy(),
+    )

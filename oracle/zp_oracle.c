@@ -1,0 +1,530 @@
+/*
+ * zp_oracle.c -- plain fp64 CPU oracle for the Compressed PagedAttention hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Tests, the smoke check and the benchmark's CPU
+ * baseline leg are the only callers.  The product path (the CUDA library) never
+ * links, loads or calls this file, and this file includes nothing from it.
+ *
+ * Sources (page title, then section):
+ *   [ZP-nl]  "Zipage: Maintain High Request Concurrency for LLM Reasoning through
+ *            Compressed PagedAttention", gist.science Dutch summary,
+ *            "Technische samenvatting / Methodologie".
+ *   [ZP-ko]  the same paper, gist.science Korean summary, "기술 요약 / 2. 방법론".
+ *   [PKV]    "Paged KV cache and continuous batching for LLMs" (upskillscore),
+ *            "How it works".
+ *
+ * What is computed, step by step (one "unit" = one request x layer x kv head):
+ *   plan       [ZP-nl Methodologie §1, §3; ZP-ko 방법론 C]: destination blocks.
+ *   importance [ZP-ko 방법론 A, observation window]: softmax(q.k/sqrt(d)) of the
+ *              last w queries over all cached keys (causal inside the window),
+ *              averaged over the w queries and the G query heads of the group.
+ *   redundancy [ZP-nl Methodologie §5; ZP-ko 방법론 E, Lightning Redundancy
+ *              Score]: mean cosine similarity of a key to the other b-1 keys of
+ *              its own block.
+ *   score      importance - lambda * redundancy, for the C = T - w candidates.
+ *   select     [ZP-ko 방법론 A]: keep the (N-1)*b - w best candidates (score
+ *              descending, lower index first at equal score), then the window.
+ *   compact    [ZP-nl Methodologie §1]: kept rows, in original order, fill the
+ *              first N-1 blocks; block N is reserved for future decoding.
+ *   commit     [ZP-nl Methodologie §1, §3; PKV]: tables, lengths, refcounts,
+ *              released blocks back to the free stack.
+ *   decode     [PKV]: attention of one query per head over the block table.
+ *
+ * Every floating-point quantity is computed in double from the exact widening
+ * of the bf16 inputs.  No blocking, fusion or reordering beyond the definitions.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ZPO_OK 0
+#define ZPO_ERR_INVALID_ARG (-1)
+#define ZPO_ERR_OUT_OF_BLOCKS (-3)
+#define ZPO_ERR_DEVICE_CHECK (-4)
+
+/* ---------------------------------------------------------------- bf16 */
+
+double zpo_bf16_to_double(uint16_t h)
+{
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a double once, to nearest even, onto the bf16 grid (8 significant
+ * bits, fp32 exponent range).  Values beyond the largest finite bf16 become
+ * infinities; NaN stays NaN. */
+uint16_t zpo_double_to_bf16(double x)
+{
+    if (isnan(x))
+        return (uint16_t)0x7fc0;
+    double ax = fabs(x);
+    uint16_t sign = signbit(x) ? (uint16_t)0x8000 : (uint16_t)0;
+    if (ax == 0.0)
+        return sign;
+    int e;
+    frexp(ax, &e);                 /* ax = m * 2^e, m in [0.5, 1) */
+    int exp_unbiased = e - 1;      /* ax in [2^(e-1), 2^e) */
+    if (exp_unbiased < -126)
+        exp_unbiased = -126;       /* subnormal range: fixed spacing */
+    double spacing = ldexp(1.0, exp_unbiased - 7);
+    double q = rint(ax / spacing); /* default rounding mode: to nearest even */
+    double r = q * spacing;
+    if (r >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7f80);
+    float f = (float)r; /* exact: r lies on the bf16 grid */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | ((u >> 16) & 0x7fff));
+}
+
+/* Element-wise zpo_double_to_bf16 over an array. */
+void zpo_double_to_bf16_array(const double *x, uint16_t *out, long n)
+{
+    for (long i = 0; i < n; ++i)
+        out[i] = zpo_double_to_bf16(x[i]);
+}
+
+static double dot_bf16(const uint16_t *a, const uint16_t *b, int d)
+{
+    double s = 0.0;
+    for (int k = 0; k < d; ++k)
+        s += zpo_bf16_to_double(a[k]) * zpo_bf16_to_double(b[k]);
+    return s;
+}
+
+/* ---------------------------------------------------------- importance */
+
+/* Observation-window importance of the C = T - w candidates of one unit.
+ *   K: T rows of d bf16, in token order.
+ *   Q: G*w rows of d bf16; row g*w + i is query head g at window slot i, the
+ *      query of token C + i.
+ * Query i attends to keys 0 .. C+i (causal); its softmax uses exactly those.
+ * imp[j] = (1/(w*G)) * sum_{g,i} softmax_row(g,i)[j]   for j < C.
+ * [ZP-ko 방법론 A, observation window]; formula as adopted by this library. */
+void zpo_importance(const uint16_t *K, const uint16_t *Q, int T, int d, int w, int G,
+                    double *imp)
+{
+    int C = T - w;
+    double scale = 1.0 / sqrt((double)d);
+    double *logit = (double *)malloc(sizeof(double) * (size_t)T);
+    for (int j = 0; j < C; ++j)
+        imp[j] = 0.0;
+    for (int g = 0; g < G; ++g) {
+        for (int i = 0; i < w; ++i) {
+            const uint16_t *q = Q + (size_t)(g * w + i) * d;
+            int visible = C + i + 1;
+            double m = -INFINITY;
+            for (int j = 0; j < visible; ++j) {
+                logit[j] = dot_bf16(q, K + (size_t)j * d, d) * scale;
+                if (logit[j] > m)
+                    m = logit[j];
+            }
+            double S = 0.0;
+            for (int j = 0; j < visible; ++j)
+                S += exp(logit[j] - m);
+            for (int j = 0; j < C; ++j)
+                imp[j] += exp(logit[j] - m) / S;
+        }
+    }
+    for (int j = 0; j < C; ++j)
+        imp[j] /= (double)(w * G);
+    free(logit);
+}
+
+/* ---------------------------------------------------------- redundancy */
+
+/* Lightning Redundancy Score [ZP-nl Methodologie §5; ZP-ko 방법론 E]: only the
+ * b keys of the same block are compared, O(N*b^2) per unit.
+ * red[j] = (1/(b-1)) * sum_{k in block(j), k != j} cos(K_j, K_k), where a
+ * zero-norm key has cosine 0 with every key.  All T keys get a value; window
+ * keys count as "other keys" of their block. */
+void zpo_redundancy(const uint16_t *K, int T, int d, int b, double *red)
+{
+    double *norm = (double *)malloc(sizeof(double) * (size_t)b);
+    for (int base = 0; base < T; base += b) {
+        for (int j = 0; j < b; ++j) {
+            const uint16_t *kj = K + (size_t)(base + j) * d;
+            norm[j] = sqrt(dot_bf16(kj, kj, d));
+        }
+        for (int j = 0; j < b; ++j) {
+            double sum = 0.0;
+            for (int k = 0; k < b; ++k) {
+                if (k == j)
+                    continue;
+                double c = 0.0;
+                if (norm[j] > 0.0 && norm[k] > 0.0)
+                    c = dot_bf16(K + (size_t)(base + j) * d, K + (size_t)(base + k) * d, d) /
+                        (norm[j] * norm[k]);
+                sum += c;
+            }
+            red[base + j] = sum / (double)(b - 1);
+        }
+    }
+    free(norm);
+}
+
+/* score[j] = imp[j] - lambda * red[j] for the C candidates. */
+void zpo_unit_scores(const uint16_t *K, const uint16_t *Q, int T, int d, int b, int w, int G,
+                     double lambda, double *imp, double *red, double *score)
+{
+    int C = T - w;
+    zpo_importance(K, Q, T, d, w, G, imp);
+    zpo_redundancy(K, T, d, b, red);
+    for (int j = 0; j < C; ++j)
+        score[j] = imp[j] - lambda * red[j];
+}
+
+/* -------------------------------------------------------------- select */
+
+/* Candidate order: higher score first; at equal score the lower index first. */
+static int better(const double *score, int32_t a, int32_t b)
+{
+    if (score[a] > score[b])
+        return 1;
+    if (score[a] < score[b])
+        return 0;
+    return a < b;
+}
+
+static void merge_sort(int32_t *idx, int32_t *tmp, int n, const double *score)
+{
+    if (n < 2)
+        return;
+    int h = n / 2;
+    merge_sort(idx, tmp, h, score);
+    merge_sort(idx + h, tmp, n - h, score);
+    int i = 0, j = h, o = 0;
+    while (i < h && j < n)
+        tmp[o++] = better(score, idx[j], idx[i]) ? idx[j++] : idx[i++];
+    while (i < h)
+        tmp[o++] = idx[i++];
+    while (j < n)
+        tmp[o++] = idx[j++];
+    memcpy(idx, tmp, sizeof(int32_t) * (size_t)n);
+}
+
+/* Token-wise eviction for one unit [ZP-ko 방법론 A]: of the C candidates keep
+ * the n_keep best in the candidate order, then append the window C..T-1.
+ * kept[] receives n_keep + w indices in ascending (original) order.
+ * Evicting the lowest-score token one at a time with fixed scores removes the
+ * same set, so a sort is the whole selection. */
+void zpo_select(const double *score, int C, int w, int n_keep, int32_t *kept)
+{
+    int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (size_t)(C > 0 ? C : 1));
+    int32_t *tmp = (int32_t *)malloc(sizeof(int32_t) * (size_t)(C > 0 ? C : 1));
+    unsigned char *keep = (unsigned char *)calloc((size_t)(C > 0 ? C : 1), 1);
+    for (int j = 0; j < C; ++j)
+        idx[j] = j;
+    merge_sort(idx, tmp, C, score);
+    for (int r = 0; r < n_keep; ++r)
+        keep[idx[r]] = 1;
+    int o = 0;
+    for (int j = 0; j < C; ++j)
+        if (keep[j])
+            kept[o++] = j;
+    for (int i = 0; i < w; ++i)
+        kept[o++] = C + i;
+    free(idx);
+    free(tmp);
+    free(keep);
+}
+
+/* ---------------------------------------------------------------- plan */
+
+/* Destination blocks for the compressing requests [ZP-nl Methodologie §1, §3;
+ * ZP-ko 방법론 C].  Reading adopted: with the refcounts as they are at call
+ * start, block p of a request is rewritten in place when its refcount is 1 and
+ * compressed into a fresh target block from the free stack when it is > 1 (a
+ * shared block is never rewritten).  The reserved last block is kept when its
+ * refcount is 1, else replaced by a fresh block.  Targets are popped from the
+ * top of the free stack in (request, block) order.
+ *
+ * tables: rows of `stride` int32; request r uses row req_idx[r] (or r when
+ * req_idx is NULL); lengths indexed the same way.  dst_table[r*N + p] receives
+ * the destination block of (r, p).  Nothing is modified; returns a status and
+ * the number of popped blocks in *n_pops. */
+int zpo_plan(const int32_t *tables, int stride, const int32_t *lengths, const int32_t *req_idx,
+             int R, int num_rows, int N, int b, int num_blocks, const int32_t *refcount,
+             const int32_t *free_ids, int free_count, int32_t *dst_table, int *n_pops)
+{
+    *n_pops = 0;
+    if (R < 0 || N < 2 || b < 2 || stride < N)
+        return ZPO_ERR_INVALID_ARG;
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        if (row < 0 || row >= num_rows)
+            return ZPO_ERR_INVALID_ARG;
+        for (int r2 = 0; r2 < r; ++r2)
+            if ((req_idx ? req_idx[r2] : r2) == row)
+                return ZPO_ERR_INVALID_ARG;
+        if (lengths[row] != N * b)
+            return ZPO_ERR_INVALID_ARG;
+        for (int p = 0; p < N; ++p) {
+            int32_t blk = tables[(size_t)row * stride + p];
+            if (blk < 0 || blk >= num_blocks || refcount[blk] < 1)
+                return ZPO_ERR_INVALID_ARG;
+        }
+    }
+    int pops = 0;
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        for (int p = 0; p < N; ++p) {
+            int32_t blk = tables[(size_t)row * stride + p];
+            if (refcount[blk] > 1) {
+                if (pops >= free_count)
+                    return ZPO_ERR_OUT_OF_BLOCKS;
+                int32_t t = free_ids[free_count - 1 - pops];
+                if (t < 0 || t >= num_blocks || refcount[t] != 0)
+                    return ZPO_ERR_DEVICE_CHECK;
+                dst_table[(size_t)r * N + p] = t;
+                ++pops;
+            } else {
+                dst_table[(size_t)r * N + p] = blk;
+            }
+        }
+    }
+    *n_pops = pops;
+    return ZPO_OK;
+}
+
+/* Applies a plan [ZP-nl Methodologie §1, §3; PKV]: every replaced block loses
+ * one reference per holder, in (request, block) order; a block whose count
+ * reaches zero is pushed onto the free stack at that moment (after the pops).
+ * Targets get refcount 1, rows get the destination table, lengths become
+ * (N-1)*b.  Returns the new free count. */
+int zpo_commit(int32_t *tables, int stride, int32_t *lengths, const int32_t *req_idx, int R,
+               int N, int b, int32_t *refcount, int32_t *free_ids, int free_count,
+               const int32_t *dst_table, int n_pops)
+{
+    int top = free_count - n_pops;
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        for (int p = 0; p < N; ++p) {
+            int32_t src = tables[(size_t)row * stride + p];
+            int32_t dst = dst_table[(size_t)r * N + p];
+            if (dst != src) {
+                refcount[src] -= 1;
+                if (refcount[src] == 0)
+                    free_ids[top++] = src;
+                refcount[dst] = 1;
+                tables[(size_t)row * stride + p] = dst;
+            }
+        }
+        lengths[row] = (N - 1) * b;
+    }
+    return top;
+}
+
+/* ------------------------------------------------------------ compress */
+
+typedef struct {
+    int L, Hkv, Hq, d, b, num_blocks;
+    const uint16_t *const *kpool; /* [L] -> [num_blocks][Hkv][b][d] */
+    const uint16_t *const *vpool;
+    uint16_t *const *kout; /* [L] pools written with the compacted rows */
+    uint16_t *const *vout;
+    const int32_t *tables;
+    int stride;
+    const int32_t *req_idx;
+    int R, N, w;
+    double lambda;
+    const uint16_t *window_q; /* [L][R][Hq][w][d] */
+    const int32_t *dst_table;
+    double *scores_out; /* [L][R][Hkv][T] or NULL */
+    int32_t *kept_out;  /* [L][R][Hkv][(N-1)b] or NULL */
+    int next_unit;
+    pthread_mutex_t mu;
+} compress_job;
+
+static size_t slab_off(const compress_job *J, int32_t blk, int h)
+{
+    return ((size_t)blk * J->Hkv + h) * (size_t)J->b * J->d;
+}
+
+static void compress_unit(compress_job *J, int unit)
+{
+    int h = unit % J->Hkv;
+    int l = (unit / J->Hkv) % J->L;
+    int r = unit / (J->Hkv * J->L);
+    int row = J->req_idx ? J->req_idx[r] : r;
+    int b = J->b, d = J->d, N = J->N, w = J->w;
+    int T = N * b, C = T - w, G = J->Hq / J->Hkv;
+    int n_keep = (N - 1) * b - w;
+    const int32_t *src_row = J->tables + (size_t)row * J->stride;
+    const int32_t *dst_row = J->dst_table + (size_t)r * N;
+
+    /* gather the unit's K and V rows in token order */
+    uint16_t *K = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)T * d);
+    uint16_t *V = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)T * d);
+    for (int t = 0; t < T; ++t) {
+        size_t off = slab_off(J, src_row[t / b], h) + (size_t)(t % b) * d;
+        memcpy(K + (size_t)t * d, J->kpool[l] + off, sizeof(uint16_t) * d);
+        memcpy(V + (size_t)t * d, J->vpool[l] + off, sizeof(uint16_t) * d);
+    }
+    const uint16_t *Q = J->window_q + (((size_t)l * J->R + r) * J->Hq + (size_t)h * G) * w * d;
+    double *imp = (double *)malloc(sizeof(double) * (size_t)T);
+    double *red = (double *)malloc(sizeof(double) * (size_t)T);
+    double *score = (double *)malloc(sizeof(double) * (size_t)T);
+    int32_t *kept = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N - 1) * b);
+    zpo_unit_scores(K, Q, T, d, b, w, G, J->lambda, imp, red, score);
+    zpo_select(score, C, w, n_keep, kept);
+
+    /* compaction: destination token j <- source token kept[j] */
+    for (int j = 0; j < (N - 1) * b; ++j) {
+        size_t off = slab_off(J, dst_row[j / b], h) + (size_t)(j % b) * d;
+        memcpy(J->kout[l] + off, K + (size_t)kept[j] * d, sizeof(uint16_t) * d);
+        memcpy(J->vout[l] + off, V + (size_t)kept[j] * d, sizeof(uint16_t) * d);
+    }
+    size_t u = ((size_t)l * J->R + r) * J->Hkv + h;
+    if (J->scores_out) {
+        for (int j = 0; j < C; ++j)
+            J->scores_out[u * T + j] = score[j];
+        for (int j = C; j < T; ++j)
+            J->scores_out[u * T + j] = INFINITY;
+    }
+    if (J->kept_out)
+        memcpy(J->kept_out + u * (size_t)(N - 1) * b, kept, sizeof(int32_t) * (size_t)(N - 1) * b);
+    free(K);
+    free(V);
+    free(imp);
+    free(red);
+    free(score);
+    free(kept);
+}
+
+static void *compress_worker(void *arg)
+{
+    compress_job *J = (compress_job *)arg;
+    int units = J->R * J->L * J->Hkv;
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        int u = J->next_unit++;
+        pthread_mutex_unlock(&J->mu);
+        if (u >= units)
+            break;
+        compress_unit(J, u);
+    }
+    return NULL;
+}
+
+/* Whole compression of R requests over all L layers and Hkv heads.
+ * kpool/vpool hold the input bytes and are only read; kout/vout receive the
+ * compacted rows (they may be the same arrays as kpool/vpool only when no
+ * unit reads a block another unit writes, which holds for valid caches since
+ * shared blocks are never written; pass copies to be safe).  The integer state
+ * (tables, lengths, refcount, free stack) is updated in place, or left as it
+ * was when the status is not OK.  Units are spread over `nthreads` threads. */
+int zpo_compress(int L, int Hkv, int Hq, int d, int b, int num_blocks,
+                 const uint16_t *const *kpool, const uint16_t *const *vpool,
+                 uint16_t *const *kout, uint16_t *const *vout,
+                 int32_t *tables, int stride, int32_t *lengths, const int32_t *req_idx, int R,
+                 int num_rows, const uint16_t *window_q, int N, int w, double lambda,
+                 int32_t *free_ids, int32_t *free_count, int32_t *refcount,
+                 double *scores_out, int32_t *kept_out, int nthreads)
+{
+    if (L < 1 || Hkv < 1 || Hq < Hkv || Hq % Hkv || d < 1 || w < 1 || w > b)
+        return ZPO_ERR_INVALID_ARG;
+    int32_t *dst = (int32_t *)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1) * N);
+    int pops = 0;
+    int st = zpo_plan(tables, stride, lengths, req_idx, R, num_rows, N, b, num_blocks, refcount,
+                      free_ids, *free_count, dst, &pops);
+    if (st != ZPO_OK) {
+        free(dst);
+        return st;
+    }
+    compress_job J;
+    J.L = L; J.Hkv = Hkv; J.Hq = Hq; J.d = d; J.b = b; J.num_blocks = num_blocks;
+    J.kpool = kpool; J.vpool = vpool; J.kout = kout; J.vout = vout;
+    J.tables = tables; J.stride = stride; J.req_idx = req_idx;
+    J.R = R; J.N = N; J.w = w; J.lambda = lambda; J.window_q = window_q;
+    J.dst_table = dst; J.scores_out = scores_out; J.kept_out = kept_out;
+    J.next_unit = 0;
+    pthread_mutex_init(&J.mu, NULL);
+    if (nthreads < 1)
+        nthreads = 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    for (int i = 0; i < nthreads; ++i)
+        pthread_create(&th[i], NULL, compress_worker, &J);
+    for (int i = 0; i < nthreads; ++i)
+        pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.mu);
+    *free_count = zpo_commit(tables, stride, lengths, req_idx, R, N, b, refcount, free_ids,
+                             *free_count, dst, pops);
+    free(dst);
+    return ZPO_OK;
+}
+
+/* -------------------------------------------------------------- decode */
+
+/* Paged decode attention [PKV]: for request r and query head hq (kv head
+ * hq / (Hq/Hkv)), o = sum_t softmax_t(scale * q.k_t) v_t over the first
+ * lengths[r] tokens, token t living in block tables[r*stride + t/b], slot t%b.
+ * out64 (nullable) gets the exact double result, out_bf16 its single RNE
+ * rounding.  A zero length gives a zero output. */
+int zpo_decode_attn(const uint16_t *q, const uint16_t *kpool, const uint16_t *vpool,
+                    const int32_t *tables, int stride, const int32_t *lengths, int R, int Hq,
+                    int Hkv, int d, int b, int num_blocks, double scale, double *out64,
+                    uint16_t *out_bf16)
+{
+    if (Hq % Hkv)
+        return ZPO_ERR_INVALID_ARG;
+    int G = Hq / Hkv;
+    for (int r = 0; r < R; ++r) {
+        int len = lengths[r];
+        if (len < 0 || len > stride * b)
+            return ZPO_ERR_INVALID_ARG;
+        for (int p = 0; p < (len + b - 1) / b; ++p) {
+            int32_t blk = tables[(size_t)r * stride + p];
+            if (blk < 0 || blk >= num_blocks)
+                return ZPO_ERR_INVALID_ARG;
+        }
+    }
+    int maxlen = 1;
+    for (int r = 0; r < R; ++r)
+        if (lengths[r] > maxlen)
+            maxlen = lengths[r];
+    double *logit = (double *)malloc(sizeof(double) * (size_t)maxlen);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)d);
+    for (int r = 0; r < R; ++r) {
+        int len = lengths[r];
+        for (int hq = 0; hq < Hq; ++hq) {
+            int h = hq / G;
+            const uint16_t *qv = q + ((size_t)r * Hq + hq) * d;
+            double m = -INFINITY;
+            for (int t = 0; t < len; ++t) {
+                int32_t blk = tables[(size_t)r * stride + t / b];
+                const uint16_t *k = kpool + (((size_t)blk * Hkv + h) * b + t % b) * d;
+                logit[t] = scale * dot_bf16(qv, k, d);
+                if (logit[t] > m)
+                    m = logit[t];
+            }
+            double S = 0.0;
+            for (int t = 0; t < len; ++t)
+                S += exp(logit[t] - m);
+            for (int k = 0; k < d; ++k)
+                acc[k] = 0.0;
+            for (int t = 0; t < len; ++t) {
+                int32_t blk = tables[(size_t)r * stride + t / b];
+                const uint16_t *v = vpool + (((size_t)blk * Hkv + h) * b + t % b) * d;
+                double p = exp(logit[t] - m) / S;
+                for (int k = 0; k < d; ++k)
+                    acc[k] += p * zpo_bf16_to_double(v[k]);
+            }
+            for (int k = 0; k < d; ++k) {
+                size_t o = ((size_t)r * Hq + hq) * d + k;
+                if (out64)
+                    out64[o] = acc[k];
+                if (out_bf16)
+                    out_bf16[o] = zpo_double_to_bf16(acc[k]);
+            }
+        }
+    }
+    free(logit);
+    free(acc);
+    return ZPO_OK;
+}

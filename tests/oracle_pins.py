@@ -1,0 +1,584 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each ``pin_*`` function takes a loaded oracle (``oracle.Oracle``) and raises
+AssertionError when the oracle disagrees with a closed form, a brute-force
+enumeration, an independent library routine (torch fp64), a hand-worked
+value, or an invariant the pages state.  ``test_oracle_pins.py`` runs them on
+the real oracle; ``test_oracle_mutants.py`` runs them on copies of the oracle
+with one planted mistake each and requires that some pin fails.
+
+Sources: "Zipage: Maintain High Request Concurrency for LLM Reasoning through
+Compressed PagedAttention" (gist.science summaries: Dutch "Methodologie" §1,
+§3, §5; Korean "방법론" A, C, E) and "Paged KV cache and continuous batching
+for LLMs" ("How it works").
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ------------------------------------------------------------------ helpers
+
+def bf16(x) -> np.ndarray:
+    """uint16 bf16 bit patterns of float data (rounded by torch)."""
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def widen(bits) -> np.ndarray:
+    bits = np.asarray(bits, dtype=np.uint16)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def rng(seed):
+    return np.random.default_rng(seed)
+
+
+def close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    err = np.max(np.abs(a - b)) if a.size else 0.0
+    assert np.all(np.isfinite(a)), f"{what}: non-finite values"
+    assert err <= tol, f"{what}: max abs err {err:.3e} > {tol:.1e}"
+
+
+def torch_importance(K, Q, w, G):
+    """Observation-window importance with torch's fp64 softmax (independent)."""
+    Kd = torch.tensor(widen(K))
+    Qd = torch.tensor(widen(Q))
+    T, d = Kd.shape
+    C = T - w
+    logits = (Qd @ Kd.T) / math.sqrt(d)            # [G*w, T]
+    rows = torch.arange(G * w) % w                  # window slot of each row
+    mask = torch.arange(T)[None, :] > (C + rows)[:, None]
+    logits = logits.masked_fill(mask, float("-inf"))
+    P = torch.softmax(logits, dim=-1)
+    return P[:, :C].mean(dim=0).numpy()
+
+
+def torch_redundancy(K, b):
+    Kd = torch.tensor(widen(K))
+    T, d = Kd.shape
+    out = np.zeros(T)
+    for base in range(0, T, b):
+        blk = Kd[base:base + b]
+        cos = torch.nn.functional.cosine_similarity(blk[:, None, :], blk[None, :, :], dim=-1,
+                                                    eps=1e-300)
+        norms = blk.norm(dim=-1)
+        zero = norms == 0
+        cos[zero, :] = 0.0
+        cos[:, zero] = 0.0
+        cos.fill_diagonal_(0.0)
+        out[base:base + b] = (cos.sum(dim=1) / (b - 1)).numpy()
+    return out
+
+
+# --------------------------------------------------------------- importance
+
+def pin_importance_uniform_zero_queries(orc):
+    """q = 0: every visible logit is 0, so window row i spreads 1/(C+i+1) over
+    keys 0..C+i and imp_j = (1/w) sum_i 1/(C+i+1) for every candidate."""
+    T, d, w, G = 48, 16, 4, 2
+    C = T - w
+    K = bf16(rng(1).standard_normal((T, d)))
+    Q = np.zeros((G * w, d), dtype=np.uint16)
+    imp = orc.importance(K, Q, w, G)
+    expect = sum(1.0 / (C + i + 1) for i in range(w)) / w
+    close(imp, np.full(C, expect), 1e-15, "importance with q = 0")
+
+
+def pin_importance_equal_keys(orc):
+    """All keys equal: logits are equal on each row; same closed form."""
+    T, d, w, G = 40, 8, 5, 3
+    C = T - w
+    row = rng(2).standard_normal(d)
+    K = bf16(np.tile(row, (T, 1)))
+    Q = bf16(rng(3).standard_normal((G * w, d)))
+    imp = orc.importance(K, Q, w, G)
+    expect = sum(1.0 / (C + i + 1) for i in range(w)) / w
+    close(imp, np.full(C, expect), 1e-14, "importance with equal keys")
+
+
+def pin_importance_dominant_key(orc):
+    """One key aligned with every query and 8x longer: its logit exceeds the
+    others by ~32, so it takes all of the probability mass (imp -> 1)."""
+    T, d, w, G = 64, 16, 4, 2
+    u = np.where(rng(4).standard_normal(d) > 0, 1.0, -1.0)
+    K = 0.01 * rng(5).standard_normal((T, d))
+    jstar = 17
+    K[jstar] = 8.0 * u
+    Q = np.tile(u, (G * w, 1))
+    imp = orc.importance(bf16(K), bf16(Q), w, G)
+    assert abs(imp[jstar] - 1.0) < 1e-11, imp[jstar]
+    others = np.delete(imp, jstar)
+    assert np.all(others < 1e-12) and np.all(others >= 0.0)
+
+
+def pin_importance_torch_softmax(orc):
+    """Random keys and queries against torch's fp64 softmax with the causal
+    window mask (query i of the window sees keys up to C+i)."""
+    for seed, (T, d, w, G) in enumerate([(64, 16, 8, 4), (48, 32, 5, 1), (33, 8, 3, 2)]):
+        K = bf16(2.0 * rng(10 + seed).standard_normal((T, d)))
+        Q = bf16(2.0 * rng(20 + seed).standard_normal((G * w, d)))
+        close(orc.importance(K, Q, w, G), torch_importance(K, Q, w, G), 1e-13,
+              f"importance vs torch softmax {T, d, w, G}")
+
+
+# --------------------------------------------------------------- redundancy
+
+def pin_redundancy_identical_keys(orc):
+    b, d = 8, 16
+    K = bf16(np.tile(rng(6).standard_normal(d), (3 * b, 1)))
+    close(orc.redundancy(K, b), np.ones(3 * b), 1e-14, "redundancy of identical keys")
+
+
+def pin_redundancy_orthogonal_keys(orc):
+    b, d = 8, 16
+    K = np.zeros((b, d))
+    for j in range(b):
+        K[j, (3 * j) % d] = 1.0 + j
+    close(orc.redundancy(bf16(K), b), np.zeros(b), 1e-15, "redundancy of orthogonal keys")
+
+
+def pin_redundancy_opposite_halves(orc):
+    """b/2 copies of u and b/2 of -u: each key has b/2-1 cosines of +1 and
+    b/2 of -1, so red = -1/(b-1)."""
+    b, d = 16, 8
+    u = rng(7).standard_normal(d)
+    K = np.vstack([np.tile(u, (b // 2, 1)), np.tile(-u, (b // 2, 1))])
+    close(orc.redundancy(bf16(K), b), np.full(b, -1.0 / (b - 1)), 1e-14,
+          "redundancy of opposite halves")
+
+
+def pin_redundancy_zero_key(orc):
+    """A zero key has cosine 0 with everything: its own red is 0, and each
+    other (identical) key sees b-2 cosines of 1, so red = (b-2)/(b-1)."""
+    b, d = 8, 4
+    K = np.tile(rng(8).standard_normal(d), (b, 1))
+    K[3] = 0.0
+    red = orc.redundancy(bf16(K), b)
+    expect = np.full(b, (b - 2) / (b - 1))
+    expect[3] = 0.0
+    close(red, expect, 1e-14, "redundancy with a zero key")
+
+
+def pin_redundancy_handworked(orc):
+    with open(os.path.join(GOLDEN, "lrs_handworked.json")) as f:
+        g = json.load(f)
+    red = orc.redundancy(bf16(np.array(g["keys"], dtype=np.float64)), g["b"])
+    close(red, g["red"], 1e-14, "hand-worked redundancy")
+
+
+def pin_redundancy_torch_cosine(orc):
+    for seed, (T, b, d) in enumerate([(64, 16, 32), (48, 4, 8), (30, 6, 5)]):
+        K = bf16(rng(30 + seed).standard_normal((T, d)))
+        close(orc.redundancy(K, b), torch_redundancy(K, b), 1e-13,
+              f"redundancy vs torch cosine {T, b, d}")
+
+
+def pin_redundancy_block_locality(orc):
+    """Only keys of the same block are compared: changing block 1 leaves the
+    values of block 0 unchanged."""
+    b, d = 8, 8
+    K = rng(40).standard_normal((3 * b, d))
+    r0 = orc.redundancy(bf16(K), b)
+    K2 = K.copy()
+    K2[b:2 * b] = rng(41).standard_normal((b, d))
+    r1 = orc.redundancy(bf16(K2), b)
+    close(r0[:b], r1[:b], 0.0, "block 0 redundancy after changing block 1")
+    close(r0[2 * b:], r1[2 * b:], 0.0, "block 2 redundancy after changing block 1")
+
+
+# -------------------------------------------------------------------- score
+
+def pin_score_lambda_zero_is_importance(orc):
+    T, d, b, w, G = 64, 16, 8, 4, 2
+    K = bf16(rng(50).standard_normal((T, d)))
+    Q = bf16(rng(51).standard_normal((G * w, d)))
+    imp, red, score = orc.unit_scores(K, Q, b, w, G, 0.0)
+    close(score, torch_importance(K, Q, w, G), 1e-13, "score at lambda 0")
+
+
+def pin_score_large_lambda_evicts_most_redundant(orc):
+    """As lambda grows the importance term becomes negligible: the b evicted
+    candidates are the b most redundant ones."""
+    N, b, d, w, G = 6, 4, 8, 2, 2
+    T = N * b
+    K = bf16(rng(52).standard_normal((T, d)))
+    Q = bf16(rng(53).standard_normal((G * w, d)))
+    _, red, score = orc.unit_scores(K, Q, b, w, G, 1e6)
+    C = T - w
+    kept = orc.select(score, w, C - b)
+    evicted = sorted(set(range(C)) - set(kept.tolist()))
+    most = sorted(np.argsort(-red[:C], kind="stable")[:b].tolist())
+    assert evicted == most, (evicted, most)
+    close(score, torch_importance(K, Q, w, G) - 1e6 * torch_redundancy(K, b)[:C], 1e-7,
+          "score at lambda 1e6")
+
+
+def pin_score_mixture(orc):
+    """score = imp - lambda * red against the torch versions of both terms."""
+    T, d, b, w, G = 96, 16, 16, 8, 4
+    K = bf16(rng(54).standard_normal((T, d)))
+    Q = bf16(rng(55).standard_normal((G * w, d)))
+    _, _, score = orc.unit_scores(K, Q, b, w, G, 0.5)
+    C = T - w
+    close(score, torch_importance(K, Q, w, G) - 0.5 * torch_redundancy(K, b)[:C], 1e-13,
+          "score vs torch terms")
+
+
+# ------------------------------------------------------------------- select
+
+def _brute_force_keep(score, n_keep):
+    """Among all size-n_keep subsets, the ones with the largest total score;
+    of those the lexicographically smallest sorted index tuple."""
+    best = None
+    for sub in itertools.combinations(range(len(score)), n_keep):
+        s = sum(score[i] for i in sub)
+        key = (-s, sub)
+        if best is None or key < best:
+            best = key
+    return list(best[1])
+
+
+def pin_select_brute_force(orc):
+    """Integer scores with deliberate ties, every subset enumerated."""
+    b, w = 4, 3
+    for seed, C in enumerate([12, 16, 20]):
+        score = rng(60 + seed).integers(0, 5, size=C).astype(np.float64)
+        kept = orc.select(score, w, C - b)
+        assert kept[:C - b].tolist() == _brute_force_keep(score.tolist(), C - b), seed
+        assert kept[C - b:].tolist() == list(range(C, C + w))
+
+
+def pin_select_all_equal(orc):
+    """All scores equal: the higher indices lose the tie, so the b highest
+    candidates are evicted."""
+    C, b, w = 40, 8, 4
+    kept = orc.select(np.zeros(C), w, C - b)
+    assert kept.tolist() == list(range(C - b)) + list(range(C, C + w))
+
+
+def pin_select_invariants(orc):
+    """Window kept, exactly (N-1)*b entries, strictly increasing."""
+    N, b, w = 8, 16, 8
+    C = N * b - w
+    score = rng(61).standard_normal(C)
+    kept = orc.select(score, w, (N - 1) * b - w)
+    assert kept.size == (N - 1) * b
+    assert np.all(np.diff(kept) > 0)
+    assert kept[-w:].tolist() == list(range(C, C + w))
+    evicted = sorted(set(range(C)) - set(kept.tolist()))
+    assert evicted == sorted(np.argsort(score)[:b].tolist())
+
+
+# ------------------------------------------------------------ block accounting
+
+def _state(tables, refcount, free_ids, N, b):
+    tables = np.asarray(tables, dtype=np.int32)
+    R = tables.shape[0]
+    return dict(tables=tables.copy(), lengths=np.full(R, N * b, dtype=np.int32),
+                refcount=np.asarray(refcount, dtype=np.int32).copy(),
+                free_ids=np.asarray(free_ids, dtype=np.int32).copy())
+
+
+def _apply(orc, s, free_count, N, b, num_blocks, req_idx=None):
+    st, dst, pops = orc.plan(s["tables"], s["lengths"], s["refcount"], s["free_ids"],
+                             free_count, N, b, num_blocks, req_idx=req_idx)
+    if st != 0:
+        return st, free_count, dst
+    fc = orc.commit(s["tables"], s["lengths"], s["refcount"], s["free_ids"], free_count, dst,
+                    pops, N, b, req_idx=req_idx)
+    return st, fc, dst
+
+
+def pin_blocks_no_sharing(orc):
+    N, b = 4, 4
+    tables = [[0, 1, 2, 3], [4, 5, 6, 7]]
+    rc = [1] * 8 + [0] * 4
+    free = [8, 9, 10, 11]
+    s = _state(tables, rc, free, N, b)
+    st, fc, dst = _apply(orc, s, 4, N, b, 12)
+    assert st == 0 and fc == 4
+    assert s["tables"].tolist() == tables and s["refcount"].tolist() == rc
+    assert s["lengths"].tolist() == [(N - 1) * b] * 2
+
+
+def pin_blocks_shared_prefix(orc):
+    """Block 0 shared by both requests (refcount 2): both compress into fresh
+    targets popped from the top of the stack (request 0 first); block 0 drops
+    to refcount 0 on its last holder and is pushed after the pops."""
+    N, b = 3, 4
+    tables = [[0, 1, 2], [0, 3, 4]]
+    rc = [2, 1, 1, 1, 1, 0, 0, 0]
+    free = [5, 6, 7, -1, -1, -1, -1, -1]
+    s = _state(tables, rc, free, N, b)
+    st, fc, dst = _apply(orc, s, 3, N, b, 8)
+    assert st == 0
+    assert dst.tolist() == [[7, 1, 2], [6, 3, 4]]
+    assert s["tables"].tolist() == [[7, 1, 2], [6, 3, 4]]
+    assert s["refcount"].tolist() == [0, 1, 1, 1, 1, 0, 1, 1]
+    assert fc == 2 and s["free_ids"][:fc].tolist() == [5, 0]
+
+
+def pin_blocks_partial_holders(orc):
+    """Refcount 3 with only two compressing holders: the block keeps one
+    reference and is not freed; a shared reserved block is replaced too."""
+    N, b = 2, 4
+    tables = [[0, 9], [0, 9], [0, 2]]
+    rc = [3, 0, 1, 0, 0, 0, 0, 0, 0, 2]
+    free = [1, 3, 4, 5, 6, 7, 8, -1, -1, -1]
+    s = _state(tables, rc, free, N, b)
+    st, fc, dst = _apply(orc, s, 7, N, b, 10, req_idx=np.array([0, 1], dtype=np.int32))
+    assert st == 0
+    assert dst.tolist() == [[8, 7], [6, 5]]
+    assert s["tables"].tolist() == [[8, 7], [6, 5], [0, 2]]
+    assert s["refcount"][0] == 1 and s["refcount"][9] == 0
+    assert fc == 7 - 4 + 1 and s["free_ids"][:fc].tolist() == [1, 3, 4, 9]
+
+
+def pin_blocks_conservation(orc):
+    """On a random valid cache: free + blocks in use = capacity, the sum of
+    refcounts equals the number of table references, targets are unique per
+    request, and shared-at-start blocks are never destinations."""
+    g = rng(70)
+    N, b, R, group, pb = 6, 4, 12, 3, 2
+    num_blocks = 200
+    perm = g.permutation(num_blocks).astype(np.int32)
+    tables = np.zeros((R, N), dtype=np.int32)
+    rc = np.zeros(num_blocks, dtype=np.int32)
+    nxt = 0
+    for gi in range(R // group):
+        shared = perm[nxt:nxt + pb]
+        nxt += pb
+        for r in range(gi * group, (gi + 1) * group):
+            tables[r, :pb] = shared
+            tables[r, pb:] = perm[nxt:nxt + N - pb]
+            nxt += N - pb
+    for x in tables.reshape(-1):
+        rc[x] += 1
+    free = np.full(num_blocks, -1, dtype=np.int32)
+    nfree = num_blocks - nxt
+    free[:nfree] = perm[nxt:]
+    shared_at_start = set(np.nonzero(rc > 1)[0].tolist())
+    req = np.array([0, 1, 2, 4, 7, 9, 10], dtype=np.int32)
+    s = _state(tables, rc, free, N, b)
+    st, fc, dst = _apply(orc, s, nfree, N, b, num_blocks, req_idx=req)
+    assert st == 0
+    assert fc + int(np.count_nonzero(s["refcount"] >= 1)) == num_blocks
+    assert int(s["refcount"].sum()) == s["tables"].size
+    for r in range(dst.shape[0]):
+        assert len(set(dst[r].tolist())) == N
+        assert not (set(dst[r].tolist()) & shared_at_start)
+    assert len(set(s["free_ids"][:fc].tolist())) == fc
+    assert np.all(s["refcount"][s["free_ids"][:fc]] == 0)
+
+
+def pin_blocks_out_of_blocks(orc):
+    """Too few free blocks: status 'out of blocks' and nothing modified."""
+    N, b = 2, 4
+    tables = [[0, 1], [0, 2]]
+    rc = [2, 1, 1, 0]
+    free = [3, -1, -1, -1]
+    s = _state(tables, rc, free, N, b)
+    before = {k: v.copy() for k, v in s.items()}
+    st, fc, _ = _apply(orc, s, 1, N, b, 4)
+    assert st == -3 and fc == 1
+    for k in s:
+        assert np.array_equal(s[k], before[k]), k
+
+
+def pin_blocks_invalid(orc):
+    """A length other than N*b (the trigger needs a full last block) or a
+    block id out of range is rejected."""
+    N, b = 2, 4
+    s = _state([[0, 1]], [1, 1, 0], [2, -1, -1], N, b)
+    s["lengths"][0] = N * b - 1
+    assert _apply(orc, s, 1, N, b, 3)[0] == -1
+    s = _state([[0, 5]], [1, 1, 0], [2, -1, -1], N, b)
+    assert _apply(orc, s, 1, N, b, 3)[0] == -1
+
+
+# ------------------------------------------------------------ whole compress
+
+def _tiny_cache(seed, N=6, b=4, d=8, Hkv=2, G=2, L=2, R=3, share=True, w=3):
+    """A tiny random cache: request 0 and 1 share their first block."""
+    g = rng(seed)
+    num_blocks = R * N + 8
+    perm = g.permutation(num_blocks).astype(np.int32)
+    tables = np.zeros((R, N), dtype=np.int32)
+    nxt = 0
+    for r in range(R):
+        tables[r] = perm[nxt:nxt + N]
+        nxt += N
+    if share:
+        tables[1, 0] = tables[0, 0]
+        nxt_free = perm[nxt:]
+        nxt_free = np.concatenate([nxt_free, [perm[N]]])  # request 1's old block 0 is free
+    else:
+        nxt_free = perm[nxt:]
+    rc = np.zeros(num_blocks, dtype=np.int32)
+    for x in tables.reshape(-1):
+        rc[x] += 1
+    free = np.full(num_blocks, -1, dtype=np.int32)
+    free[:len(nxt_free)] = nxt_free
+    kp = [bf16(g.standard_normal((num_blocks, Hkv, b, d))) for _ in range(L)]
+    vp = [bf16(g.standard_normal((num_blocks, Hkv, b, d))) for _ in range(L)]
+    wq = bf16(g.standard_normal((L, R, Hkv * G, w, d)))
+    return dict(kp=kp, vp=vp, tables=tables, lengths=np.full(R, N * b, dtype=np.int32),
+                rc=rc, free=free, free_count=len(nxt_free), wq=wq, N=N, b=b, d=d, Hkv=Hkv,
+                G=G, L=L, R=R, w=w)
+
+
+def _gather(pool, row, h, b):
+    return np.concatenate([pool[blk, h] for blk in row], axis=0)
+
+
+def pin_compress_rows_and_shared_blocks(orc):
+    """Every compacted row byte-equals the input row at its kept index; the
+    shared block is byte-identical afterwards; (N-1)*b rows per head; the
+    kept indices match a fresh select on the oracle's own scores."""
+    c = _tiny_cache(80)
+    N, b, w, L, R, Hkv = c["N"], c["b"], c["w"], c["L"], c["R"], c["Hkv"]
+    res = orc.compress(c["kp"], c["vp"], c["tables"], c["lengths"], c["wq"], N, w, 0.5,
+                       c["free"], c["free_count"], c["rc"], Hq=Hkv * c["G"])
+    assert res["status"] == 0
+    shared = c["tables"][0, 0]
+    for l in range(L):
+        assert np.array_equal(res["kpools"][l][shared], c["kp"][l][shared])
+        assert np.array_equal(res["vpools"][l][shared], c["vp"][l][shared])
+        for r in range(R):
+            for h in range(Hkv):
+                kept = res["kept"][l, r, h]
+                assert kept.size == (N - 1) * b and np.all(np.diff(kept) > 0)
+                src_k = _gather(c["kp"][l], c["tables"][r], h, b)
+                src_v = _gather(c["vp"][l], c["tables"][r], h, b)
+                new_row = res["tables"][r, :N - 1]
+                got_k = _gather(res["kpools"][l], new_row, h, b)
+                got_v = _gather(res["vpools"][l], new_row, h, b)
+                assert np.array_equal(got_k, src_k[kept])
+                assert np.array_equal(got_v, src_v[kept])
+                C = N * b - w
+                K = src_k
+                Q = c["wq"][l, r, h * c["G"]:(h + 1) * c["G"]].reshape(-1, c["d"])
+                _, _, score = orc.unit_scores(K, Q, b, w, c["G"], 0.5)
+                close(res["scores"][l, r, h, :C], score, 0.0, "scores_out")
+                assert kept.tolist() == orc.select(score, w, (N - 1) * b - w).tolist()
+    assert res["lengths"].tolist() == [(N - 1) * b] * R
+    assert res["tables"][0, 0] != shared and res["tables"][1, 0] != shared
+    assert res["refcount"][shared] == 0
+
+
+# ------------------------------------------------------------------- decode
+
+def torch_decode(q, kpool, vpool, tables, lengths, scale):
+    """Dense gather + torch fp64 scaled_dot_product_attention."""
+    qd = torch.tensor(widen(q))
+    R, Hq, d = qd.shape
+    Hkv, b = kpool.shape[1], kpool.shape[2]
+    G = Hq // Hkv
+    out = torch.zeros(R, Hq, d, dtype=torch.float64)
+    for r in range(R):
+        n = int(lengths[r])
+        if n == 0:
+            continue
+        blocks = tables[r, :(n + b - 1) // b]
+        K = torch.tensor(widen(np.concatenate([kpool[x] for x in blocks], axis=1)))[:, :n]
+        V = torch.tensor(widen(np.concatenate([vpool[x] for x in blocks], axis=1)))[:, :n]
+        K = K.repeat_interleave(G, dim=0)
+        V = V.repeat_interleave(G, dim=0)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qd[r][:, None, :], K, V, scale=scale)
+        out[r] = o[:, 0, :]
+    return out.numpy()
+
+
+def _decode_case(seed, R=3, Hkv=2, G=3, d=16, b=4, nb=6, num_blocks=30):
+    g = rng(seed)
+    kpool = bf16(g.standard_normal((num_blocks, Hkv, b, d)))
+    vpool = bf16(g.standard_normal((num_blocks, Hkv, b, d)))
+    tables = np.stack([g.permutation(num_blocks)[:nb] for _ in range(R)]).astype(np.int32)
+    q = bf16(g.standard_normal((R, Hkv * G, d)))
+    return q, kpool, vpool, tables
+
+
+def pin_decode_torch_sdpa(orc):
+    q, kp, vp, tables = _decode_case(90)
+    lengths = np.array([24, 13, 1], dtype=np.int32)
+    scale = 1.0 / math.sqrt(q.shape[-1])
+    st, o64, o16 = orc.decode_attn(q, kp, vp, tables, lengths, scale)
+    assert st == 0
+    close(o64, torch_decode(q, kp, vp, tables, lengths, scale), 1e-13, "decode vs torch sdpa")
+    close(widen(o16), torch.tensor(o64).to(torch.bfloat16).to(torch.float64).numpy(), 0.0,
+          "bf16 rounding of the decode output")
+
+
+def pin_decode_closed_forms(orc):
+    """All keys equal -> uniform weights -> the mean of the V rows; a zero
+    length gives zeros."""
+    q, kp, vp, tables = _decode_case(91, R=2)
+    kp = np.broadcast_to(kp[:1, :, :1, :], kp.shape).copy()
+    lengths = np.array([10, 0], dtype=np.int32)
+    st, o64, _ = orc.decode_attn(q, kp, vp, tables, lengths, 0.25)
+    assert st == 0
+    b = kp.shape[2]
+    Hkv = kp.shape[1]
+    G = q.shape[1] // Hkv
+    V = widen(np.concatenate([vp[x] for x in tables[0, :3]], axis=1))[:, :10]
+    expect = np.repeat(V.mean(axis=1), G, axis=0)
+    close(o64[0], expect, 1e-14, "decode with equal keys")
+    close(o64[1], np.zeros_like(o64[1]), 0.0, "decode with zero length")
+
+
+def pin_decode_dominant_key(orc):
+    """One key aligned with the query and much longer: its V row comes out."""
+    q, kp, vp, tables = _decode_case(92, R=1, Hkv=1, G=1, d=16)
+    qv = np.where(widen(q)[0, 0] > 0, 1.0, -1.0)
+    q = bf16(qv[None, None, :])
+    kf = 0.01 * widen(kp)
+    blk, slot = tables[0, 2], 1
+    kf[blk, 0, slot] = 8.0 * qv
+    kp = bf16(kf)
+    st, o64, _ = orc.decode_attn(q, kp, vp, tables, np.array([20], dtype=np.int32), 1.0)
+    assert st == 0
+    close(o64[0, 0], widen(vp[blk, 0, slot]), 1e-30, "decode dominant key")
+
+
+def pin_decode_compacted_equals_masked(orc):
+    """Attention over the compacted cache equals full attention over the
+    original cache restricted to the kept indices."""
+    c = _tiny_cache(93, L=1, R=2)
+    N, b, w, Hkv, G, d = c["N"], c["b"], c["w"], c["Hkv"], c["G"], c["d"]
+    res = orc.compress(c["kp"], c["vp"], c["tables"], c["lengths"], c["wq"], N, w, 0.5,
+                       c["free"], c["free_count"], c["rc"], Hq=Hkv * G)
+    assert res["status"] == 0
+    q = bf16(rng(94).standard_normal((c["R"], Hkv * G, d)))
+    scale = 1.0 / math.sqrt(d)
+    st, o64, _ = orc.decode_attn(q, res["kpools"][0], res["vpools"][0], res["tables"],
+                                 res["lengths"], scale)
+    assert st == 0
+    for r in range(c["R"]):
+        for hq in range(Hkv * G):
+            h = hq // G
+            kept = res["kept"][0, r, h]
+            K = torch.tensor(widen(_gather(c["kp"][0], c["tables"][r], h, b)))
+            V = torch.tensor(widen(_gather(c["vp"][0], c["tables"][r], h, b)))
+            mask = torch.zeros(N * b, dtype=torch.bool)
+            mask[torch.tensor(kept, dtype=torch.long)] = True
+            qq = torch.tensor(widen(q[r, hq]))
+            o = torch.nn.functional.scaled_dot_product_attention(
+                qq[None, None, :], K[None], V[None], attn_mask=mask[None, None, :],
+                scale=scale)[0, 0]
+            close(o64[r, hq], o.numpy(), 1e-12, "compacted vs masked attention")
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
