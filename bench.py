@@ -1,0 +1,472 @@
+#!/usr/bin/env python3
+"""Benchmark of the compression + decode-attention hot path on one GB300.
+
+A step = one zp_compress call over every request, layer and kv head of the
+workload (plan, fused score/select/compact kernel, finalize) followed by
+paged decode attention over the compacted tables, one call per layer.
+Default workload: Qwen3-8B-shaped single layer (8/32 heads, d 128, b 16,
+N_max 128, w 8, lambda 0.5, 64 requests at N_max, no sharing).
+
+Before each step (outside the timed events) the block tables, lengths,
+refcounts and free stack are restored from a pristine device copy (a few KB)
+and a 256 MiB buffer is written to flush L2; the KV pool itself is compacted
+in place step after step (after the first step its rows are the compacted
+rows plus the stale reserved block, which stands in for new tokens).
+
+`--impl reference` times the CPU oracle (plain fp64 C, all host cores) on
+the same workload instead.  Under torchrun each rank runs its own replica
+(weak scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV tokens compressed/s and decode-attn HBM GB/s (fraction of ~8 TB/s), 1 GB300"
+UNIT = "request-tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--workload", default="qwen3_1l")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=200)
+    return p.parse_args()
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest():
+    from compressed_paged_kv_gb300 import _build
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(_build.CSRC)):
+        with open(os.path.join(_build.CSRC, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_digest") == kernel_source_digest():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return False
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "rows", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in self.rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            for n, v in zip(names, r[4:8]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(self.rows)}
+
+
+def device_index(torch):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    idx = torch.cuda.current_device()
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if idx < len(ids):
+            return ids[idx]
+    return idx
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args, world, rank, local):
+    import torch
+    import torch.distributed as dist
+
+    from compressed_paged_kv_gb300 import _build
+    from compressed_paged_kv_gb300 import workloads as W
+    from compressed_paged_kv_gb300 import zp
+
+    _build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    wl = W.WORKLOADS[args.workload]
+    st = W.build_cache(wl, dev, seed=wl.seed + 7919 * rank)
+    host_snap = W.snapshot(st) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    cache = zp.Cache(st.k_pools, st.v_pools, wl.Hq, max_requests=st.block_tables.shape[0],
+                     max_blocks_per_req=st.block_tables.shape[1])
+    req_idx = st.compress_rows if wl.mixed else None
+    dec_rows = st.compress_rows  # decode the compacted requests
+    Rc = st.window_q.shape[1]
+    T = wl.T
+    scale = 1.0 / math.sqrt(wl.d)
+    pristine = [t.clone() for t in (st.block_tables, st.lengths, st.refcount, st.free_ids,
+                                    st.free_count)]
+    live = [st.block_tables, st.lengths, st.refcount, st.free_ids, st.free_count]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    q = [st.decode_q[l][dec_rows.long()].contiguous() for l in range(wl.L)]
+    out = [torch.empty_like(x) for x in q]
+
+    def restore():
+        for a, b in zip(live, pristine):
+            a.copy_(b)
+
+    def compress(scores=None, kept=None):
+        cache.compress(st.block_tables, st.lengths, st.window_q, wl.N, wl.w, wl.lam,
+                       st.free_ids, st.free_count, st.refcount, req_idx=req_idx,
+                       scores_out=scores, kept_out=kept)
+
+    def decode():
+        for l in range(wl.L):
+            cache.decode(l, q[l], st.block_tables, st.lengths, scale, out[l], req_idx=dec_rows)
+
+    K, Wm = args.steps, args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for _ in range(Wm):
+        restore()
+        flush.zero_()
+        compress()
+        decode()
+    torch.cuda.synchronize()
+    assert cache.status() == zp.OK, "device error during warm-up"
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(device_index(torch)) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(K):
+            restore()
+            flush.zero_()
+            ev[i][0].record()
+            compress()
+            ev[i][1].record()
+            decode()
+            ev[i][2].record()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    status = cache.status()
+    comp_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    step_ms = sum(c + d for c, d in zip(comp_ms, dec_ms)) / K
+    comp_avg = sum(comp_ms) / K
+    dec_avg = sum(dec_ms) / K
+
+    # moved rows of a steady-state step (from the kept indices), for the bytes
+    restore()
+    scores_dbg = None
+    kept_dbg = torch.empty((wl.L, Rc, wl.Hkv, (wl.N - 1) * wl.b), dtype=torch.int32, device=dev)
+    src_tab = st.block_tables[st.compress_rows.long(), :wl.N].clone()
+    compress(scores_dbg, kept_dbg)
+    dst_tab = st.block_tables[st.compress_rows.long(), :wl.N - 1]
+    j = torch.arange((wl.N - 1) * wl.b, device=dev, dtype=torch.int32)
+    k = kept_dbg.long()
+    src_blk = torch.gather(src_tab.long()[None, :, None, :].expand(wl.L, Rc, wl.Hkv, wl.N), 3,
+                           k // wl.b)
+    dst_blk = dst_tab.long()[None, :, None, :].repeat_interleave(wl.b, dim=3)
+    moved = int(((k != j) | (src_blk != dst_blk)).sum().item())
+    units = wl.units(Rc)
+    row = wl.d * 2
+    comp_bytes = units * (T * row + wl.w * wl.G * row) + 3 * moved * row
+    comp_bytes_bound = units * wl.unit_bytes()
+    dec_tokens = wl.L * Rc * (wl.N - 1) * wl.b
+    dec_bytes = dec_tokens * wl.Hkv * row * 2 + 2 * wl.L * Rc * wl.Hq * row
+
+    # e2e through host buffers: per-step inputs H2D from pinned memory,
+    # decode outputs and the new block tables back to the host
+    restore()
+    h_wq = st.window_q.cpu().pin_memory()
+    h_q = [x.cpu().pin_memory() for x in q]
+    h_state = [t.cpu().pin_memory() for t in pristine]
+    h_out = [torch.empty_like(x, device="cpu").pin_memory() for x in out]
+    h_tab = torch.empty_like(st.block_tables, device="cpu").pin_memory()
+    h_len = torch.empty_like(st.lengths, device="cpu").pin_memory()
+    h2d = h_wq.numel() * 2 + sum(x.numel() * 2 for x in h_q) + sum(t.numel() * 4 for t in h_state)
+    d2h = sum(x.numel() * 2 for x in h_out) + h_tab.numel() * 4 + h_len.numel() * 4
+    E = args.e2e_steps
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_ms_total = 0.0
+    for i in range(E + 3):
+        flush.zero_()
+        e0.record()
+        st.window_q.copy_(h_wq, non_blocking=True)
+        for a, b in zip(live, h_state):
+            a.copy_(b, non_blocking=True)
+        for a, b in zip(q, h_q):
+            a.copy_(b, non_blocking=True)
+        compress()
+        decode()
+        for a, b in zip(h_out, out):
+            a.copy_(b, non_blocking=True)
+        h_tab.copy_(st.block_tables, non_blocking=True)
+        h_len.copy_(st.lengths, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if i >= 3:
+            e2e_ms_total += e0.elapsed_time(e1)
+    e2e_ms = e2e_ms_total / E
+    status2 = cache.status()
+
+    # max over ranks
+    vals = torch.tensor([step_ms, comp_avg, dec_avg, e2e_ms, t_wall], dtype=torch.float64,
+                        device=dev)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    step_ms, comp_avg, dec_avg, e2e_ms, t_wall = vals.tolist()
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    req_tokens = Rc * T  # request-tokens compressed per step (per rank)
+    peak, peak_src = peaks()
+    comp_gbs = comp_bytes / (comp_avg * 1e-3) / 1e9
+    dec_gbs = dec_bytes / (dec_avg * 1e-3) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": world * req_tokens / (step_ms * 1e-3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": Wm,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; shapes of the named model, no weights)",
+        "config": {
+            "workload": f"{wl.name}: L={wl.L} Hkv={wl.Hkv} Hq={wl.Hq} d={wl.d} b={wl.b} "
+                        f"N_max={wl.N} w={wl.w} lambda={wl.lam} R={Rc}",
+            "global_batch": world * Rc,
+            "seq_len": T,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "flushed between steps (256 MiB write); pool 2x larger than L2",
+            "step": "zp_compress (all layers/heads) + zp_paged_decode_attn per layer",
+        },
+        "compress_ms": comp_avg,
+        "decode_ms": dec_avg,
+        "compress_tokens_per_s": world * req_tokens / (comp_avg * 1e-3),
+        "compress_gbs": comp_gbs,
+        "compress_bytes_per_call": comp_bytes,
+        "compress_bytes_upper_bound": comp_bytes_bound,
+        "moved_rows": moved,
+        "decode_gbs": dec_gbs,
+        "decode_frac_of_8tbs": dec_gbs / NOMINAL_HBM_GBS,
+        "decode_frac_of_measured": dec_gbs / peak,
+        "compress_frac_of_8tbs": comp_gbs / NOMINAL_HBM_GBS,
+        "roofline": {
+            "kernel": "zp_compress_kernel (timed over its zp_compress call: plan + fused + "
+                      "finalize launches)",
+            "bound": "hbm",
+            "achieved": comp_gbs,
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": comp_gbs / peak,
+            "traffic": recorded_traffic(wl.name),
+            "peak_source": peak_src,
+            "algorithmic_bytes": "per unit T*d*2 (K read) + w*G*d*2 (window q) + 3*M*d*2 "
+                                 "(V read, K and V write of the M moved rows)",
+        },
+        "e2e": {"value": world * req_tokens / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": e2e_ms},
+        "gpu_launches": K * (3 + wl.L * (1 if cache_splits_one(wl, Rc, cache) else 2)),
+        "wall_s_timed_loop": t_wall,
+        "device_status": [status, status2],
+    }
+    res["clocks"] = clk.summary()
+    if host_snap is not None:
+        res["cpu_baseline"] = cpu_baseline(wl, host_snap, req_tokens)
+    if world > 1:
+        dist.destroy_process_group()
+    return res
+
+
+def cache_splits_one(wl, R, cache):
+    """Mirror of the library's split choice (one decode launch when 1)."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    pairs = R * wl.Hkv
+    splits = min(16, max(1, (4 * sms + pairs - 1) // pairs))
+    splits = min(splits, max(1, wl.N // 4))
+    bps = (wl.N + splits - 1) // splits
+    return (wl.N + bps - 1) // bps == 1
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_step(orc, wl, snap, nthreads):
+    """One oracle step on host copies: whole compression, then decode of the
+    compacted requests on every layer.  Returns seconds."""
+    import numpy as np
+    t0 = time.perf_counter()
+    req = snap["compress_rows"] if wl.mixed else None
+    res = orc.compress(snap["k_pools"], snap["v_pools"], snap["block_tables"], snap["lengths"],
+                       snap["window_q"], wl.N, wl.w, wl.lam, snap["free_ids"],
+                       snap["free_count"], snap["refcount"], Hq=wl.Hq, req_idx=req,
+                       want_scores=False, want_kept=False, nthreads=nthreads)
+    assert res["status"] == 0
+    rows = snap["compress_rows"]
+    rng = np.random.default_rng(0)
+    for l in range(wl.L):
+        q = rng.standard_normal((len(rows), wl.Hq, wl.d)).astype(np.float32)
+        qb = (q.view(np.uint32) >> 16).astype(np.uint16)
+        st, _, _ = orc.decode_attn(qb, res["kpools"][l], res["vpools"][l],
+                                   res["tables"][rows], res["lengths"][rows],
+                                   1.0 / math.sqrt(wl.d))
+        assert st == 0
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, snap, req_tokens):
+    import oracle
+    orc = oracle.load()
+    cores = os.cpu_count() or 1
+    secs = oracle_step(orc, wl, snap, cores)
+    return {"value": req_tokens / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"one full step of {wl.name} (all {wl.units(snap['window_q'].shape[1])} "
+                      f"units + decode of the compacted requests), fp64 C oracle, "
+                      f"{secs:.1f} s wall"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    import oracle
+    from compressed_paged_kv_gb300 import workloads as W
+    oracle.build()
+    orc = oracle.load()
+    wl = W.WORKLOADS[args.workload]
+    st = W.build_cache(wl, "cpu")
+    snap = W.snapshot(st)
+    del st
+    cores = os.cpu_count() or 1
+    Rc = snap["window_q"].shape[1]
+    req_tokens = Rc * wl.T
+    for _ in range(args.warmup if args.warmup < 3 else 3):
+        oracle_step(orc, wl, snap, cores)
+    t = [oracle_step(orc, wl, snap, cores) for _ in range(min(args.steps, 5))]
+    step_s = sum(t) / len(t)
+    v = req_tokens / step_s
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+        "steps": len(t), "warmup": min(args.warmup, 3), "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "global_batch": Rc, "seq_len": wl.T,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"full {wl.name} steps (compress + decode), "
+                                   f"{len(t)} timed"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_gpu(args, world, rank, local)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

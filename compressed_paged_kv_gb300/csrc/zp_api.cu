@@ -1,0 +1,379 @@
+// zp_api.cu -- the C ABI declared in include/zp.h: handle, argument checks,
+// TMA tensor maps, launches.  Host code only.
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "zp_internal.cuh"
+
+using zp::Workspace;
+
+namespace {
+
+constexpr int kMaxSplits = 16;
+
+struct Alloc {
+    size_t off = 0;
+    size_t take(size_t bytes, size_t align = 256)
+    {
+        off = (off + align - 1) / align * align;
+        const size_t o = off;
+        off += bytes;
+        return o;
+    }
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2D view [num_blocks * Hkv * b rows][d] of a pool, box {64 columns, b rows},
+// 128-byte swizzle: one (block, kv head) slab is loaded as d/64 boxes.
+bool encode_pool_map(CUtensorMap *map, void *pool, int num_blocks, int hkv, int d)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(d),
+                          static_cast<cuuint64_t>(num_blocks) * hkv * zp::kBlk};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(zp::kBlk)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+struct zp_cache {
+    int device = 0;
+    int L = 0, Hkv = 0, Hq = 0, d = 0, b = 0, num_blocks = 0;
+    int max_requests = 0, max_blocks = 0;
+    int num_sms = 0;
+    int32_t gen = 0;
+    void *base = nullptr;
+    Workspace ws{};
+};
+
+extern "C" {
+
+const char *zp_status_string(zp_status s)
+{
+    switch (s) {
+    case ZP_OK: return "ok";
+    case ZP_ERR_INVALID_ARG: return "invalid argument";
+    case ZP_ERR_UNSUPPORTED: return "unsupported shape or size";
+    case ZP_ERR_OUT_OF_BLOCKS: return "free stack too short";
+    case ZP_ERR_DEVICE_CHECK: return "inconsistent cache state found on the device";
+    case ZP_ERR_CUDA: return "CUDA runtime error";
+    case ZP_ERR_TIMEOUT: return "bounded device wait gave up";
+    default: return "unknown status";
+    }
+}
+
+zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
+{
+    if (!desc || !out)
+        return ZP_ERR_INVALID_ARG;
+    const zp_cache_desc &D = *desc;
+    if (D.num_layers < 1 || D.num_kv_heads < 1 || D.num_q_heads < 1 || D.num_blocks < 1 ||
+        D.max_requests < 1 || D.max_blocks_per_req < 2 || !D.k_pools || !D.v_pools)
+        return ZP_ERR_INVALID_ARG;
+    if (D.num_q_heads % D.num_kv_heads != 0)
+        return ZP_ERR_INVALID_ARG;
+    if (D.head_dim != 64 && D.head_dim != 128)
+        return ZP_ERR_UNSUPPORTED;
+    if (D.block_size != zp::kBlk)
+        return ZP_ERR_UNSUPPORTED;
+    if (D.num_q_heads / D.num_kv_heads > 16)
+        return ZP_ERR_UNSUPPORTED;
+    const uint64_t rows = static_cast<uint64_t>(D.num_blocks) * D.num_kv_heads * zp::kBlk;
+    if (rows >= (1ull << 31))
+        return ZP_ERR_UNSUPPORTED;
+    for (int l = 0; l < D.num_layers; ++l)
+        if (!D.k_pools[l] || !D.v_pools[l] || !aligned(D.k_pools[l], 16) ||
+            !aligned(D.v_pools[l], 16))
+            return ZP_ERR_INVALID_ARG;
+
+    zp_cache *c = new (std::nothrow) zp_cache();
+    if (!c)
+        return ZP_ERR_CUDA;
+    c->L = D.num_layers;
+    c->Hkv = D.num_kv_heads;
+    c->Hq = D.num_q_heads;
+    c->d = D.head_dim;
+    c->b = D.block_size;
+    c->num_blocks = D.num_blocks;
+    c->max_requests = D.max_requests;
+    c->max_blocks = D.max_blocks_per_req;
+    if (cudaGetDevice(&c->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) !=
+            cudaSuccess) {
+        delete c;
+        return ZP_ERR_CUDA;
+    }
+
+    const size_t entries = static_cast<size_t>(D.max_requests) * D.max_blocks_per_req;
+    const size_t part = static_cast<size_t>(D.max_requests) * D.num_q_heads * kMaxSplits *
+                        (D.head_dim + 2);
+    Alloc A;
+    const size_t o_sticky = A.take(4);
+    const size_t o_call = A.take(4);
+    const size_t o_kmaps = A.take(sizeof(CUtensorMap) * D.num_layers, 128);
+    const size_t o_vmaps = A.take(sizeof(CUtensorMap) * D.num_layers, 128);
+    const size_t o_kp = A.take(sizeof(void *) * D.num_layers);
+    const size_t o_vp = A.take(sizeof(void *) * D.num_layers);
+    const size_t o_dst = A.take(4 * entries);
+    const size_t o_push = A.take(4 * entries);
+    const size_t o_cnt = A.take(16);
+    const size_t o_occ = A.take(4 * static_cast<size_t>(D.num_blocks));
+    const size_t o_last = A.take(4 * static_cast<size_t>(D.num_blocks));
+    const size_t o_rowmark = A.take(4 * static_cast<size_t>(D.max_requests));
+    const size_t o_part = A.take(4 * part);
+    const size_t total = A.take(0);
+
+    if (cudaMalloc(&c->base, total) != cudaSuccess) {
+        cudaGetLastError();
+        delete c;
+        return ZP_ERR_CUDA;
+    }
+    uint8_t *b = static_cast<uint8_t *>(c->base);
+    Workspace &ws = c->ws;
+    ws.sticky = reinterpret_cast<int32_t *>(b + o_sticky);
+    ws.call = reinterpret_cast<int32_t *>(b + o_call);
+    ws.kmaps = reinterpret_cast<CUtensorMap *>(b + o_kmaps);
+    ws.vmaps = reinterpret_cast<CUtensorMap *>(b + o_vmaps);
+    ws.kpools = reinterpret_cast<void **>(b + o_kp);
+    ws.vpools = reinterpret_cast<void **>(b + o_vp);
+    ws.dst_table = reinterpret_cast<int32_t *>(b + o_dst);
+    ws.push_list = reinterpret_cast<int32_t *>(b + o_push);
+    ws.counters = reinterpret_cast<int32_t *>(b + o_cnt);
+    ws.occ = reinterpret_cast<int32_t *>(b + o_occ);
+    ws.last = reinterpret_cast<int32_t *>(b + o_last);
+    ws.rowmark = reinterpret_cast<int32_t *>(b + o_rowmark);
+    ws.dec_part = reinterpret_cast<float *>(b + o_part);
+    ws.dec_part_floats = part;
+
+    std::vector<CUtensorMap> kmaps(D.num_layers), vmaps(D.num_layers);
+    bool ok = true;
+    for (int l = 0; l < D.num_layers && ok; ++l) {
+        ok = encode_pool_map(&kmaps[l], D.k_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim) &&
+             encode_pool_map(&vmaps[l], D.v_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim);
+    }
+    ok = ok && cudaMemset(c->base, 0, o_kmaps) == cudaSuccess &&
+         cudaMemset(b + o_rowmark, 0, 4 * static_cast<size_t>(D.max_requests)) == cudaSuccess &&
+         cudaMemcpy(ws.kmaps, kmaps.data(), sizeof(CUtensorMap) * D.num_layers,
+                    cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(ws.vmaps, vmaps.data(), sizeof(CUtensorMap) * D.num_layers,
+                    cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(ws.kpools, D.k_pools, sizeof(void *) * D.num_layers,
+                    cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(ws.vpools, D.v_pools, sizeof(void *) * D.num_layers,
+                    cudaMemcpyHostToDevice) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        cudaFree(c->base);
+        delete c;
+        return ZP_ERR_CUDA;
+    }
+    *out = c;
+    return ZP_OK;
+}
+
+void zp_cache_destroy(zp_cache *cache)
+{
+    if (!cache)
+        return;
+    if (cache->base)
+        cudaFree(cache->base);
+    delete cache;
+}
+
+static bool on_device(const zp_cache *c)
+{
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess && dev == c->device;
+}
+
+zp_status zp_compress(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int32_t num_rows,
+                      int32_t *lengths, const int32_t *req_idx, int32_t R, const void *window_q,
+                      int32_t n_max, int32_t window, float lambda, const zp_block_pool *pool,
+                      void *stream, float *scores_out, int32_t *kept_out)
+{
+    if (!c || !block_tables || !lengths || !window_q || !pool || !pool->free_ids ||
+        !pool->free_count || !pool->refcount)
+        return ZP_ERR_INVALID_ARG;
+    if (R < 0 || num_rows < 1 || num_rows > c->max_requests || R > num_rows)
+        return ZP_ERR_INVALID_ARG;
+    if (n_max < 2 || bt_stride < n_max || pool->capacity < 1)
+        return ZP_ERR_INVALID_ARG;
+    if (window < 1 || window > c->b || !std::isfinite(lambda))
+        return ZP_ERR_INVALID_ARG;
+    if (!aligned(window_q, 16) || !aligned(scores_out, 4) || !aligned(kept_out, 4))
+        return ZP_ERR_INVALID_ARG;
+    const int G = c->Hq / c->Hkv;
+    const int T = n_max * c->b;
+    const int tw = zp::compress_tile_words(T);
+    const int rows = window * G;
+    if (n_max > c->max_blocks || tw == 0 || rows > zp::kMaxRows)
+        return ZP_ERR_UNSUPPORTED;
+    if (R == 0)
+        return ZP_OK;
+    if (!on_device(c))
+        return ZP_ERR_INVALID_ARG;
+    const int mt = rows <= 16 ? 1 : rows <= 32 ? 2 : 4;
+    const int cs = T / (8 * 16 * tw);
+    const long long units = static_cast<long long>(R) * c->L * c->Hkv;
+    if (units * cs >= (1ll << 31))
+        return ZP_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    c->gen = c->gen >= 0x7ffffff0 ? 1 : c->gen + 1;
+    zp::PlanArgs pa{};
+    pa.tables = block_tables;
+    pa.stride = bt_stride;
+    pa.num_rows = num_rows;
+    pa.lengths = lengths;
+    pa.req_idx = req_idx;
+    pa.R = R;
+    pa.N = n_max;
+    pa.num_blocks = c->num_blocks;
+    pa.refcount = pool->refcount;
+    pa.free_ids = pool->free_ids;
+    pa.free_count = pool->free_count;
+    pa.capacity = pool->capacity;
+    pa.gen = c->gen;
+    pa.ws = c->ws;
+    if (zp::launch_plan(pa, s) != cudaSuccess)
+        return ZP_ERR_CUDA;
+
+    zp::CompressArgs ca{};
+    ca.kmaps = c->ws.kmaps;
+    ca.kpools = c->ws.kpools;
+    ca.vpools = c->ws.vpools;
+    ca.tables = block_tables;
+    ca.stride = bt_stride;
+    ca.req_idx = req_idx;
+    ca.dst_table = c->ws.dst_table;
+    ca.window_q = static_cast<const __nv_bfloat16 *>(window_q);
+    ca.scores_out = scores_out;
+    ca.kept_out = kept_out;
+    ca.call = c->ws.call;
+    ca.sticky = c->ws.sticky;
+    ca.L = c->L;
+    ca.Hkv = c->Hkv;
+    ca.Hq = c->Hq;
+    ca.R = R;
+    ca.N = n_max;
+    ca.w = window;
+    ca.rows = rows;
+    ca.cs = cs;
+    ca.lambda = lambda;
+    ca.inv_rows = 1.0f / static_cast<float>(rows);
+    ca.logit_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c->d)));
+    if (zp::launch_compress(ca, c->d, tw, mt, static_cast<int>(units), s) != cudaSuccess)
+        return ZP_ERR_CUDA;
+
+    zp::FinalizeArgs fa{};
+    fa.tables = block_tables;
+    fa.stride = bt_stride;
+    fa.lengths = lengths;
+    fa.req_idx = req_idx;
+    fa.R = R;
+    fa.N = n_max;
+    fa.refcount = pool->refcount;
+    fa.free_ids = pool->free_ids;
+    fa.free_count = pool->free_count;
+    fa.ws = c->ws;
+    if (zp::launch_finalize(fa, s) != cudaSuccess)
+        return ZP_ERR_CUDA;
+    return ZP_OK;
+}
+
+zp_status zp_paged_decode_attn(zp_cache *c, int32_t layer, const void *q,
+                               const int32_t *block_tables, int32_t bt_stride, int32_t num_rows,
+                               const int32_t *lengths, const int32_t *req_idx, int32_t R,
+                               float scale, void *out, void *stream)
+{
+    if (!c || !q || !block_tables || !lengths || !out)
+        return ZP_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= c->L || R < 0 || R > c->max_requests || num_rows < 1 ||
+        bt_stride < 1 || !std::isfinite(scale))
+        return ZP_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 2))
+        return ZP_ERR_INVALID_ARG;
+    if (static_cast<long long>(bt_stride) * c->b >= (1ll << 31))
+        return ZP_ERR_UNSUPPORTED;
+    if (R == 0)
+        return ZP_OK;
+    if (!on_device(c))
+        return ZP_ERR_INVALID_ARG;
+
+    // splits per (request, kv head): enough CTAs for ~4 per SM, at most
+    // kMaxSplits, never fewer than 4 blocks per split
+    const int pairs = R * c->Hkv;
+    const int target = 4 * c->num_sms;
+    int splits = std::min(kMaxSplits, std::max(1, (target + pairs - 1) / pairs));
+    splits = std::min(splits, std::max(1, bt_stride / 4));
+    const int bps = (bt_stride + splits - 1) / splits;
+    splits = (bt_stride + bps - 1) / bps;
+
+    zp::DecodeArgs da{};
+    // the per-layer maps live in device memory; kernels take their address
+    da.kmap = c->ws.kmaps + layer;
+    da.vmap = c->ws.vmaps + layer;
+    da.q = static_cast<const __nv_bfloat16 *>(q);
+    da.tables = block_tables;
+    da.stride = bt_stride;
+    da.num_rows = num_rows;
+    da.lengths = lengths;
+    da.req_idx = req_idx;
+    da.R = R;
+    da.Hkv = c->Hkv;
+    da.Hq = c->Hq;
+    da.num_blocks = c->num_blocks;
+    da.splits = splits;
+    da.bps = bps;
+    da.logit_scale = scale * 1.4426950408889634f;
+    da.out = static_cast<__nv_bfloat16 *>(out);
+    da.part = c->ws.dec_part;
+    da.sticky = c->ws.sticky;
+    if (zp::launch_decode(da, c->d, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ZP_ERR_CUDA;
+    return ZP_OK;
+}
+
+zp_status zp_cache_status(zp_cache *c, void *stream, int32_t *out_status)
+{
+    if (!c || !out_status)
+        return ZP_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, c->ws.sticky, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(c->ws.sticky, 0, 4, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return ZP_ERR_CUDA;
+    *out_status = v;
+    return ZP_OK;
+}
+
+}  // extern "C"

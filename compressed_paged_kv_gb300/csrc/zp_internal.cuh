@@ -1,0 +1,319 @@
+// zp_internal.cuh -- shared device helpers and launch-argument structs of the
+// sm_103a Compressed PagedAttention library.  Internal: not part of the C ABI.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; no driver-API link)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zp.h"
+
+namespace zp {
+
+constexpr int kBlk = 16;            // tokens per block (the only supported size)
+constexpr int kMaxRows = 64;        // window rows per unit: w * (Hq / Hkv)
+constexpr int kMaxCluster = 8;      // CTAs per unit in the compression kernel
+constexpr uint32_t kWaitSpins = 1u << 22;  // bound on every mbarrier wait
+
+// ----------------------------------------------------------------- workspace
+// Device memory the handle owns (allocated once in zp_cache_create).
+struct Workspace {
+    int32_t *sticky;     // [1]  first device-detected error since last read
+    int32_t *call;       // [1]  status of the compression call in flight
+    CUtensorMap *kmaps;  // [L]  K pool maps, 128B swizzle, box {64, 16}
+    CUtensorMap *vmaps;  // [L]  V pool maps, same
+    void **kpools;       // [L]  device copies of the pool pointers
+    void **vpools;       // [L]
+    int32_t *dst_table;  // [max_requests * max_blocks] plan: destination blocks
+    int32_t *push_list;  // [max_requests * max_blocks] plan: blocks to free, in order
+    int32_t *counters;   // [4]  plan: pops, pushes
+    int32_t *occ;        // [num_blocks] plan: holders of a replaced block in this call
+    int32_t *last;       // [num_blocks] plan: last (request, block) entry of such a block
+    int32_t *rowmark;    // [max_requests] generation stamps (duplicate-row check)
+    float *dec_part;     // decode split partials
+    size_t dec_part_floats;
+};
+
+// ------------------------------------------------------------ launch args
+struct PlanArgs {
+    const int32_t *tables;
+    int32_t stride, num_rows;
+    const int32_t *lengths;
+    const int32_t *req_idx;
+    int32_t R, N, num_blocks;
+    const int32_t *refcount;
+    const int32_t *free_ids;
+    const int32_t *free_count;
+    int32_t capacity;
+    int32_t gen;
+    Workspace ws;
+};
+
+struct FinalizeArgs {
+    int32_t *tables;
+    int32_t stride;
+    int32_t *lengths;
+    const int32_t *req_idx;
+    int32_t R, N;
+    int32_t *refcount;
+    int32_t *free_ids;
+    int32_t *free_count;
+    Workspace ws;
+};
+
+struct CompressArgs {
+    const CUtensorMap *kmaps;
+    void *const *kpools;
+    void *const *vpools;
+    const int32_t *tables;
+    int32_t stride;
+    const int32_t *req_idx;
+    const int32_t *dst_table;
+    const __nv_bfloat16 *window_q;
+    float *scores_out;
+    int32_t *kept_out;
+    int32_t *call;
+    int32_t *sticky;
+    int32_t L, Hkv, Hq, R, N, w, rows, cs;
+    float lambda;
+    float inv_rows;       // 1 / (w * G)
+    float logit_scale;    // log2(e) / sqrt(d): logits are kept in base 2
+};
+
+struct DecodeArgs {
+    const CUtensorMap *kmap;
+    const CUtensorMap *vmap;
+    const __nv_bfloat16 *q;
+    const int32_t *tables;
+    int32_t stride, num_rows;
+    const int32_t *lengths;
+    const int32_t *req_idx;
+    int32_t R, Hkv, Hq, num_blocks;
+    int32_t splits, bps;  // splits per (request, kv head), blocks per split
+    float logit_scale;    // scale * log2(e)
+    __nv_bfloat16 *out;
+    float *part;          // [R][Hq][splits][2 + d] (m, l, o[d]) when splits > 1
+    int32_t *sticky;
+};
+
+// Launchers (defined next to their kernels).
+cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
+cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s);
+cudaError_t launch_compress(const CompressArgs &a, int d, int tw, int mt, int units,
+                            cudaStream_t s);
+int compress_tile_words(int T);  // 16-key tiles per warp for T tokens, 0 if unsupported
+cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t s);
+
+// ------------------------------------------------------------ device helpers
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void set_error(int32_t *word, int32_t code)
+{
+    atomicCAS(word, 0, code);
+}
+
+// mbarrier ------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Bounded wait on a phase of an mbarrier; false when the bound was hit.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    const uint32_t addr = smem_u32(bar);
+    for (uint32_t i = 0; i < kWaitSpins; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done)
+            return true;
+        if (i > 64)
+            __nanosleep(64);
+    }
+    return false;
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (TMA / bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// TMA: 2D tile load global -> shared, completion counted on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Bulk (untiled) copy global -> shared; 16-byte aligned, size multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ldmatrix / mma ---------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// D += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Byte offset of 16-byte chunk `ch` (8 bf16) of row `row` in a [rows][d] bf16
+// tile stored as d/64 column panels of [rows][128 B] with the 128-byte
+// swizzle (chunk index XOR row % 8) -- the layout TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B into a 1024-byte aligned buffer.
+__device__ __forceinline__ uint32_t swz(int row, int ch, int rows)
+{
+    return static_cast<uint32_t>((ch >> 3) * rows * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
+}
+
+// cluster --------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    cluster_arrive();
+    cluster_wait();
+}
+
+// Address of the same shared variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int32_t ld_dsmem_s32(uint32_t addr)
+{
+    int32_t v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// global / shared 16-byte moves ------------------------------------------------
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_global_nc_v4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_global_v4(void *p, uint4 v)
+{
+    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// fp32 -> u32 map that preserves order (-0.0 sorts just below +0.0).
+__device__ __forceinline__ uint32_t f32_order(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+#endif  // __CUDACC__
+
+}  // namespace zp

@@ -1,0 +1,181 @@
+/*
+ * zp.h -- C ABI of the GB300 (sm_103a) Compressed PagedAttention hot path.
+ *
+ * The method: "Zipage: Maintain High Request Concurrency for LLM Reasoning
+ * through Compressed PagedAttention" as summarised on gist.science (Dutch
+ * "Technische samenvatting / Methodologie", Korean "기술 요약 / 2. 방법론"),
+ * over the paged KV cache of "Paged KV cache and continuous batching for LLMs"
+ * ("How it works").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer documented as "device" is CUDA device memory OWNED BY THE
+ *    CALLER.  The library never frees caller memory.  The library owns only
+ *    the opaque zp_cache handle and the device workspace it allocates in
+ *    zp_cache_create (status word, tensor maps, per-call scratch).
+ *  - bf16 tensors are passed as void* and hold IEEE bfloat16 values.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call only enqueues work on `stream`: nothing
+ *    synchronises except zp_cache_status.
+ *  - Argument errors that the host can see are returned synchronously,
+ *    before anything is enqueued.  Errors that only the device can see (a
+ *    length or block id read from device memory, an empty free stack) are
+ *    recorded in the handle's sticky status word, and every later kernel of
+ *    the same call skips its writes; read the word with zp_cache_status.
+ *  - A handle serves at most one zp_compress and one zp_paged_decode_attn in
+ *    flight at a time (they may run concurrently on two streams when they
+ *    touch disjoint requests).  More concurrency needs more handles.
+ *
+ * KV pool layout (one K pool and one V pool per layer, caller-owned):
+ *     pool[num_blocks][num_kv_heads][block_size][head_dim]   bf16, contiguous
+ * so one (block, kv head) slab is block_size*head_dim*2 bytes (4 KiB at
+ * b = 16, d = 128) and one token row is head_dim*2 bytes.  All layers and kv
+ * heads of a request share its block table row.  Pool base addresses must be
+ * 16-byte aligned.
+ */
+#ifndef ZP_H
+#define ZP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t zp_status;
+
+#define ZP_OK 0
+#define ZP_ERR_INVALID_ARG (-1)   /* bad argument (host- or device-detected) */
+#define ZP_ERR_UNSUPPORTED (-2)   /* shape or size outside the supported set */
+#define ZP_ERR_OUT_OF_BLOCKS (-3) /* free stack too short for the target blocks */
+#define ZP_ERR_DEVICE_CHECK (-4)  /* inconsistent cache state found on the device */
+#define ZP_ERR_CUDA (-5)          /* a CUDA runtime call failed */
+#define ZP_ERR_TIMEOUT (-6)       /* a bounded device-side wait gave up */
+
+typedef struct zp_cache zp_cache;
+
+/* Shape of the cache and the caller's per-layer pools.
+ * Supported: head_dim 64 or 128, block_size 16, num_q_heads a multiple of
+ * num_kv_heads.  max_requests bounds the rows of any block table passed to
+ * the handle and the batch of any call; max_blocks_per_req bounds the row
+ * stride of those tables (it sizes the workspace). */
+typedef struct {
+    int32_t num_layers;         /* L >= 1 */
+    int32_t num_kv_heads;       /* Hkv >= 1 */
+    int32_t num_q_heads;        /* Hq, multiple of Hkv */
+    int32_t head_dim;           /* d: 64 or 128 */
+    int32_t block_size;         /* b: 16 */
+    int32_t num_blocks;         /* physical blocks in each pool */
+    int32_t max_requests;       /* >= 1 */
+    int32_t max_blocks_per_req; /* >= 2 */
+    void *const *k_pools;       /* host array of L device pointers (bf16 pools) */
+    void *const *v_pools;       /* host array of L device pointers (bf16 pools) */
+} zp_cache_desc;
+
+/* Free-block stack and refcounts of the pool (device, caller-owned).
+ * free_ids[0 .. *free_count) are the free block ids; the top of the stack is
+ * free_ids[*free_count - 1].  refcount[blk] counts the block-table entries
+ * (over all live requests) that point at blk; a free block has refcount 0. */
+typedef struct {
+    int32_t *free_ids;   /* device [capacity] */
+    int32_t *free_count; /* device [1] */
+    int32_t *refcount;   /* device [num_blocks] */
+    int32_t capacity;    /* length of free_ids, >= 1 */
+} zp_block_pool;
+
+/* Creates a handle over caller-owned pools and allocates its workspace.
+ * Returns ZP_ERR_INVALID_ARG / ZP_ERR_UNSUPPORTED for a bad descriptor
+ * (checked before any CUDA call), ZP_ERR_CUDA if an allocation fails.
+ * *out is set only on success; the current CUDA device is recorded. */
+zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out);
+
+/* Frees the handle and its workspace (not the pools).  NULL is a no-op.
+ * The caller must make sure no work that uses the handle is in flight. */
+void zp_cache_destroy(zp_cache *cache);
+
+/* Compressed PagedAttention compression of R requests, every layer and kv head
+ * ("Methodologie" §1, §3, §5 of the Dutch summary; "방법론" A, C, E of the
+ * Korean summary).  A request qualifies when it holds n_max full blocks
+ * (lengths == n_max * block_size).  For each (request, layer, kv head):
+ *   importance  softmax(q . k / sqrt(d)) of the w window queries (the last w
+ *               tokens, always in the last block; query i sees keys up to its
+ *               own position), averaged over the w queries and the
+ *               num_q_heads/num_kv_heads query heads of the group;
+ *   redundancy  Lightning Redundancy Score: mean cosine similarity of a key to
+ *               the other block_size-1 keys of its own block (0 for a zero key);
+ *   score       importance - lambda * redundancy over the C = T - w
+ *               candidates (T = n_max * block_size);
+ *   select      keep the (n_max-1)*b - w highest scores (at equal score the
+ *               lower index), i.e. evict exactly b candidates; the window is
+ *               always kept;
+ *   compact     the kept tokens, in original order, fill blocks 0..n_max-2 of
+ *               the request; block n_max-1 stays reserved for decoding.
+ * Blocks are decided on the refcounts at call start: a block with refcount 1
+ * is rewritten in place; a block with refcount > 1 (a shared prefix) is never
+ * written -- its destination is a fresh target block popped from the top of
+ * the free stack (in request, block order), and it loses one reference per
+ * compressing holder; a shared reserved block is replaced by a fresh block.
+ * A block whose refcount reaches 0 is pushed on the free stack (after the
+ * pops), in the order a sequential pass over (request, block) zeroes it.
+ * Afterwards table rows hold the destination blocks and lengths are
+ * (n_max-1)*b.
+ *
+ *  block_tables  device int32 [num_rows][bt_stride], in/out
+ *  lengths       device int32 [num_rows], in/out (== n_max*b on input)
+ *  req_idx       device int32 [R] row of each compressing request, distinct,
+ *                or NULL for rows 0..R-1
+ *  window_q      device bf16 [L][R][Hq][w][d]: window queries of request r
+ *                (row g*w + i of kv head h's group is query head h*G+g at
+ *                window slot i, the query of token T - w + i)
+ *  n_max         blocks per request at compression; n_max*b a multiple of 128,
+ *                at most 4096
+ *  window        w, 1 <= w <= b, w * (Hq/Hkv) <= 64
+ *  lambda        redundancy weight
+ *  pool          free stack + refcounts, updated in place
+ *  scores_out    NULL or device fp32 [L][R][Hkv][T]: candidate scores
+ *                (+inf at window positions)
+ *  kept_out      NULL or device int32 [L][R][Hkv][(n_max-1)*b]: kept source
+ *                positions, ascending
+ * All-or-nothing: on a device-detected error (bad length, bad or duplicate
+ * row, bad block id, refcount inconsistent, free stack too short) nothing is
+ * written and the sticky status records the error. */
+zp_status zp_compress(zp_cache *cache, int32_t *block_tables, int32_t bt_stride,
+                      int32_t num_rows, int32_t *lengths, const int32_t *req_idx, int32_t R,
+                      const void *window_q, int32_t n_max, int32_t window, float lambda,
+                      const zp_block_pool *pool, void *stream, float *scores_out,
+                      int32_t *kept_out);
+
+/* Paged decode attention over the block tables of one layer ("Paged KV cache
+ * and continuous batching for LLMs", "How it works"): for request i and query
+ * head hq (kv head hq / (Hq/Hkv)),
+ *     out = sum_t softmax_t(scale * q . k_t) v_t,   t < lengths[row],
+ * token t living in block block_tables[row][t / b], slot t % b, where
+ * row = req_idx[i] (or i when req_idx is NULL).  fp32 accumulation, one
+ * round-to-nearest-even to bf16.  A zero length gives a zero output.
+ *
+ *  layer         0 <= layer < L
+ *  q             device bf16 [R][Hq][d]
+ *  block_tables  device int32 [num_rows][bt_stride] (read only)
+ *  lengths       device int32 [num_rows], 0 <= lengths[row] <= bt_stride * b
+ *  req_idx       device int32 [R] or NULL
+ *  out           device bf16 [R][Hq][d]
+ * A length or block id out of range is recorded as ZP_ERR_DEVICE_CHECK in the
+ * sticky status; the affected outputs are then undefined. */
+zp_status zp_paged_decode_attn(zp_cache *cache, int32_t layer, const void *q,
+                               const int32_t *block_tables, int32_t bt_stride, int32_t num_rows,
+                               const int32_t *lengths, const int32_t *req_idx, int32_t R,
+                               float scale, void *out, void *stream);
+
+/* Synchronises `stream`, returns the handle's sticky device status in
+ * *out_status (ZP_OK or the first device-detected error since the last
+ * read) and clears it.  Returns ZP_ERR_CUDA if the stream reports an error. */
+zp_status zp_cache_status(zp_cache *cache, void *stream, int32_t *out_status);
+
+/* Static description of a status code ("ok", "invalid argument", ...). */
+const char *zp_status_string(zp_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZP_H */

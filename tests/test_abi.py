@@ -1,0 +1,82 @@
+"""The C ABI library loads without a GPU and exports every entry point that
+include/*.h declares; host-side descriptor checks return before any CUDA call."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from compressed_paged_kv_gb300 import _build, zp
+    _build.build()
+    return zp.lib()
+
+
+def declared_functions():
+    names = []
+    for path in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(path).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(zp_[a-z0-9_]+)\s*\(",
+                            src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("zp_cache_create", "zp_cache_destroy", "zp_compress", "zp_paged_decode_attn",
+              "zp_cache_status", "zp_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    from compressed_paged_kv_gb300 import zp
+    assert zp.status_string(zp.OK) == "ok"
+    assert "free stack" in zp.status_string(zp.ERR_OUT_OF_BLOCKS)
+
+
+def test_descriptor_checks_need_no_gpu(lib):
+    from compressed_paged_kv_gb300 import zp
+    P = ctypes.c_void_p
+    dummy = (P * 1)(P(256))
+
+    def create(**kw):
+        base = dict(num_layers=1, num_kv_heads=2, num_q_heads=4, head_dim=64, block_size=16,
+                    num_blocks=8, max_requests=2, max_blocks_per_req=8)
+        base.update(kw)
+        d = zp.zp_cache_desc(base["num_layers"], base["num_kv_heads"], base["num_q_heads"],
+                             base["head_dim"], base["block_size"], base["num_blocks"],
+                             base["max_requests"], base["max_blocks_per_req"], dummy, dummy)
+        h = P()
+        return lib.zp_cache_create(ctypes.byref(d), ctypes.byref(h))
+
+    assert create(head_dim=96) == zp.ERR_UNSUPPORTED
+    assert create(block_size=32) == zp.ERR_UNSUPPORTED
+    assert create(num_q_heads=5) == zp.ERR_INVALID_ARG
+    assert create(num_layers=0) == zp.ERR_INVALID_ARG
+    assert create(max_blocks_per_req=1) == zp.ERR_INVALID_ARG
+    assert create(num_kv_heads=1, num_q_heads=32) == zp.ERR_UNSUPPORTED
+    assert lib.zp_cache_create(None, None) == zp.ERR_INVALID_ARG
+    assert lib.zp_compress(None, None, 0, 0, None, None, 0, None, 0, 0, 0.0, None, None, None,
+                           None) == zp.ERR_INVALID_ARG
+    assert lib.zp_paged_decode_attn(None, 0, None, None, 0, 0, None, None, 0, 0.0, None,
+                                    None) == zp.ERR_INVALID_ARG
+    lib.zp_cache_destroy(None)
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    from compressed_paged_kv_gb300 import zp
+    monkeypatch.setattr(zp, "_lib", None)
+    monkeypatch.setattr(zp, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        zp.lib()
