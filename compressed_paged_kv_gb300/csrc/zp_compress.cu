@@ -19,9 +19,11 @@
 //                       [c*TPC, (c+1)*TPC).  K chunk -> shared memory by TMA
 //                       (128B swizzle); window logits and the intra-block
 //                       Gram on the tensor cores (mma.sync bf16, fp32
-//                       accumulate); softmax statistics and a 4-pass radix
-//                       select exchanged over distributed shared memory;
-//                       kept rows scattered to their destination slots.
+//                       accumulate); softmax statistics and the b lowest
+//                       scores (warp radix select on the fp32 score bits,
+//                       merged per CTA and then per cluster) exchanged over
+//                       distributed shared memory; kept rows scattered to
+//                       their destination slots.
 //   zp_finalize_kernel  1 CTA: commits tables, lengths, refcounts, free stack.
 #include "zp_internal.cuh"
 
@@ -246,6 +248,82 @@ __global__ void __launch_bounds__(kPlanThreads) zp_finalize_kernel(const Finaliz
 
 // ============================================================ fused kernel
 
+// Warp radix select: the k smallest of the 32*KPL distinct 64-bit keys held
+// KPL per lane (slot s of lane l is entry l + 32 s), MSB first, one bit per
+// step: at each bit the keys with a 0 are counted by ballot; if they cover
+// the remaining demand the search continues among them, else all of them are
+// taken and it continues among the 1s.  chosen[s] is the ballot mask of the
+// selected entries of slot s (the same in every lane).  Entries equal to ~0
+// are padding; if any are needed they are taken in entry order.
+template <int KPL>
+__device__ __forceinline__ void warp_select_smallest(const uint64_t (&key)[KPL], int k,
+                                                     uint32_t (&chosen)[KPL])
+{
+    uint32_t active[KPL];
+    int n_active = 0;
+#pragma unroll
+    for (int s = 0; s < KPL; ++s) {
+        active[s] = 0xffffffffu;
+        chosen[s] = 0u;
+        n_active += 32;
+    }
+    int need = k;
+    for (int bit = 63; bit >= 0 && need > 0 && need < n_active; --bit) {
+        uint32_t zeros[KPL];
+        int nz = 0;
+#pragma unroll
+        for (int s = 0; s < KPL; ++s) {
+            zeros[s] = __ballot_sync(0xffffffffu, ((key[s] >> bit) & 1ull) == 0ull) & active[s];
+            nz += __popc(zeros[s]);
+        }
+        if (nz >= need) {
+#pragma unroll
+            for (int s = 0; s < KPL; ++s)
+                active[s] = zeros[s];
+            n_active = nz;
+        } else {
+#pragma unroll
+            for (int s = 0; s < KPL; ++s) {
+                chosen[s] |= zeros[s];
+                active[s] &= ~zeros[s];
+            }
+            need -= nz;
+            n_active -= nz;
+        }
+    }
+    if (need > 0 && need >= n_active) {
+#pragma unroll
+        for (int s = 0; s < KPL; ++s)
+            chosen[s] |= active[s];
+        need -= n_active;
+    }
+    // equal (padding) keys left over: take the first `need` in entry order
+#pragma unroll
+    for (int s = 0; s < KPL; ++s) {
+        while (need > 0 && active[s] & ~chosen[s]) {
+            const uint32_t m = active[s] & ~chosen[s];
+            chosen[s] |= m & (~m + 1u);
+            --need;
+        }
+    }
+}
+
+// Writes the selected keys to dst[0..) in entry order (slot, then lane).
+template <int KPL>
+__device__ __forceinline__ void warp_compact_keys(const uint64_t (&key)[KPL],
+                                                  const uint32_t (&chosen)[KPL], uint64_t *dst)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t lt = (1u << lane) - 1u;
+    int base = 0;
+#pragma unroll
+    for (int s = 0; s < KPL; ++s) {
+        if ((chosen[s] >> lane) & 1u)
+            dst[base + __popc(chosen[s] & lt)] = key[s];
+        base += __popc(chosen[s]);
+    }
+}
+
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
@@ -269,12 +347,11 @@ struct CompressSmem {
     static constexpr int off_red = off_score + TPC * 4;             // float [TPC]
     static constexpr int off_diag = off_red + TPC * 4;              // float [TPC]
     static constexpr int off_doff = off_diag + TPC * 4;             // int [TPC]
-    static constexpr int off_dst = off_doff + TPC * 4;              // int [TPC]
-    static constexpr int off_hist = off_dst + TPC * 4;              // int [2][256] (remote-read)
-    static constexpr int off_cnt = off_hist + 2 * 256 * 4;          // int [2] (remote-read)
-    static constexpr int off_misc = off_cnt + 4 * 4;                // int [8]
-    static constexpr int off_scan = off_misc + 8 * 4;               // int [NW + 1] (+pad)
-    static constexpr int off_bmove = off_scan + 16 * 4;             // int [NBLK]
+    static constexpr int off_cand = off_doff + TPC * 4;             // u64 [NW][b]
+    static constexpr int off_pub = off_cand + kWarps * kBlk * 8;    // u64 [b] (remote-read)
+    static constexpr int off_ev = off_pub + kBlk * 8;               // int [b]
+    static constexpr int off_misc = off_ev + kBlk * 4;              // int [8]
+    static constexpr int off_bmove = off_misc + 8 * 4;              // int [NBLK]
     static constexpr int off_bar = (off_bmove + NBLK * 4 + 15) / 16 * 16;  // 2 mbarriers
     static constexpr int BYTES = off_bar + 16;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024 B
@@ -304,11 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1) zp_compress_kernel(const Compress
     float *sRed = reinterpret_cast<float *>(sm + S::off_red);
     float *sDiag = reinterpret_cast<float *>(sm + S::off_diag);
     int *sDoff = reinterpret_cast<int *>(sm + S::off_doff);
-    int *sDst = reinterpret_cast<int *>(sm + S::off_dst);
-    int *sHist = reinterpret_cast<int *>(sm + S::off_hist);
-    int *sCnt = reinterpret_cast<int *>(sm + S::off_cnt);
+    uint64_t *sCand = reinterpret_cast<uint64_t *>(sm + S::off_cand);
+    uint64_t *sPub = reinterpret_cast<uint64_t *>(sm + S::off_pub);
+    int *sEv = reinterpret_cast<int *>(sm + S::off_ev);
     int *sMisc = reinterpret_cast<int *>(sm + S::off_misc);
-    int *sScan = reinterpret_cast<int *>(sm + S::off_scan);
     int *sBMove = reinterpret_cast<int *>(sm + S::off_bmove);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::off_bar);
 
@@ -336,8 +412,6 @@ __global__ void __launch_bounds__(kThreads, 1) zp_compress_kernel(const Compress
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
         fence_mbar_init();
-        sCnt[0] = 0;
-        sCnt[1] = 0;
     }
     for (int q = tid; q < NBLK; q += kThreads)
         sBMove[q] = 0;
@@ -547,13 +621,22 @@ __global__ void __launch_bounds__(kThreads, 1) zp_compress_kernel(const Compress
     cluster_sync();  // (1) per-CTA softmax statistics published
 
     if (tid < ROWS) {
+        // all remote loads first, so they are in flight together
+        float mv[kMaxCluster], sv[kMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c) {
+            mv[c] = c < cs ? ld_dsmem_f32(dsmem_addr(sStatM + tid, c)) : -INFINITY;
+            sv[c] = c < cs ? ld_dsmem_f32(dsmem_addr(sStatS + tid, c)) : 0.f;
+        }
         float m = -INFINITY;
-        for (int c = 0; c < cs; ++c)
-            m = fmaxf(m, ld_dsmem_f32(dsmem_addr(sStatM + tid, c)));
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            m = fmaxf(m, mv[c]);
         float s = 0.f;
-        for (int c = 0; c < cs; ++c)
-            s += ld_dsmem_f32(dsmem_addr(sStatS + tid, c)) *
-                 exp2f(ld_dsmem_f32(dsmem_addr(sStatM + tid, c)) - m);
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            if (c < cs)
+                s += sv[c] * exp2f(mv[c] - m);
         sGm[tid] = m;
         sGinv[tid] = tid < a.rows ? 1.0f / s : 0.f;
     }
@@ -585,103 +668,65 @@ __global__ void __launch_bounds__(kThreads, 1) zp_compress_kernel(const Compress
     __syncthreads();
 
     // ---- select: the b lowest candidates under (score ascending, index
-    // descending) are evicted.  4-pass MSB radix select on the order-
-    // preserving image of the fp32 score bits, histograms summed over the
-    // cluster through distributed shared memory.
-    uint32_t u[KPT];
-    bool cand[KPT];
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-        const int k = tid * KPT + j;
-        cand[j] = k < TPC && (t0 + k) < C;
-        u[j] = cand[j] ? f32_order(sScore[k]) : 0u;
-    }
-    uint32_t prefix = 0u, pmask = 0u;
-    int need = kBlk;
-    for (int pass = 0; pass < 4; ++pass) {
-        int *hist = sHist + (pass & 1) * 256;
-        hist[tid] = 0;
-        __syncthreads();
-        const int shift = 24 - 8 * pass;
-#pragma unroll
-        for (int j = 0; j < KPT; ++j)
-            if (cand[j] && (u[j] & pmask) == prefix)
-                atomicAdd(&hist[(u[j] >> shift) & 255u], 1);
-        cluster_sync();  // (2..5) histograms published
-        int tot = 0;
-        for (int c = 0; c < cs; ++c)
-            tot += ld_dsmem_s32(dsmem_addr(hist + tid, c));
-        int all;
-        const int excl = block_excl_scan<kThreads>(tot, sScan, all);
-        if (excl < need && need <= excl + tot) {
-            sMisc[0] = tid;
-            sMisc[1] = need - excl;
-        }
-        __syncthreads();
-        const uint32_t digit = static_cast<uint32_t>(sMisc[0]);
-        need = sMisc[1];
-        prefix |= digit << shift;
-        pmask |= 0xffu << shift;
-    }
-    // prefix is now the image of the b-th lowest score; `need` of the
-    // candidates equal to it are evicted (the highest indices first)
+    // descending) are evicted.  Each candidate carries a distinct 64-bit key:
+    // the order-preserving image of its fp32 score bits above the complement
+    // of its index.  A warp radix select (MSB first, one bit per step, by
+    // ballot) keeps each warp's b smallest keys, warp 0 keeps the CTA's b
+    // smallest of those, and after one cluster barrier warp 0 of every CTA
+    // selects the unit's b smallest among the cluster's candidates.
     {
-        int lt = 0, eq = 0;
+        constexpr int KW = 16 * TW;              // keys per warp
+        constexpr int KPL = (KW + 31) / 32;      // keys per lane
+        uint64_t key[KPL];
 #pragma unroll
-        for (int j = 0; j < KPT; ++j)
-            if (cand[j]) {
-                lt += u[j] < prefix;
-                eq += u[j] == prefix;
+        for (int s = 0; s < KPL; ++s) {
+            const int kk = lane + 32 * s;
+            key[s] = ~0ull;
+            if (kk < KW) {
+                const int k = wi * KW + kk, tok = t0 + k;
+                const uint32_t hi = tok < C ? f32_order(sScore[k]) : 0xffffffffu;
+                key[s] = (static_cast<uint64_t>(hi) << 32) | (0xffffffffu - static_cast<uint32_t>(tok));
             }
-        if (lt)
-            atomicAdd(&sCnt[0], lt);
-        if (eq)
-            atomicAdd(&sCnt[1], eq);
-    }
-    cluster_sync();  // (6) per-CTA counts published
-    if (tid == 0) {
-        int rem = need, take_me = 0, ev_before = 0;
-        for (int c = cs - 1; c >= 0; --c) {
-            const int eq_c = ld_dsmem_s32(dsmem_addr(sCnt + 1, c));
-            const int take = eq_c < rem ? eq_c : rem;
-            rem -= take;
-            if (c == static_cast<int>(crank))
-                take_me = take;
-            if (c < static_cast<int>(crank))
-                ev_before += ld_dsmem_s32(dsmem_addr(sCnt, c)) + take;
         }
-        sMisc[2] = take_me;
-        sMisc[3] = ev_before;
+        uint32_t chosen[KPL];
+        warp_select_smallest<KPL>(key, kBlk, chosen);
+        warp_compact_keys<KPL>(key, chosen, sCand + wi * kBlk);
+    }
+    __syncthreads();
+    if (wi == 0) {
+        uint64_t key[4];
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+            key[s] = sCand[lane + 32 * s];
+        uint32_t chosen[4];
+        warp_select_smallest<4>(key, kBlk, chosen);
+        warp_compact_keys<4>(key, chosen, sPub);
+    }
+    cluster_sync();  // (2) each CTA's b candidates published
+    if (wi == 0) {
+        uint64_t key[4];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            const int e = lane + 32 * s, c = e >> 4;
+            key[s] = c < cs ? ld_dsmem_u64(dsmem_addr(sPub + (e & 15), c)) : ~0ull;
+        }
+        uint32_t chosen[4];
+        warp_select_smallest<4>(key, kBlk, chosen);
+        warp_compact_keys<4>(key, chosen, sCand);  // the unit's b evicted keys
+        __syncwarp();
+        if (lane < kBlk) {
+            const uint32_t mine = 0xffffffffu - static_cast<uint32_t>(sCand[lane]);
+            int rank = 0;
+#pragma unroll
+            for (int i = 0; i < kBlk; ++i)
+                rank += (0xffffffffu - static_cast<uint32_t>(sCand[i])) < mine;
+            sEv[rank] = static_cast<int>(mine);
+        }
     }
     cluster_arrive();  // no remote shared-memory reads after this point
     __syncthreads();
-    const int take_me = sMisc[2], ev_before = sMisc[3];
-    const int eq_cta = sCnt[1];
 
-    bool evict[KPT];
     {
-        int my_eq = 0;
-#pragma unroll
-        for (int j = 0; j < KPT; ++j)
-            my_eq += cand[j] && u[j] == prefix;
-        int tot;
-        int eq_run = block_excl_scan<kThreads>(my_eq, sScan, tot);
-        int my_ev = 0;
-#pragma unroll
-        for (int j = 0; j < KPT; ++j) {
-            bool ev = false;
-            if (cand[j]) {
-                if (u[j] < prefix) {
-                    ev = true;
-                } else if (u[j] == prefix) {
-                    ++eq_run;  // inclusive count of equal candidates up to here
-                    ev = (eq_cta - eq_run) < take_me;
-                }
-            }
-            evict[j] = ev;
-            my_ev += ev;
-        }
-        int ev_run = block_excl_scan<kThreads>(my_ev, sScan, tot) + ev_before;
         const size_t uo = ((size_t)l * a.R + r) * a.Hkv + h;
 #pragma unroll
         for (int j = 0; j < KPT; ++j) {
@@ -689,11 +734,17 @@ __global__ void __launch_bounds__(kThreads, 1) zp_compress_kernel(const Compress
             if (k >= TPC)
                 continue;
             const int tok = t0 + k;
-            int dp = -1, doff = -1;
-            if (evict[j]) {
-                ++ev_run;
-            } else {
-                dp = tok - ev_run;
+            int before = 0;
+            bool ev = false;
+#pragma unroll
+            for (int i = 0; i < kBlk; ++i) {
+                const int e = sEv[i];
+                before += e < tok;
+                ev |= e == tok;
+            }
+            int doff = -1;
+            if (!ev) {
+                const int dp = tok - before;
                 const int dblk = dst_row[dp >> 4];
                 const int sblk = src_row[tok >> 4];
                 if (dp != tok || dblk != sblk) {
@@ -703,7 +754,6 @@ __global__ void __launch_bounds__(kThreads, 1) zp_compress_kernel(const Compress
                 if (a.kept_out)
                     a.kept_out[uo * (size_t)(T - kBlk) + dp] = tok;
             }
-            sDst[k] = dp;
             sDoff[k] = doff;
             if (a.scores_out)
                 a.scores_out[uo * (size_t)T + tok] = (tok < C) ? sScore[k] : INFINITY;

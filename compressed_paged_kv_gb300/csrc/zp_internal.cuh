@@ -261,6 +261,13 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ uint64_t ld_dsmem_u64(uint32_t addr)
+{
+    uint64_t v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ int32_t ld_dsmem_s32(uint32_t addr)
 {
     int32_t v;

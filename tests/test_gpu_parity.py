@@ -153,6 +153,7 @@ def test_fully_shared_request(orc):
     reserved one included): both compress into fresh blocks, the old blocks
     are all freed and stay byte-identical."""
     st = _small_state(R=2, spare_blocks=40)
+    shared = st.block_tables[0].clone()
     old1 = st.block_tables[1].clone()
     st.block_tables[1] = st.block_tables[0]
     st.refcount[st.block_tables[0].long()] = 2
@@ -161,7 +162,7 @@ def test_fully_shared_request(orc):
     st.free_ids[fc:fc + old1.numel()] = old1
     st.free_count += old1.numel()
     H.check_compress(orc, st)
-    assert int(st.refcount[old1.long()].sum()) == 0
+    assert int(st.refcount[shared.long()].sum()) == 0
 
 
 def test_partial_holders(orc):
