@@ -13,7 +13,7 @@ namespace zp {
 
 constexpr int kBlk = 16;            // tokens per block (the only supported size)
 constexpr int kMaxRows = 64;        // window rows per unit: w * (Hq / Hkv)
-constexpr int kMaxCluster = 8;      // CTAs per unit in the compression kernel
+constexpr int kMaxCluster = 16;     // CTAs per unit in the compression kernel
 constexpr uint32_t kWaitSpins = 1u << 22;  // bound on every mbarrier wait
 
 // ----------------------------------------------------------------- workspace
@@ -100,9 +100,19 @@ struct DecodeArgs {
 // Launchers (defined next to their kernels).
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s);
-cudaError_t launch_compress(const CompressArgs &a, int d, int tw, int mt, int units,
+// Chunking of one unit's T tokens: `nw` warps per CTA, `tw` 16-key tiles per
+// warp (tokens per CTA = 16 * nw * tw), `cs` CTAs per cluster.
+struct CompressShape {
+    int nw, tw, cs;
+};
+bool compress_config(int T, bool allow16, CompressShape *out);
+bool compress_cluster16_ok();  // can this device schedule the 16-CTA clusters?
+cudaError_t launch_compress(const CompressArgs &a, int d, CompressShape shape, int mt, int units,
                             cudaStream_t s);
-int compress_tile_words(int T);  // 16-key tiles per warp for T tokens, 0 if unsupported
+cudaError_t launch_compress_d64(const CompressArgs &a, CompressShape shape, int mt, int units,
+                                cudaStream_t s);
+cudaError_t launch_compress_d128(const CompressArgs &a, CompressShape shape, int mt, int units,
+                                 cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t s);
 
 // ------------------------------------------------------------ device helpers
