@@ -22,9 +22,11 @@
 //   4. the b lowest candidates under (score ascending, index descending):
 //      each warp radix-selects its b smallest 64-bit keys (order-preserving
 //      image of the fp32 score bits above the complemented index), the CTA
-//      ranks its warps' candidates, the cluster ranks the CTAs' sorted lists;
+//      ranks its warps' candidates into a sorted list, and b steps of a
+//      k-way merge of the cluster's sorted lists give the unit's b;
 //   5. kept rows are written to their destination slots: K from shared
-//      memory, V through a staging copy.  Exactly b tokens are evicted, so
+//      memory, V through a staging copy (its blocks are prefetched into L2
+//      when the CTA starts).  Exactly b tokens are evicted, so
 //      destination j reads source kept[j] with j <= kept[j] <= j + b.  In-place
 //      writes of the next CTA can only reach this CTA's last block, whose V
 //      rows are staged before the first cluster barrier; every K row is in
@@ -111,23 +113,6 @@ __device__ __forceinline__ void warp_compact_keys(const uint64_t (&key)[KPL],
     }
 }
 
-// Number of entries of the ascending 16-entry list `a` below `key`.
-__device__ __forceinline__ int count_below16(const uint64_t *a, uint64_t key)
-{
-    int p = 0;
-    if (a[p + 7] < key)
-        p += 8;
-    if (a[p + 3] < key)
-        p += 4;
-    if (a[p + 1] < key)
-        p += 2;
-    if (a[p] < key)
-        p += 1;
-    if (p == 15 && a[15] < key)
-        p = 16;
-    return p;
-}
-
 template <int D, int NW, int TW, int MT>
 struct CompressSmem {
     static constexpr int NT = NW * 32;
@@ -141,9 +126,11 @@ struct CompressSmem {
     static constexpr int off_q = off_k + K_BYTES;
     static constexpr int off_vt = off_q + Q_BYTES;
     static constexpr int off_rowa = off_vt + VT_BYTES;              // float [NW][ROWS]
-    static constexpr int off_statm = off_rowa + NW * ROWS * 4;      // float [ROWS] (remote-read)
-    static constexpr int off_stats = off_statm + ROWS * 4;          // float [ROWS] (remote-read)
-    static constexpr int off_gm = off_stats + ROWS * 4;             // float [ROWS]
+    static constexpr int NG = NT / ROWS > 0 ? NT / ROWS : 1;    // stats merge thread groups
+    static constexpr int RA = (NW > NG ? NW : NG) * ROWS;           // sRowA / sPart entries
+    static constexpr int off_stat = off_rowa + RA * 4;              // float2 [ROWS] (remote-read)
+    static constexpr int off_part = off_stat + ROWS * 8;            // float [RA]
+    static constexpr int off_gm = off_part + RA * 4;                // float [ROWS]
     static constexpr int off_ginv = off_gm + ROWS * 4;              // float [ROWS]
     static constexpr int off_score = off_ginv + ROWS * 4;           // float [TPC]
     static constexpr int off_red = off_score + TPC * 4;             // float [TPC]
@@ -179,8 +166,8 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
     uint8_t *sQ = sm + S::off_q;
     uint8_t *sVt = sm + S::off_vt;
     float *sRowA = reinterpret_cast<float *>(sm + S::off_rowa);
-    float *sStatM = reinterpret_cast<float *>(sm + S::off_statm);
-    float *sStatS = reinterpret_cast<float *>(sm + S::off_stats);
+    float2 *sStat = reinterpret_cast<float2 *>(sm + S::off_stat);
+    float *sPart = reinterpret_cast<float *>(sm + S::off_part);
     float *sGm = reinterpret_cast<float *>(sm + S::off_gm);
     float *sGinv = reinterpret_cast<float *>(sm + S::off_ginv);
     float *sScore = reinterpret_cast<float *>(sm + S::off_score);
@@ -244,6 +231,13 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
             const __nv_bfloat16 *vsrc = static_cast<const __nv_bfloat16 *>(a.vpools[l]) +
                                         ((size_t)blk * a.Hkv + h) * kBlk * D;
             bulk_g2s(sVt, vsrc, S::VT_BYTES, &bars[0]);
+        }
+        // the other V blocks are staged much later: start their trip to L2 now
+        for (int q = lane; q < NBLK - 1; q += 32) {
+            const int blk = src_row[blk0 + q];
+            prefetch_l2(static_cast<const __nv_bfloat16 *>(a.vpools[l]) +
+                            ((size_t)blk * a.Hkv + h) * kBlk * D,
+                        kBlk * D * 2);
         }
     }
     {
@@ -357,11 +351,16 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int j = (lane >> 2) + (e >> 1) * 8, k = nt * 8 + (lane & 3) * 2 + (e & 1);
-                if (j == k) {
-                    const float dj = gram[tt][nt][e];
-                    sInvN[key0 + j] = dj > 0.f ? 1.0f / sqrtf(dj) : 0.f;
-                }
+                if (j == k)
+                    sInvN[key0 + j] = gram[tt][nt][e];  // |k_j|^2 for now
             }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int s = 0; s < TW / 2; ++s) {  // one key per lane
+        const int key = wi * TW * 16 + s * 32 + lane;
+        const float dj = sInvN[key];
+        sInvN[key] = dj > 0.f ? 1.0f / sqrtf(dj) : 0.f;
     }
     __syncthreads();
     if (tid < ROWS) {
@@ -419,30 +418,52 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
 #pragma unroll
         for (int w2 = 0; w2 < NW; ++w2)
             s += sRowA[w2 * ROWS + tid];
-        sStatM[tid] = sGm[tid];
-        sStatS[tid] = s;
+        sStat[tid] = make_float2(sGm[tid], s);
     }
     cluster_sync();  // (1) per-CTA softmax statistics published
 
-    for (int t = tid; t < ROWS; t += NT) {
-        // all remote loads first, so they are in flight together
-        float mv[kMaxCluster], sv[kMaxCluster];
+    // merge over the cluster: thread group g takes CTAs g, g+NG, ... (all
+    // remote loads first, so they are in flight together)
+    {
+        constexpr int NG = NT / ROWS > 0 ? NT / ROWS : 1;
+        constexpr int PER = (kMaxCluster + NG - 1) / NG;
+        for (int t = tid; t < ROWS * NG; t += NT) {
+            const int rr = t % ROWS, g = t / ROWS;
+            float2 v[PER];
 #pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c) {
-            mv[c] = c < cs ? ld_dsmem_f32(dsmem_addr(sStatM + t, c)) : -INFINITY;
-            sv[c] = c < cs ? ld_dsmem_f32(dsmem_addr(sStatS + t, c)) : 0.f;
+            for (int i = 0; i < PER; ++i) {
+                const int c = g + i * NG;
+                v[i] = c < cs ? ld_dsmem_f32x2(dsmem_addr(sStat + rr, c))
+                              : make_float2(-INFINITY, 0.f);
+            }
+            float m = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < PER; ++i)
+                m = fmaxf(m, v[i].x);
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < PER; ++i)
+                if (v[i].y > 0.f)
+                    sum += v[i].y * exp2f(v[i].x - m);
+            sRowA[g * ROWS + rr] = m;
+            sPart[g * ROWS + rr] = sum;
         }
-        float m = -INFINITY;
+        __syncthreads();
+        if (tid < ROWS) {
+            float m = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c)
-            m = fmaxf(m, mv[c]);
-        float s = 0.f;
+            for (int g = 0; g < NG; ++g)
+                m = fmaxf(m, sRowA[g * ROWS + tid]);
+            float sum = 0.f;
 #pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c)
-            if (c < cs)
-                s += sv[c] * exp2f(mv[c] - m);
-        sGm[t] = m;
-        sGinv[t] = t < a.rows ? 1.0f / s : 0.f;
+            for (int g = 0; g < NG; ++g) {
+                const float sg = sPart[g * ROWS + tid];
+                if (sg > 0.f)
+                    sum += sg * exp2f(sRowA[g * ROWS + tid] - m);
+            }
+            sGm[tid] = m;
+            sGinv[tid] = tid < a.rows ? 1.0f / sum : 0.f;
+        }
     }
     __syncthreads();
 
@@ -502,14 +523,20 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
         sAll[e] = ld_dsmem_u64(dsmem_addr(sPub + (e & (kBlk - 1)), e / kBlk));
     cluster_arrive();  // no remote shared-memory reads after this point
     __syncthreads();
-    // the unit's b smallest: global rank from the sorted per-CTA lists
-    for (int e = tid; e < cs * kBlk; e += NT) {
-        const uint64_t k0 = sAll[e];
-        int rank = 0;
-        for (int c = 0; c < cs; ++c)
-            rank += count_below16(sAll + c * kBlk, k0);
-        if (rank < kBlk)
-            sEv[rank] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k0));
+    // the unit's b smallest: b steps of a k-way merge of the sorted per-CTA
+    // lists, lane c holding the head of list c
+    if (wi == 0) {
+        int ptr = 0;
+        for (int step = 0; step < kBlk; ++step) {
+            const uint64_t head = (lane < cs && ptr < kBlk) ? sAll[lane * kBlk + ptr] : ~0ull;
+            const uint32_t hi = static_cast<uint32_t>(head >> 32), lo = static_cast<uint32_t>(head);
+            const uint32_t mhi = __reduce_min_sync(0xffffffffu, hi);
+            const uint32_t mlo = __reduce_min_sync(0xffffffffu, hi == mhi ? lo : 0xffffffffu);
+            if (lane < cs && hi == mhi && lo == mlo)
+                ++ptr;
+            if (lane == 0)
+                sEv[step] = static_cast<int>(0xffffffffu - mlo);
+        }
     }
     __syncthreads();
 

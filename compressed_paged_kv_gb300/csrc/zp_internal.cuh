@@ -271,6 +271,19 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ float2 ld_dsmem_f32x2(uint32_t addr)
+{
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+
+// Starts moving [p, p + bytes) from global memory into L2 (no completion).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint64_t ld_dsmem_u64(uint32_t addr)
 {
     uint64_t v;
