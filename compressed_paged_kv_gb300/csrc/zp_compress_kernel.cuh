@@ -8,8 +8,9 @@
 //
 // One unit = (request, layer, kv head) = T = N_max * b cached tokens.  A
 // thread-block cluster of `cs` CTAs owns the unit; CTA c owns tokens
-// [c*TPC, (c+1)*TPC) and keeps their K rows in shared memory (TMA, 128-byte
-// swizzle).  Steps:
+// [c*TPC, (c+1)*TPC) and keeps their K rows in shared memory.  Steps:
+//   0. every K row of the chunk is copied into shared memory by its own bulk
+//      copy (rows padded to d*2+16 bytes so that ldmatrix is conflict-free);
 //   1. logits of the w*G window rows against the CTA's keys and the b x b
 //      Gram of every block, on the tensor cores (mma.sync m16n8k16 bf16,
 //      fp32 accumulate), logits kept in registers in base 2;
@@ -22,11 +23,11 @@
 //   4. the b lowest candidates under (score ascending, index descending):
 //      each warp radix-selects its b smallest 64-bit keys (order-preserving
 //      image of the fp32 score bits above the complemented index), the CTA
-//      ranks its warps' candidates into a sorted list, and b steps of a
-//      k-way merge of the cluster's sorted lists give the unit's b;
-//   5. kept rows are written to their destination slots: K from shared
-//      memory, V through a staging copy (its blocks are prefetched into L2
-//      when the CTA starts).  Exactly b tokens are evicted, so
+//      ranks its warps' candidates into a sorted list, and each of the
+//      cluster's candidates is ranked against all sorted lists;
+//   5. kept rows are written to their destination slots by one bulk copy
+//      per row: K from shared memory, V through a staging copy (its blocks
+//      are prefetched into L2 when the CTA starts).  Exactly b tokens are evicted, so
 //      destination j reads source kept[j] with j <= kept[j] <= j + b.  In-place
 //      writes of the next CTA can only reach this CTA's last block, whose V
 //      rows are staged before the first cluster barrier; every K row is in
@@ -113,15 +114,33 @@ __device__ __forceinline__ void warp_compact_keys(const uint64_t (&key)[KPL],
     }
 }
 
+// Number of entries of the ascending 16-entry list `a` below `key`.
+__device__ __forceinline__ int count_below16(const uint64_t *a, uint64_t key)
+{
+    int p = 0;
+    if (a[p + 7] < key)
+        p += 8;
+    if (a[p + 3] < key)
+        p += 4;
+    if (a[p + 1] < key)
+        p += 2;
+    if (a[p] < key)
+        p += 1;
+    if (p == 15 && a[15] < key)
+        p = 16;
+    return p;
+}
+
 template <int D, int NW, int TW, int MT>
 struct CompressSmem {
     static constexpr int NT = NW * 32;
     static constexpr int TPC = NW * TW * 16;  // tokens per CTA
     static constexpr int NBLK = TPC / kBlk;
     static constexpr int ROWS = MT * 16;
-    static constexpr int K_BYTES = TPC * D * 2;
+    static constexpr int RS = D * 2 + 16;  // padded row stride: conflict-free ldmatrix
+    static constexpr int K_BYTES = TPC * RS;
     static constexpr int Q_BYTES = ROWS * D * 2;
-    static constexpr int VT_BYTES = kBlk * D * 2;
+    static constexpr int VT_BYTES = kBlk * RS;
     static constexpr int off_k = 0;
     static constexpr int off_q = off_k + K_BYTES;
     static constexpr int off_vt = off_q + Q_BYTES;
@@ -154,8 +173,9 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
 {
     using S = CompressSmem<D, NW, TW, MT>;
     constexpr int NT = S::NT, TPC = S::TPC, NBLK = S::NBLK, ROWS = S::ROWS;
-    constexpr int HALVES = D / 64;
+    constexpr int RS = S::RS;
     constexpr int CPR = D / 8;           // 16-byte chunks per row
+    constexpr uint32_t ROW_BYTES = D * 2;
     constexpr int KPT = TPC / NT;        // keys per thread (TW / 2)
     static_assert(TW % 2 == 0 && KPT >= 1, "two or more 16-key tiles per warp");
 
@@ -206,39 +226,30 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
         fence_mbar_init();
+        mbar_arrive_expect_tx(&bars[0], (TPC + kBlk) * ROW_BYTES);
     }
     for (int q = tid; q < NBLK; q += NT)
         sBMove[q] = 0;
     __syncthreads();
 
-    // ---- loads: K chunk (TMA, swizzled), the V rows of the chunk's last
-    // block (bulk copy; the next CTA may overwrite them in place later), and
-    // the window queries (plain loads into the same swizzled layout).
-    if (wi == 0) {
-        const CUtensorMap *kmap = a.kmaps + l;
-        if (lane == 0)
-            mbar_arrive_expect_tx(&bars[0], S::K_BYTES + S::VT_BYTES);
-        __syncwarp();
-        for (int q = lane; q < NBLK; q += 32) {
-            const int blk = src_row[blk0 + q];
-            const int y = (blk * a.Hkv + h) * kBlk;
-#pragma unroll
-            for (int hf = 0; hf < HALVES; ++hf)
-                tma_load_2d(sK + hf * TPC * 128 + q * kBlk * 128, kmap, hf * 64, y, &bars[0]);
-        }
-        if (lane == 0) {
-            const int blk = src_row[blk0 + NBLK - 1];
-            const __nv_bfloat16 *vsrc = static_cast<const __nv_bfloat16 *>(a.vpools[l]) +
-                                        ((size_t)blk * a.Hkv + h) * kBlk * D;
-            bulk_g2s(sVt, vsrc, S::VT_BYTES, &bars[0]);
-        }
-        // the other V blocks are staged much later: start their trip to L2 now
-        for (int q = lane; q < NBLK - 1; q += 32) {
-            const int blk = src_row[blk0 + q];
-            prefetch_l2(static_cast<const __nv_bfloat16 *>(a.vpools[l]) +
-                            ((size_t)blk * a.Hkv + h) * kBlk * D,
-                        kBlk * D * 2);
-        }
+    // ---- loads, one bulk copy per 256-byte row into padded shared rows: the
+    // K chunk, the V rows of the chunk's last block (the next CTA may
+    // overwrite them in place later), and an L2 prefetch of the other V
+    // blocks (staged much later); the window queries by plain loads.
+    const __nv_bfloat16 *kpool_in = static_cast<const __nv_bfloat16 *>(a.kpools[l]);
+    const __nv_bfloat16 *vpool_in = static_cast<const __nv_bfloat16 *>(a.vpools[l]);
+    for (int k = tid; k < TPC; k += NT) {
+        const int blk = src_row[blk0 + (k >> 4)];
+        bulk_g2s(sK + k * RS, kpool_in + (((size_t)blk * a.Hkv + h) * kBlk + (k & 15)) * D,
+                 ROW_BYTES, &bars[0]);
+    }
+    if (tid < kBlk) {
+        const int blk = src_row[blk0 + NBLK - 1];
+        bulk_g2s(sVt + tid * RS, vpool_in + (((size_t)blk * a.Hkv + h) * kBlk + tid) * D,
+                 ROW_BYTES, &bars[0]);
+    } else if (tid >= 32 && tid < 32 + NBLK - 1) {
+        const int blk = src_row[blk0 + tid - 32];
+        prefetch_l2(vpool_in + ((size_t)blk * a.Hkv + h) * kBlk * D, kBlk * ROW_BYTES);
     }
     {
         const __nv_bfloat16 *qsrc =
@@ -288,7 +299,8 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
             for (int tt = 0; tt < TW; ++tt) {
                 const int key0 = (wi * TW + tt) * 16;
                 uint32_t kb[4];
-                ldsm_x4(kb_base + swz(key0 + (mi >> 1) * 8 + (lane & 7), ks * 2 + (mi & 1), TPC), kb);
+                ldsm_x4(kb_base + (key0 + (mi >> 1) * 8 + (lane & 7)) * RS + (ks * 2 + (mi & 1)) * 16,
+                        kb);
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
                     mma_bf16(acc[mt][tt][0], qa[mt][0], qa[mt][1], qa[mt][2], qa[mt][3], kb[0], kb[1]);
@@ -523,20 +535,17 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
         sAll[e] = ld_dsmem_u64(dsmem_addr(sPub + (e & (kBlk - 1)), e / kBlk));
     cluster_arrive();  // no remote shared-memory reads after this point
     __syncthreads();
-    // the unit's b smallest: b steps of a k-way merge of the sorted per-CTA
-    // lists, lane c holding the head of list c
-    if (wi == 0) {
-        int ptr = 0;
-        for (int step = 0; step < kBlk; ++step) {
-            const uint64_t head = (lane < cs && ptr < kBlk) ? sAll[lane * kBlk + ptr] : ~0ull;
-            const uint32_t hi = static_cast<uint32_t>(head >> 32), lo = static_cast<uint32_t>(head);
-            const uint32_t mhi = __reduce_min_sync(0xffffffffu, hi);
-            const uint32_t mlo = __reduce_min_sync(0xffffffffu, hi == mhi ? lo : 0xffffffffu);
-            if (lane < cs && hi == mhi && lo == mlo)
-                ++ptr;
-            if (lane == 0)
-                sEv[step] = static_cast<int>(0xffffffffu - mlo);
-        }
+    // the unit's b smallest: the global rank of each candidate, counted in
+    // every sorted per-CTA list by binary search (the searches interleave)
+    for (int e = tid; e < cs * kBlk; e += NT) {
+        const uint64_t k0 = sAll[e];
+        int rank = 0;
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            if (c < cs)
+                rank += count_below16(sAll + c * kBlk, k0);
+        if (rank < kBlk)
+            sEv[rank] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k0));
     }
     __syncthreads();
 
@@ -573,68 +582,53 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
     }
     __syncthreads();
 
-    // ---- 5. compaction: K rows from shared memory
+    // ---- 5. compaction: one bulk copy per moved row.  K from shared memory.
+    __nv_bfloat16 *kpool = static_cast<__nv_bfloat16 *>(a.kpools[l]);
+    __nv_bfloat16 *vpool = static_cast<__nv_bfloat16 *>(a.vpools[l]);
     if (!bad) {
-        __nv_bfloat16 *kpool = static_cast<__nv_bfloat16 *>(a.kpools[l]);
-        const uint32_t kb_base = smem_u32(sK);
-        for (int c = tid; c < TPC * CPR; c += NT) {
-            const int k = c / CPR, ch = c - k * CPR;
+        for (int k = tid; k < TPC; k += NT) {
             const int doff = sDoff[k];
-            if (doff < 0)
-                continue;
-            const uint4 v = ld_shared_v4(kb_base + swz(k, ch, TPC));
-            st_global_v4(kpool + (size_t)doff * D + ch * 8, v);
+            if (doff >= 0)
+                bulk_s2g(kpool + (size_t)doff * D, sK + k * RS, ROW_BYTES);
         }
     }
+    bulk_commit();
+    bulk_wait_read0();  // the K rows have been read out of shared memory
     fence_proxy_async_smem();
     __syncthreads();
 
-    // V rows of the moved tokens: stage the source blocks (except the last,
-    // already staged) into the K buffer, then scatter.
-    if (wi == 0) {
-        int nv = 0;
-        for (int q = lane; q < NBLK - 1; q += 32)
-            nv += (!bad && sBMove[q]) ? 1 : 0;
+    // V rows of the moved tokens (outside the already staged last block) into
+    // the K rows' place, then out to their destinations.
+    int nv = 0;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            nv += __shfl_xor_sync(0xffffffffu, nv, o);
-        if (lane == 0) {
-            sMisc[4] = nv;
-            if (nv > 0)
-                mbar_arrive_expect_tx(&bars[1], nv * kBlk * D * 2);
+    for (int j = 0; j < KPT; ++j) {
+        const int k = tid * KPT + j;
+        const bool mv = !bad && k < TPC - kBlk && sDoff[k] >= 0;
+        if (mv) {
+            const int blk = src_row[blk0 + (k >> 4)];
+            bulk_g2s(sK + k * RS, vpool_in + (((size_t)blk * a.Hkv + h) * kBlk + (k & 15)) * D,
+                     ROW_BYTES, &bars[1]);
         }
-        __syncwarp();
-        if (nv > 0) {
-            for (int q = lane; q < NBLK - 1; q += 32) {
-                if (!sBMove[q])
-                    continue;
-                const int blk = src_row[blk0 + q];
-                const __nv_bfloat16 *vsrc = static_cast<const __nv_bfloat16 *>(a.vpools[l]) +
-                                            ((size_t)blk * a.Hkv + h) * kBlk * D;
-                bulk_g2s(sK + q * kBlk * D * 2, vsrc, kBlk * D * 2, &bars[1]);
-            }
-        }
+        nv += __syncthreads_count(mv);
     }
-    __syncthreads();
-    if (sMisc[4] > 0)
+    if (tid == 0 && nv > 0)
+        mbar_arrive_expect_tx(&bars[1], nv * ROW_BYTES);
+    if (nv > 0)
         bad |= !mbar_wait(&bars[1], 0);
     bad = __syncthreads_or(bad);
     if (!bad) {
-        __nv_bfloat16 *vpool = static_cast<__nv_bfloat16 *>(a.vpools[l]);
-        const uint32_t v_base = smem_u32(sK), vt_base = smem_u32(sVt);
-        for (int c = tid; c < TPC * CPR; c += NT) {
-            const int k = c / CPR, ch = c - k * CPR;
+        for (int k = tid; k < TPC; k += NT) {
             const int doff = sDoff[k];
-            if (doff < 0)
-                continue;
-            const uint32_t src = (k >= TPC - kBlk) ? vt_base + ((k - (TPC - kBlk)) * CPR + ch) * 16
-                                                   : v_base + (k * CPR + ch) * 16;
-            st_global_v4(vpool + (size_t)doff * D + ch * 8, ld_shared_v4(src));
+            if (doff >= 0)
+                bulk_s2g(vpool + (size_t)doff * D,
+                         k >= TPC - kBlk ? sVt + (k - (TPC - kBlk)) * RS : sK + k * RS, ROW_BYTES);
         }
     } else if (tid == 0) {
         set_error(a.call, ZP_ERR_TIMEOUT);
         set_error(a.sticky, ZP_ERR_TIMEOUT);
     }
+    bulk_commit();
+    bulk_wait_read0();
     cluster_wait();  // peers may still read this CTA's shared memory until here
 }
 
