@@ -114,23 +114,6 @@ __device__ __forceinline__ void warp_compact_keys(const uint64_t (&key)[KPL],
     }
 }
 
-// Number of entries of the ascending 16-entry list `a` below `key`.
-__device__ __forceinline__ int count_below16(const uint64_t *a, uint64_t key)
-{
-    int p = 0;
-    if (a[p + 7] < key)
-        p += 8;
-    if (a[p + 3] < key)
-        p += 4;
-    if (a[p + 1] < key)
-        p += 2;
-    if (a[p] < key)
-        p += 1;
-    if (p == 15 && a[15] < key)
-        p = 16;
-    return p;
-}
-
 template <int D, int NW, int TW, int MT>
 struct CompressSmem {
     static constexpr int NT = NW * 32;
@@ -161,8 +144,8 @@ struct CompressSmem {
     static constexpr int off_ev = off_all + kMaxCluster * kBlk * 8;  // int [b]
     static constexpr int off_misc = off_ev + kBlk * 4;              // int [8]
     static constexpr int off_bmove = off_misc + 8 * 4;              // int [NBLK]
-    static constexpr int off_bar = (off_bmove + NBLK * 4 + 15) / 16 * 16;  // 2 mbarriers
-    static constexpr int BYTES = off_bar + 16;
+    static constexpr int off_bar = (off_bmove + NBLK * 4 + 15) / 16 * 16;  // 1 + NT mbarriers
+    static constexpr int BYTES = off_bar + 8 + NT * 8;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024 B
     static constexpr int MIN_BLOCKS = NW == 4 ? (TW <= 2 ? 4 : 2) : (TW <= 2 ? 2 : 1);
 };
@@ -201,6 +184,7 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
     int *sMisc = reinterpret_cast<int *>(sm + S::off_misc);
     int *sBMove = reinterpret_cast<int *>(sm + S::off_bmove);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::off_bar);
+    uint64_t *sVbar = bars + 1;  // one per thread: its V rows
 
     const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
     const int cs = a.cs;
@@ -222,14 +206,12 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
     const int blk0 = t0 / kBlk;
     const int G = a.Hq / a.Hkv;
 
-    if (tid == 0) {
+    mbar_init(&sVbar[tid], 1);
+    if (tid == 0)
         mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        fence_mbar_init();
+    fence_mbar_init();
+    if (tid == 0)
         mbar_arrive_expect_tx(&bars[0], (TPC + kBlk) * ROW_BYTES);
-    }
-    for (int q = tid; q < NBLK; q += NT)
-        sBMove[q] = 0;
     __syncthreads();
 
     // ---- loads, one bulk copy per 256-byte row into padded shared rows: the
@@ -247,9 +229,26 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
         const int blk = src_row[blk0 + NBLK - 1];
         bulk_g2s(sVt + tid * RS, vpool_in + (((size_t)blk * a.Hkv + h) * kBlk + tid) * D,
                  ROW_BYTES, &bars[0]);
-    } else if (tid >= 32 && tid < 32 + NBLK - 1) {
-        const int blk = src_row[blk0 + tid - 32];
-        prefetch_l2(vpool_in + ((size_t)blk * a.Hkv + h) * kBlk * D, kBlk * ROW_BYTES);
+    } else if (tid >= 32 && tid < 32 + 2 * NBLK) {
+        // L2 prefetch of the K and V blocks of the same chunk of the unit one
+        // resident wave ahead (that CTA then loads from L2), or of this
+        // chunk's V blocks in the first wave
+        const int q = (tid - 32) >> 1;
+        const bool is_v = (tid - 32) & 1;
+        const int ahead = unit + a.prefetch_ahead;
+        if (ahead < a.units) {
+            const int ah = ahead % a.Hkv, al = (ahead / a.Hkv) % a.L, ar = ahead / (a.Hkv * a.L);
+            const int arow = a.req_idx ? a.req_idx[ar] : ar;
+            const int blk = a.tables[(size_t)arow * a.stride + blk0 + q];
+            const void *pool = is_v ? a.vpools[al] : a.kpools[al];
+            prefetch_l2(static_cast<const __nv_bfloat16 *>(pool) +
+                            ((size_t)blk * a.Hkv + ah) * kBlk * D,
+                        kBlk * ROW_BYTES);
+        }
+        if (is_v && unit < a.prefetch_ahead && q < NBLK - 1) {
+            const int blk = src_row[blk0 + q];
+            prefetch_l2(vpool_in + ((size_t)blk * a.Hkv + h) * kBlk * D, kBlk * ROW_BYTES);
+        }
     }
     {
         const __nv_bfloat16 *qsrc =
@@ -535,17 +534,20 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
         sAll[e] = ld_dsmem_u64(dsmem_addr(sPub + (e & (kBlk - 1)), e / kBlk));
     cluster_arrive();  // no remote shared-memory reads after this point
     __syncthreads();
-    // the unit's b smallest: the global rank of each candidate, counted in
-    // every sorted per-CTA list by binary search (the searches interleave)
-    for (int e = tid; e < cs * kBlk; e += NT) {
-        const uint64_t k0 = sAll[e];
-        int rank = 0;
-#pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c)
-            if (c < cs)
-                rank += count_below16(sAll + c * kBlk, k0);
-        if (rank < kBlk)
-            sEv[rank] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k0));
+    // the unit's b smallest: b steps of a k-way merge of the sorted per-CTA
+    // lists, lane c holding the head of list c
+    if (wi == 0) {
+        int ptr = 0;
+        for (int step = 0; step < kBlk; ++step) {
+            const uint64_t head = (lane < cs && ptr < kBlk) ? sAll[lane * kBlk + ptr] : ~0ull;
+            const uint32_t hi = static_cast<uint32_t>(head >> 32), lo = static_cast<uint32_t>(head);
+            const uint32_t mhi = __reduce_min_sync(0xffffffffu, hi);
+            const uint32_t mlo = __reduce_min_sync(0xffffffffu, hi == mhi ? lo : 0xffffffffu);
+            if (lane < cs && hi == mhi && lo == mlo)
+                ++ptr;
+            if (lane == 0)
+                sEv[step] = static_cast<int>(0xffffffffu - mlo);
+        }
     }
     __syncthreads();
 
@@ -568,10 +570,8 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
                 const int dp = tok - before;
                 const int dblk = dst_row[dp >> 4];
                 const int sblk = src_row[tok >> 4];
-                if (dp != tok || dblk != sblk) {
+                if (dp != tok || dblk != sblk)
                     doff = (dblk * a.Hkv + h) * kBlk + (dp & 15);
-                    sBMove[k >> 4] = 1;
-                }
                 if (a.kept_out)
                     a.kept_out[uo * (size_t)(T - kBlk) + dp] = tok;
             }
@@ -582,52 +582,62 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
     }
     __syncthreads();
 
-    // ---- 5. compaction: one bulk copy per moved row.  K from shared memory.
+    // ---- 5. compaction: one bulk copy per moved row.  Each thread owns its
+    // rows: K goes out of shared memory, then (once that copy has read the
+    // row) the V row is staged in its place and goes out too.  Rows of the
+    // last block take their V from the rows staged at the start.
     __nv_bfloat16 *kpool = static_cast<__nv_bfloat16 *>(a.kpools[l]);
     __nv_bfloat16 *vpool = static_cast<__nv_bfloat16 *>(a.vpools[l]);
     if (!bad) {
-        for (int k = tid; k < TPC; k += NT) {
-            const int doff = sDoff[k];
-            if (doff >= 0)
-                bulk_s2g(kpool + (size_t)doff * D, sK + k * RS, ROW_BYTES);
-        }
-    }
-    bulk_commit();
-    bulk_wait_read0();  // the K rows have been read out of shared memory
-    fence_proxy_async_smem();
-    __syncthreads();
-
-    // V rows of the moved tokens (outside the already staged last block) into
-    // the K rows' place, then out to their destinations.
-    int nv = 0;
+        int doffs[KPT];
 #pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-        const int k = tid * KPT + j;
-        const bool mv = !bad && k < TPC - kBlk && sDoff[k] >= 0;
-        if (mv) {
-            const int blk = src_row[blk0 + (k >> 4)];
-            bulk_g2s(sK + k * RS, vpool_in + (((size_t)blk * a.Hkv + h) * kBlk + (k & 15)) * D,
-                     ROW_BYTES, &bars[1]);
+        for (int j = 0; j < KPT; ++j) {
+            const int k = tid * KPT + j;
+            doffs[j] = sDoff[k];
+            if (doffs[j] >= 0)
+                bulk_s2g(kpool + (size_t)doffs[j] * D, sK + k * RS, ROW_BYTES);
         }
-        nv += __syncthreads_count(mv);
-    }
-    if (tid == 0 && nv > 0)
-        mbar_arrive_expect_tx(&bars[1], nv * ROW_BYTES);
-    if (nv > 0)
-        bad |= !mbar_wait(&bars[1], 0);
-    bad = __syncthreads_or(bad);
-    if (!bad) {
-        for (int k = tid; k < TPC; k += NT) {
-            const int doff = sDoff[k];
-            if (doff >= 0)
-                bulk_s2g(vpool + (size_t)doff * D,
-                         k >= TPC - kBlk ? sVt + (k - (TPC - kBlk)) * RS : sK + k * RS, ROW_BYTES);
+        bulk_commit();
+        int staged = 0;
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) {
+            const int k = tid * KPT + j;
+            if (doffs[j] >= 0 && k >= TPC - kBlk)
+                bulk_s2g(vpool + (size_t)doffs[j] * D, sVt + (k - (TPC - kBlk)) * RS, ROW_BYTES);
+            else if (doffs[j] >= 0)
+                ++staged;
         }
+        if (staged > 0) {
+            bulk_wait_read0();  // this thread's K rows have left shared memory
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&sVbar[tid], staged * ROW_BYTES);
+#pragma unroll
+            for (int j = 0; j < KPT; ++j) {
+                const int k = tid * KPT + j;
+                if (doffs[j] >= 0 && k < TPC - kBlk) {
+                    const int blk = src_row[blk0 + (k >> 4)];
+                    bulk_g2s(sK + k * RS,
+                             vpool_in + (((size_t)blk * a.Hkv + h) * kBlk + (k & 15)) * D,
+                             ROW_BYTES, &sVbar[tid]);
+                }
+            }
+            if (mbar_wait(&sVbar[tid], 0)) {
+#pragma unroll
+                for (int j = 0; j < KPT; ++j) {
+                    const int k = tid * KPT + j;
+                    if (doffs[j] >= 0 && k < TPC - kBlk)
+                        bulk_s2g(vpool + (size_t)doffs[j] * D, sK + k * RS, ROW_BYTES);
+                }
+            } else {
+                set_error(a.call, ZP_ERR_TIMEOUT);
+                set_error(a.sticky, ZP_ERR_TIMEOUT);
+            }
+        }
+        bulk_commit();
     } else if (tid == 0) {
         set_error(a.call, ZP_ERR_TIMEOUT);
         set_error(a.sticky, ZP_ERR_TIMEOUT);
     }
-    bulk_commit();
     bulk_wait_read0();
     cluster_wait();  // peers may still read this CTA's shared memory until here
 }
@@ -688,6 +698,52 @@ bool cluster16_ok_t()
         return false;
     }
     return n > 0;
+}
+
+// Clusters of `cs` CTAs of this kernel that the device can hold at once.
+template <int D, int NW, int TW, int MT>
+int resident_clusters_t(int cs)
+{
+    using Sm = CompressSmem<D, NW, TW, MT>;
+    auto kern = zp_compress_kernel<D, NW, TW, MT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::ALLOC) !=
+            cudaSuccess ||
+        (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                       cudaSuccess)) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cs) * 1024u, 1, 1);
+    cfg.blockDim = dim3(Sm::NT, 1, 1);
+    cfg.dynamicSmemBytes = Sm::ALLOC;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int D>
+int resident_clusters_for_d(CompressShape sh, int mt)
+{
+#define ZP_CASE(NW_, TW_, MT_)                                    \
+    if (sh.nw == NW_ && sh.tw == TW_ && mt == MT_)                 \
+        return resident_clusters_t<D, NW_, TW_, MT_>(sh.cs);
+    ZP_CASE(4, 2, 1) ZP_CASE(4, 2, 2) ZP_CASE(4, 2, 4)
+    ZP_CASE(4, 4, 1) ZP_CASE(4, 4, 2) ZP_CASE(4, 4, 4)
+    ZP_CASE(8, 2, 1) ZP_CASE(8, 2, 2) ZP_CASE(8, 2, 4)
+    ZP_CASE(8, 4, 1) ZP_CASE(8, 4, 2) ZP_CASE(8, 4, 4)
+#undef ZP_CASE
+    return 0;
 }
 
 template <int D>
