@@ -26,8 +26,9 @@
 //      ranks its warps' candidates into a sorted list, and each of the
 //      cluster's candidates is ranked against all sorted lists;
 //   5. kept rows are written to their destination slots by one bulk copy
-//      per row: K from shared memory, V through a staging copy (its blocks
-//      are prefetched into L2 when the CTA starts).  Exactly b tokens are evicted, so
+//      per row: K from shared memory, V through a staging copy.  During its
+//      compute phases a CTA prefetches into L2 the K and V blocks of the
+//      unit one resident wave ahead, so memory does not idle between waves.  Exactly b tokens are evicted, so
 //      destination j reads source kept[j] with j <= kept[j] <= j + b.  In-place
 //      writes of the next CTA can only reach this CTA's last block, whose V
 //      rows are staged before the first cluster barrier; every K row is in
@@ -229,26 +230,6 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
         const int blk = src_row[blk0 + NBLK - 1];
         bulk_g2s(sVt + tid * RS, vpool_in + (((size_t)blk * a.Hkv + h) * kBlk + tid) * D,
                  ROW_BYTES, &bars[0]);
-    } else if (tid >= 32 && tid < 32 + 2 * NBLK) {
-        // L2 prefetch of the K and V blocks of the same chunk of the unit one
-        // resident wave ahead (that CTA then loads from L2), or of this
-        // chunk's V blocks in the first wave
-        const int q = (tid - 32) >> 1;
-        const bool is_v = (tid - 32) & 1;
-        const int ahead = unit + a.prefetch_ahead;
-        if (ahead < a.units) {
-            const int ah = ahead % a.Hkv, al = (ahead / a.Hkv) % a.L, ar = ahead / (a.Hkv * a.L);
-            const int arow = a.req_idx ? a.req_idx[ar] : ar;
-            const int blk = a.tables[(size_t)arow * a.stride + blk0 + q];
-            const void *pool = is_v ? a.vpools[al] : a.kpools[al];
-            prefetch_l2(static_cast<const __nv_bfloat16 *>(pool) +
-                            ((size_t)blk * a.Hkv + ah) * kBlk * D,
-                        kBlk * ROW_BYTES);
-        }
-        if (is_v && unit < a.prefetch_ahead && q < NBLK - 1) {
-            const int blk = src_row[blk0 + q];
-            prefetch_l2(vpool_in + ((size_t)blk * a.Hkv + h) * kBlk * D, kBlk * ROW_BYTES);
-        }
     }
     {
         const __nv_bfloat16 *qsrc =
@@ -308,6 +289,29 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
                 mma_bf16(gram[tt][0], kb[0], kb[2], kb[1], kb[3], kb[0], kb[1]);
                 mma_bf16(gram[tt][1], kb[0], kb[2], kb[1], kb[3], kb[2], kb[3]);
             }
+        }
+    }
+
+    // While this CTA computes, memory would idle: start moving into L2 the K
+    // and V blocks of the same chunk of the unit one resident wave ahead
+    // (that CTA then loads from L2), and in the first wave this chunk's own V
+    // blocks (staged at the end).
+    if (tid >= 32 && tid < 32 + 2 * NBLK) {
+        const int q = (tid - 32) >> 1;
+        const bool is_v = (tid - 32) & 1;
+        const int ahead = unit + a.prefetch_ahead;
+        if (ahead < a.units) {
+            const int ah = ahead % a.Hkv, al = (ahead / a.Hkv) % a.L, ar = ahead / (a.Hkv * a.L);
+            const int arow = a.req_idx ? a.req_idx[ar] : ar;
+            const int blk = a.tables[(size_t)arow * a.stride + blk0 + q];
+            const void *pool = is_v ? a.vpools[al] : a.kpools[al];
+            prefetch_l2(static_cast<const __nv_bfloat16 *>(pool) +
+                            ((size_t)blk * a.Hkv + ah) * kBlk * D,
+                        kBlk * ROW_BYTES);
+        }
+        if (is_v && unit < a.prefetch_ahead && q < NBLK - 1) {
+            const int blk = src_row[blk0 + q];
+            prefetch_l2(vpool_in + ((size_t)blk * a.Hkv + h) * kBlk * D, kBlk * ROW_BYTES);
         }
     }
 
@@ -582,62 +586,56 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
     }
     __syncthreads();
 
-    // ---- 5. compaction: one bulk copy per moved row.  Each thread owns its
-    // rows: K goes out of shared memory, then (once that copy has read the
-    // row) the V row is staged in its place and goes out too.  Rows of the
-    // last block take their V from the rows staged at the start.
+    // ---- 5. compaction: one bulk copy per moved row.  K goes out of shared
+    // memory; once a thread's K copies have read its rows, the V rows it owns
+    // (outside the last block, staged at the start) are staged in their place.
+    // In-place destinations overlap sources of this CTA, so no V row goes out
+    // before every V row of the CTA has been staged.
     __nv_bfloat16 *kpool = static_cast<__nv_bfloat16 *>(a.kpools[l]);
     __nv_bfloat16 *vpool = static_cast<__nv_bfloat16 *>(a.vpools[l]);
+    int doffs[KPT];
+#pragma unroll
+    for (int j = 0; j < KPT; ++j)
+        doffs[j] = bad ? -1 : sDoff[tid * KPT + j];
+#pragma unroll
+    for (int j = 0; j < KPT; ++j)
+        if (doffs[j] >= 0)
+            bulk_s2g(kpool + (size_t)doffs[j] * D, sK + (tid * KPT + j) * RS, ROW_BYTES);
+    bulk_commit();
+    int staged = 0;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j)
+        staged += doffs[j] >= 0 && tid * KPT + j < TPC - kBlk;
+    bool vok = true;
+    if (staged > 0) {
+        bulk_wait_read0();  // this thread's K rows have left shared memory
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&sVbar[tid], staged * ROW_BYTES);
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) {
+            const int k = tid * KPT + j;
+            if (doffs[j] >= 0 && k < TPC - kBlk) {
+                const int blk = src_row[blk0 + (k >> 4)];
+                bulk_g2s(sK + k * RS, vpool_in + (((size_t)blk * a.Hkv + h) * kBlk + (k & 15)) * D,
+                         ROW_BYTES, &sVbar[tid]);
+            }
+        }
+        vok = mbar_wait(&sVbar[tid], 0);
+    }
+    bad = __syncthreads_or(bad || !vok);
     if (!bad) {
-        int doffs[KPT];
 #pragma unroll
         for (int j = 0; j < KPT; ++j) {
             const int k = tid * KPT + j;
-            doffs[j] = sDoff[k];
             if (doffs[j] >= 0)
-                bulk_s2g(kpool + (size_t)doffs[j] * D, sK + k * RS, ROW_BYTES);
+                bulk_s2g(vpool + (size_t)doffs[j] * D,
+                         k >= TPC - kBlk ? sVt + (k - (TPC - kBlk)) * RS : sK + k * RS, ROW_BYTES);
         }
-        bulk_commit();
-        int staged = 0;
-#pragma unroll
-        for (int j = 0; j < KPT; ++j) {
-            const int k = tid * KPT + j;
-            if (doffs[j] >= 0 && k >= TPC - kBlk)
-                bulk_s2g(vpool + (size_t)doffs[j] * D, sVt + (k - (TPC - kBlk)) * RS, ROW_BYTES);
-            else if (doffs[j] >= 0)
-                ++staged;
-        }
-        if (staged > 0) {
-            bulk_wait_read0();  // this thread's K rows have left shared memory
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&sVbar[tid], staged * ROW_BYTES);
-#pragma unroll
-            for (int j = 0; j < KPT; ++j) {
-                const int k = tid * KPT + j;
-                if (doffs[j] >= 0 && k < TPC - kBlk) {
-                    const int blk = src_row[blk0 + (k >> 4)];
-                    bulk_g2s(sK + k * RS,
-                             vpool_in + (((size_t)blk * a.Hkv + h) * kBlk + (k & 15)) * D,
-                             ROW_BYTES, &sVbar[tid]);
-                }
-            }
-            if (mbar_wait(&sVbar[tid], 0)) {
-#pragma unroll
-                for (int j = 0; j < KPT; ++j) {
-                    const int k = tid * KPT + j;
-                    if (doffs[j] >= 0 && k < TPC - kBlk)
-                        bulk_s2g(vpool + (size_t)doffs[j] * D, sK + k * RS, ROW_BYTES);
-                }
-            } else {
-                set_error(a.call, ZP_ERR_TIMEOUT);
-                set_error(a.sticky, ZP_ERR_TIMEOUT);
-            }
-        }
-        bulk_commit();
     } else if (tid == 0) {
         set_error(a.call, ZP_ERR_TIMEOUT);
         set_error(a.sticky, ZP_ERR_TIMEOUT);
     }
+    bulk_commit();
     bulk_wait_read0();
     cluster_wait();  // peers may still read this CTA's shared memory until here
 }
