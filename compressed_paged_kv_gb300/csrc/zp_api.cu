@@ -293,12 +293,6 @@ zp_status zp_compress(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int
     ca.w = window;
     ca.rows = rows;
     ca.cs = cs;
-    ca.units = static_cast<int32_t>(units);
-    {
-        // prefetch distance: one wave of resident clusters (one unit each)
-        const int resident = zp::compress_resident_clusters(c->d, shape, mt);
-        ca.prefetch_ahead = resident > 0 ? resident : std::max(1, 4 * c->num_sms / cs);
-    }
     ca.lambda = lambda;
     ca.inv_rows = 1.0f / static_cast<float>(rows);
     ca.logit_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c->d)));

@@ -286,26 +286,6 @@ bool compress_config(int T, bool allow16, CompressShape *out)
     return true;
 }
 
-int compress_resident_clusters(int d, CompressShape shape, int mt)
-{
-    // small per-process cache keyed by the launch shape
-    static int keys[32];
-    static int vals[32];
-    static int n = 0;
-    const int key = ((d * 16 + shape.nw) * 16 + shape.tw) * 64 * 8 + shape.cs * 8 + mt;
-    for (int i = 0; i < n; ++i)
-        if (keys[i] == key)
-            return vals[i];
-    const int v = d == 64 ? resident_clusters_d64(shape, mt)
-                          : d == 128 ? resident_clusters_d128(shape, mt) : 0;
-    if (n < 32) {
-        keys[n] = key;
-        vals[n] = v;
-        ++n;
-    }
-    return v;
-}
-
 cudaError_t launch_compress(const CompressArgs &a, int d, CompressShape shape, int mt, int units,
                             cudaStream_t s)
 {

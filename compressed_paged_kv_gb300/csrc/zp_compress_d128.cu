@@ -10,11 +10,6 @@ cudaError_t launch_compress_d128(const CompressArgs &a, CompressShape shape, int
     return launch_compress_for_d<128>(a, shape, mt, units, s);
 }
 
-int resident_clusters_d128(CompressShape shape, int mt)
-{
-    return resident_clusters_for_d<128>(shape, mt);
-}
-
 bool compress_cluster16_ok()
 {
     static int cached = -1;

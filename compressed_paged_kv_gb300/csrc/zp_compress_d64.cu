@@ -9,9 +9,4 @@ cudaError_t launch_compress_d64(const CompressArgs &a, CompressShape shape, int 
     return launch_compress_for_d<64>(a, shape, mt, units, s);
 }
 
-int resident_clusters_d64(CompressShape shape, int mt)
-{
-    return resident_clusters_for_d<64>(shape, mt);
-}
-
 }  // namespace zp

@@ -8,9 +8,8 @@
 //
 // One unit = (request, layer, kv head) = T = N_max * b cached tokens.  A
 // thread-block cluster of `cs` CTAs owns the unit; CTA c owns tokens
-// [c*TPC, (c+1)*TPC) and keeps their K rows in shared memory.  Steps:
-//   0. every K row of the chunk is copied into shared memory by its own bulk
-//      copy (rows padded to d*2+16 bytes so that ldmatrix is conflict-free);
+// [c*TPC, (c+1)*TPC) and keeps their K rows in shared memory (TMA, 128-byte
+// swizzle).  Steps:
 //   1. logits of the w*G window rows against the CTA's keys and the b x b
 //      Gram of every block, on the tensor cores (mma.sync m16n8k16 bf16,
 //      fp32 accumulate), logits kept in registers in base 2;
@@ -23,12 +22,11 @@
 //   4. the b lowest candidates under (score ascending, index descending):
 //      each warp radix-selects its b smallest 64-bit keys (order-preserving
 //      image of the fp32 score bits above the complemented index), the CTA
-//      ranks its warps' candidates into a sorted list, and each of the
-//      cluster's candidates is ranked against all sorted lists;
-//   5. kept rows are written to their destination slots by one bulk copy
-//      per row: K from shared memory, V through a staging copy.  During its
-//      compute phases a CTA prefetches into L2 the K and V blocks of the
-//      unit one resident wave ahead, so memory does not idle between waves.  Exactly b tokens are evicted, so
+//      ranks its warps' candidates into a sorted list, and b steps of a
+//      k-way merge of the cluster's sorted lists give the unit's b;
+//   5. kept rows are written to their destination slots: K from shared
+//      memory, V through a staging copy (its blocks are prefetched into L2
+//      when the CTA starts).  Exactly b tokens are evicted, so
 //      destination j reads source kept[j] with j <= kept[j] <= j + b.  In-place
 //      writes of the next CTA can only reach this CTA's last block, whose V
 //      rows are staged before the first cluster barrier; every K row is in
@@ -121,10 +119,9 @@ struct CompressSmem {
     static constexpr int TPC = NW * TW * 16;  // tokens per CTA
     static constexpr int NBLK = TPC / kBlk;
     static constexpr int ROWS = MT * 16;
-    static constexpr int RS = D * 2 + 16;  // padded row stride: conflict-free ldmatrix
-    static constexpr int K_BYTES = TPC * RS;
+    static constexpr int K_BYTES = TPC * D * 2;
     static constexpr int Q_BYTES = ROWS * D * 2;
-    static constexpr int VT_BYTES = kBlk * RS;
+    static constexpr int VT_BYTES = kBlk * D * 2;
     static constexpr int off_k = 0;
     static constexpr int off_q = off_k + K_BYTES;
     static constexpr int off_vt = off_q + Q_BYTES;
@@ -145,8 +142,8 @@ struct CompressSmem {
     static constexpr int off_ev = off_all + kMaxCluster * kBlk * 8;  // int [b]
     static constexpr int off_misc = off_ev + kBlk * 4;              // int [8]
     static constexpr int off_bmove = off_misc + 8 * 4;              // int [NBLK]
-    static constexpr int off_bar = (off_bmove + NBLK * 4 + 15) / 16 * 16;  // 1 + NT mbarriers
-    static constexpr int BYTES = off_bar + 8 + NT * 8;
+    static constexpr int off_bar = (off_bmove + NBLK * 4 + 15) / 16 * 16;  // 2 mbarriers
+    static constexpr int BYTES = off_bar + 16;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024 B
     static constexpr int MIN_BLOCKS = NW == 4 ? (TW <= 2 ? 4 : 2) : (TW <= 2 ? 2 : 1);
 };
@@ -157,9 +154,8 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
 {
     using S = CompressSmem<D, NW, TW, MT>;
     constexpr int NT = S::NT, TPC = S::TPC, NBLK = S::NBLK, ROWS = S::ROWS;
-    constexpr int RS = S::RS;
+    constexpr int HALVES = D / 64;
     constexpr int CPR = D / 8;           // 16-byte chunks per row
-    constexpr uint32_t ROW_BYTES = D * 2;
     constexpr int KPT = TPC / NT;        // keys per thread (TW / 2)
     static_assert(TW % 2 == 0 && KPT >= 1, "two or more 16-key tiles per warp");
 
@@ -185,7 +181,6 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
     int *sMisc = reinterpret_cast<int *>(sm + S::off_misc);
     int *sBMove = reinterpret_cast<int *>(sm + S::off_bmove);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::off_bar);
-    uint64_t *sVbar = bars + 1;  // one per thread: its V rows
 
     const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
     const int cs = a.cs;
@@ -207,29 +202,43 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
     const int blk0 = t0 / kBlk;
     const int G = a.Hq / a.Hkv;
 
-    mbar_init(&sVbar[tid], 1);
-    if (tid == 0)
+    if (tid == 0) {
         mbar_init(&bars[0], 1);
-    fence_mbar_init();
-    if (tid == 0)
-        mbar_arrive_expect_tx(&bars[0], (TPC + kBlk) * ROW_BYTES);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+    }
+    for (int q = tid; q < NBLK; q += NT)
+        sBMove[q] = 0;
     __syncthreads();
 
-    // ---- loads, one bulk copy per 256-byte row into padded shared rows: the
-    // K chunk, the V rows of the chunk's last block (the next CTA may
-    // overwrite them in place later), and an L2 prefetch of the other V
-    // blocks (staged much later); the window queries by plain loads.
-    const __nv_bfloat16 *kpool_in = static_cast<const __nv_bfloat16 *>(a.kpools[l]);
-    const __nv_bfloat16 *vpool_in = static_cast<const __nv_bfloat16 *>(a.vpools[l]);
-    for (int k = tid; k < TPC; k += NT) {
-        const int blk = src_row[blk0 + (k >> 4)];
-        bulk_g2s(sK + k * RS, kpool_in + (((size_t)blk * a.Hkv + h) * kBlk + (k & 15)) * D,
-                 ROW_BYTES, &bars[0]);
-    }
-    if (tid < kBlk) {
-        const int blk = src_row[blk0 + NBLK - 1];
-        bulk_g2s(sVt + tid * RS, vpool_in + (((size_t)blk * a.Hkv + h) * kBlk + tid) * D,
-                 ROW_BYTES, &bars[0]);
+    // ---- loads: K chunk (TMA, swizzled), the V rows of the chunk's last
+    // block (bulk copy; the next CTA may overwrite them in place later), and
+    // the window queries (plain loads into the same swizzled layout).
+    if (wi == 0) {
+        const CUtensorMap *kmap = a.kmaps + l;
+        if (lane == 0)
+            mbar_arrive_expect_tx(&bars[0], S::K_BYTES + S::VT_BYTES);
+        __syncwarp();
+        for (int q = lane; q < NBLK; q += 32) {
+            const int blk = src_row[blk0 + q];
+            const int y = (blk * a.Hkv + h) * kBlk;
+#pragma unroll
+            for (int hf = 0; hf < HALVES; ++hf)
+                tma_load_2d(sK + hf * TPC * 128 + q * kBlk * 128, kmap, hf * 64, y, &bars[0]);
+        }
+        if (lane == 0) {
+            const int blk = src_row[blk0 + NBLK - 1];
+            const __nv_bfloat16 *vsrc = static_cast<const __nv_bfloat16 *>(a.vpools[l]) +
+                                        ((size_t)blk * a.Hkv + h) * kBlk * D;
+            bulk_g2s(sVt, vsrc, S::VT_BYTES, &bars[0]);
+        }
+        // the other V blocks are staged much later: start their trip to L2 now
+        for (int q = lane; q < NBLK - 1; q += 32) {
+            const int blk = src_row[blk0 + q];
+            prefetch_l2(static_cast<const __nv_bfloat16 *>(a.vpools[l]) +
+                            ((size_t)blk * a.Hkv + h) * kBlk * D,
+                        kBlk * D * 2);
+        }
     }
     {
         const __nv_bfloat16 *qsrc =
@@ -279,8 +288,7 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
             for (int tt = 0; tt < TW; ++tt) {
                 const int key0 = (wi * TW + tt) * 16;
                 uint32_t kb[4];
-                ldsm_x4(kb_base + (key0 + (mi >> 1) * 8 + (lane & 7)) * RS + (ks * 2 + (mi & 1)) * 16,
-                        kb);
+                ldsm_x4(kb_base + swz(key0 + (mi >> 1) * 8 + (lane & 7), ks * 2 + (mi & 1), TPC), kb);
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
                     mma_bf16(acc[mt][tt][0], qa[mt][0], qa[mt][1], qa[mt][2], qa[mt][3], kb[0], kb[1]);
@@ -289,29 +297,6 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
                 mma_bf16(gram[tt][0], kb[0], kb[2], kb[1], kb[3], kb[0], kb[1]);
                 mma_bf16(gram[tt][1], kb[0], kb[2], kb[1], kb[3], kb[2], kb[3]);
             }
-        }
-    }
-
-    // While this CTA computes, memory would idle: start moving into L2 the K
-    // and V blocks of the same chunk of the unit one resident wave ahead
-    // (that CTA then loads from L2), and in the first wave this chunk's own V
-    // blocks (staged at the end).
-    if (tid >= 32 && tid < 32 + 2 * NBLK) {
-        const int q = (tid - 32) >> 1;
-        const bool is_v = (tid - 32) & 1;
-        const int ahead = unit + a.prefetch_ahead;
-        if (ahead < a.units) {
-            const int ah = ahead % a.Hkv, al = (ahead / a.Hkv) % a.L, ar = ahead / (a.Hkv * a.L);
-            const int arow = a.req_idx ? a.req_idx[ar] : ar;
-            const int blk = a.tables[(size_t)arow * a.stride + blk0 + q];
-            const void *pool = is_v ? a.vpools[al] : a.kpools[al];
-            prefetch_l2(static_cast<const __nv_bfloat16 *>(pool) +
-                            ((size_t)blk * a.Hkv + ah) * kBlk * D,
-                        kBlk * ROW_BYTES);
-        }
-        if (is_v && unit < a.prefetch_ahead && q < NBLK - 1) {
-            const int blk = src_row[blk0 + q];
-            prefetch_l2(vpool_in + ((size_t)blk * a.Hkv + h) * kBlk * D, kBlk * ROW_BYTES);
         }
     }
 
@@ -574,8 +559,10 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
                 const int dp = tok - before;
                 const int dblk = dst_row[dp >> 4];
                 const int sblk = src_row[tok >> 4];
-                if (dp != tok || dblk != sblk)
+                if (dp != tok || dblk != sblk) {
                     doff = (dblk * a.Hkv + h) * kBlk + (dp & 15);
+                    sBMove[k >> 4] = 1;
+                }
                 if (a.kept_out)
                     a.kept_out[uo * (size_t)(T - kBlk) + dp] = tok;
             }
@@ -586,57 +573,68 @@ __global__ void __launch_bounds__(NW * 32, (CompressSmem<D, NW, TW, MT>::MIN_BLO
     }
     __syncthreads();
 
-    // ---- 5. compaction: one bulk copy per moved row.  K goes out of shared
-    // memory; once a thread's K copies have read its rows, the V rows it owns
-    // (outside the last block, staged at the start) are staged in their place.
-    // In-place destinations overlap sources of this CTA, so no V row goes out
-    // before every V row of the CTA has been staged.
-    __nv_bfloat16 *kpool = static_cast<__nv_bfloat16 *>(a.kpools[l]);
-    __nv_bfloat16 *vpool = static_cast<__nv_bfloat16 *>(a.vpools[l]);
-    int doffs[KPT];
+    // ---- 5. compaction: K rows from shared memory
+    if (!bad) {
+        __nv_bfloat16 *kpool = static_cast<__nv_bfloat16 *>(a.kpools[l]);
+        const uint32_t kb_base = smem_u32(sK);
+        for (int c = tid; c < TPC * CPR; c += NT) {
+            const int k = c / CPR, ch = c - k * CPR;
+            const int doff = sDoff[k];
+            if (doff < 0)
+                continue;
+            const uint4 v = ld_shared_v4(kb_base + swz(k, ch, TPC));
+            st_global_v4(kpool + (size_t)doff * D + ch * 8, v);
+        }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // V rows of the moved tokens: stage the source blocks (except the last,
+    // already staged) into the K buffer, then scatter.
+    if (wi == 0) {
+        int nv = 0;
+        for (int q = lane; q < NBLK - 1; q += 32)
+            nv += (!bad && sBMove[q]) ? 1 : 0;
 #pragma unroll
-    for (int j = 0; j < KPT; ++j)
-        doffs[j] = bad ? -1 : sDoff[tid * KPT + j];
-#pragma unroll
-    for (int j = 0; j < KPT; ++j)
-        if (doffs[j] >= 0)
-            bulk_s2g(kpool + (size_t)doffs[j] * D, sK + (tid * KPT + j) * RS, ROW_BYTES);
-    bulk_commit();
-    int staged = 0;
-#pragma unroll
-    for (int j = 0; j < KPT; ++j)
-        staged += doffs[j] >= 0 && tid * KPT + j < TPC - kBlk;
-    bool vok = true;
-    if (staged > 0) {
-        bulk_wait_read0();  // this thread's K rows have left shared memory
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&sVbar[tid], staged * ROW_BYTES);
-#pragma unroll
-        for (int j = 0; j < KPT; ++j) {
-            const int k = tid * KPT + j;
-            if (doffs[j] >= 0 && k < TPC - kBlk) {
-                const int blk = src_row[blk0 + (k >> 4)];
-                bulk_g2s(sK + k * RS, vpool_in + (((size_t)blk * a.Hkv + h) * kBlk + (k & 15)) * D,
-                         ROW_BYTES, &sVbar[tid]);
+        for (int o = 16; o > 0; o >>= 1)
+            nv += __shfl_xor_sync(0xffffffffu, nv, o);
+        if (lane == 0) {
+            sMisc[4] = nv;
+            if (nv > 0)
+                mbar_arrive_expect_tx(&bars[1], nv * kBlk * D * 2);
+        }
+        __syncwarp();
+        if (nv > 0) {
+            for (int q = lane; q < NBLK - 1; q += 32) {
+                if (!sBMove[q])
+                    continue;
+                const int blk = src_row[blk0 + q];
+                const __nv_bfloat16 *vsrc = static_cast<const __nv_bfloat16 *>(a.vpools[l]) +
+                                            ((size_t)blk * a.Hkv + h) * kBlk * D;
+                bulk_g2s(sK + q * kBlk * D * 2, vsrc, kBlk * D * 2, &bars[1]);
             }
         }
-        vok = mbar_wait(&sVbar[tid], 0);
     }
-    bad = __syncthreads_or(bad || !vok);
+    __syncthreads();
+    if (sMisc[4] > 0)
+        bad |= !mbar_wait(&bars[1], 0);
+    bad = __syncthreads_or(bad);
     if (!bad) {
-#pragma unroll
-        for (int j = 0; j < KPT; ++j) {
-            const int k = tid * KPT + j;
-            if (doffs[j] >= 0)
-                bulk_s2g(vpool + (size_t)doffs[j] * D,
-                         k >= TPC - kBlk ? sVt + (k - (TPC - kBlk)) * RS : sK + k * RS, ROW_BYTES);
+        __nv_bfloat16 *vpool = static_cast<__nv_bfloat16 *>(a.vpools[l]);
+        const uint32_t v_base = smem_u32(sK), vt_base = smem_u32(sVt);
+        for (int c = tid; c < TPC * CPR; c += NT) {
+            const int k = c / CPR, ch = c - k * CPR;
+            const int doff = sDoff[k];
+            if (doff < 0)
+                continue;
+            const uint32_t src = (k >= TPC - kBlk) ? vt_base + ((k - (TPC - kBlk)) * CPR + ch) * 16
+                                                   : v_base + (k * CPR + ch) * 16;
+            st_global_v4(vpool + (size_t)doff * D + ch * 8, ld_shared_v4(src));
         }
     } else if (tid == 0) {
         set_error(a.call, ZP_ERR_TIMEOUT);
         set_error(a.sticky, ZP_ERR_TIMEOUT);
     }
-    bulk_commit();
-    bulk_wait_read0();
     cluster_wait();  // peers may still read this CTA's shared memory until here
 }
 
@@ -696,52 +694,6 @@ bool cluster16_ok_t()
         return false;
     }
     return n > 0;
-}
-
-// Clusters of `cs` CTAs of this kernel that the device can hold at once.
-template <int D, int NW, int TW, int MT>
-int resident_clusters_t(int cs)
-{
-    using Sm = CompressSmem<D, NW, TW, MT>;
-    auto kern = zp_compress_kernel<D, NW, TW, MT>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::ALLOC) !=
-            cudaSuccess ||
-        (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-                       cudaSuccess)) {
-        cudaGetLastError();
-        return 0;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(cs) * 1024u, 1, 1);
-    cfg.blockDim = dim3(Sm::NT, 1, 1);
-    cfg.dynamicSmemBytes = Sm::ALLOC;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    return n;
-}
-
-template <int D>
-int resident_clusters_for_d(CompressShape sh, int mt)
-{
-#define ZP_CASE(NW_, TW_, MT_)                                    \
-    if (sh.nw == NW_ && sh.tw == TW_ && mt == MT_)                 \
-        return resident_clusters_t<D, NW_, TW_, MT_>(sh.cs);
-    ZP_CASE(4, 2, 1) ZP_CASE(4, 2, 2) ZP_CASE(4, 2, 4)
-    ZP_CASE(4, 4, 1) ZP_CASE(4, 4, 2) ZP_CASE(4, 4, 4)
-    ZP_CASE(8, 2, 1) ZP_CASE(8, 2, 2) ZP_CASE(8, 2, 4)
-    ZP_CASE(8, 4, 1) ZP_CASE(8, 4, 2) ZP_CASE(8, 4, 4)
-#undef ZP_CASE
-    return 0;
 }
 
 template <int D>

@@ -76,8 +76,6 @@ struct CompressArgs {
     int32_t *call;
     int32_t *sticky;
     int32_t L, Hkv, Hq, R, N, w, rows, cs;
-    int32_t units;           // R * L * Hkv
-    int32_t prefetch_ahead;  // units between a CTA and the one it prefetches for
     float lambda;
     float inv_rows;       // 1 / (w * G)
     float logit_scale;    // log2(e) / sqrt(d): logits are kept in base 2
@@ -111,14 +109,10 @@ bool compress_config(int T, bool allow16, CompressShape *out);
 bool compress_cluster16_ok();  // can this device schedule the 16-CTA clusters?
 cudaError_t launch_compress(const CompressArgs &a, int d, CompressShape shape, int mt, int units,
                             cudaStream_t s);
-// Clusters of this shape that can be resident at once (0 if unknown).
-int compress_resident_clusters(int d, CompressShape shape, int mt);
 cudaError_t launch_compress_d64(const CompressArgs &a, CompressShape shape, int mt, int units,
                                 cudaStream_t s);
 cudaError_t launch_compress_d128(const CompressArgs &a, CompressShape shape, int mt, int units,
                                  cudaStream_t s);
-int resident_clusters_d64(CompressShape shape, int mt);
-int resident_clusters_d128(CompressShape shape, int mt);
 cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t s);
 
 // ------------------------------------------------------------ device helpers
@@ -201,25 +195,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
-}
-
-// Bulk copy shared -> global, tracked in this thread's bulk group.
-__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                 "r"(smem_u32(src)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit()
-{
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Waits until every committed bulk copy of this thread has read its source.
-__device__ __forceinline__ void bulk_wait_read0()
-{
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // ldmatrix / mma ---------------------------------------------------------------
