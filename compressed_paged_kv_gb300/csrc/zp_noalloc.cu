@@ -1,0 +1,228 @@
+// zp_noalloc.cu -- paged decode attention for callers that cannot allocate.
+//
+// Some callers cannot call cudaMalloc at all: code running inside a CUDA
+// graph being captured, an allocator or memory-pool callback, a plug-in
+// loaded into a host process that owns all device memory, or a real-time
+// path that must not block on the driver's allocator.  This entry point
+// needs no zp_cache handle (whose creation allocates) and allocates nothing:
+// its split-K partial results live in a fixed file-scope device array that
+// every GPU loading the library holds until the process exits.
+//
+// The kernels here are a plain CUDA-core variant of the split-K decode
+// attention in zp_decode.cu: one CTA per (request, query head, split), a
+// warp per token at a time with a shuffle-reduced dot product, an online
+// softmax per warp, then a log-sum-exp combine.
+#include <mutex>
+
+#include "zp_internal.cuh"
+
+namespace {
+
+constexpr int kNaThreads = 128;
+constexpr int kNaWarps = kNaThreads / 32;
+constexpr int kNaMaxSplits = 16;
+// Maximum (request, query head, split) partial slots the array holds; with
+// head_dim up to 128 each slot is 130 floats, so the array is ~16.3 MiB.
+constexpr int kNaSlots = 32768;
+constexpr int kNaSlotFloats = 128 + 2;
+
+static __device__ __align__(256) float g_na_part[static_cast<size_t>(kNaSlots) * kNaSlotFloats];
+
+struct NaArgs {
+    const __nv_bfloat16 *kpool, *vpool, *q;
+    const int32_t *tables, *lengths, *req_idx;
+    int32_t stride, num_rows, num_blocks, R, Hkv, Hq, splits, tps;  // tps: tokens per split
+    float logit_scale;  // scale * log2(e)
+    float *part;        // the device address of g_na_part
+    __nv_bfloat16 *out;
+    int32_t *status;    // nullable
+};
+
+template <int D>
+__global__ void __launch_bounds__(kNaThreads) na_decode_split(const NaArgs a)
+{
+    constexpr int PER = D / 32;  // elements of a row per lane
+    __shared__ float s_m[kNaWarps], s_l[kNaWarps];
+    __shared__ float s_o[kNaWarps][D];
+    const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+    const int split = blockIdx.x, hq = blockIdx.y, r = blockIdx.z;
+    const int G = a.Hq / a.Hkv, h = hq / G;
+    int row = a.req_idx ? a.req_idx[r] : r;
+    const bool row_ok = row >= 0 && row < a.num_rows;
+    int len = row_ok ? a.lengths[row] : 0;
+    if (!row_ok || len < 0 || len > a.stride * zp::kBlk) {
+        if (threadIdx.x == 0 && split == 0 && a.status)
+            atomicCAS(a.status, 0, row_ok ? ZP_ERR_DEVICE_CHECK : ZP_ERR_INVALID_ARG);
+        len = 0;
+        row = 0;
+    }
+    float qv[PER];
+    const __nv_bfloat16 *qrow = a.q + ((size_t)r * a.Hq + hq) * D;
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+        qv[i] = __bfloat162float(qrow[lane * PER + i]);
+    const int t_begin = split * a.tps, t_end = min(len, t_begin + a.tps);
+    float m = -1e30f, l = 0.f, o[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+        o[i] = 0.f;
+    for (int t = t_begin + wi; t < t_end; t += kNaWarps) {
+        int blk = a.tables[(size_t)row * a.stride + t / zp::kBlk];
+        if (blk < 0 || blk >= a.num_blocks) {
+            if (lane == 0 && a.status)
+                atomicCAS(a.status, 0, ZP_ERR_DEVICE_CHECK);
+            continue;
+        }
+        const size_t off = (((size_t)blk * a.Hkv + h) * zp::kBlk + t % zp::kBlk) * D + lane * PER;
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < PER; ++i)
+            dot += qv[i] * __bfloat162float(a.kpool[off + i]);
+#pragma unroll
+        for (int s = 16; s > 0; s >>= 1)
+            dot += __shfl_xor_sync(0xffffffffu, dot, s);
+        const float x = dot * a.logit_scale;
+        const float m_new = fmaxf(m, x);
+        const float corr = exp2f(m - m_new), p = exp2f(x - m_new);
+        l = l * corr + p;
+#pragma unroll
+        for (int i = 0; i < PER; ++i)
+            o[i] = o[i] * corr + p * __bfloat162float(a.vpool[off + i]);
+        m = m_new;
+    }
+    if (lane == 0) {
+        s_m[wi] = m;
+        s_l[wi] = l;
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+        s_o[wi][lane * PER + i] = o[i];
+    __syncthreads();
+    float *p = a.part + (((size_t)r * a.Hq + hq) * a.splits + split) * kNaSlotFloats;
+    float M = -1e30f;
+#pragma unroll
+    for (int w = 0; w < kNaWarps; ++w)
+        M = fmaxf(M, s_m[w]);
+    for (int c = threadIdx.x; c < D; c += kNaThreads) {
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNaWarps; ++w) {
+            const float f = exp2f(s_m[w] - M);
+            L += s_l[w] * f;
+            O += s_o[w][c] * f;
+        }
+        p[c] = O;
+        if (c == 0) {
+            p[D] = M;
+            p[D + 1] = L;
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(D) na_decode_combine(const NaArgs a)
+{
+    const int rh = blockIdx.x, c = threadIdx.x;
+    const float *base = a.part + (size_t)rh * a.splits * kNaSlotFloats;
+    float M = -1e30f;
+    for (int s = 0; s < a.splits; ++s)
+        M = fmaxf(M, base[s * kNaSlotFloats + D]);
+    float L = 0.f, O = 0.f;
+    for (int s = 0; s < a.splits; ++s) {
+        const float f = exp2f(base[s * kNaSlotFloats + D] - M);
+        L += base[s * kNaSlotFloats + D + 1] * f;
+        O += base[s * kNaSlotFloats + c] * f;
+    }
+    a.out[(size_t)rh * D + c] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+}
+
+// Device address of g_na_part, looked up once per device (with that device
+// current) and cached.
+std::mutex g_na_mu;
+float *g_na_addr[256];
+bool g_na_ready[256];
+
+cudaError_t na_scratch(int device, float **out)
+{
+    if (device < 0 || device >= 256)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_na_mu);
+    if (!g_na_ready[device]) {
+        void *ptr = nullptr;
+        const cudaError_t err = cudaGetSymbolAddress(&ptr, g_na_part);
+        if (err != cudaSuccess)
+            return err;
+        g_na_addr[device] = static_cast<float *>(ptr);
+        g_na_ready[device] = true;
+    }
+    *out = g_na_addr[device];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" zp_status zp_paged_decode_attn_noalloc(
+    const void *k_pool, const void *v_pool, int32_t num_blocks, int32_t num_kv_heads,
+    int32_t num_q_heads, int32_t head_dim, const void *q, const int32_t *block_tables,
+    int32_t bt_stride, int32_t num_rows, const int32_t *lengths, const int32_t *req_idx, int32_t R,
+    float scale, void *out, int32_t *status, void *stream)
+{
+    if (!k_pool || !v_pool || !q || !block_tables || !lengths || !out)
+        return ZP_ERR_INVALID_ARG;
+    if (num_blocks < 1 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads ||
+        R < 0 || num_rows < 1 || bt_stride < 1 || !(scale == scale))
+        return ZP_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128)
+        return ZP_ERR_UNSUPPORTED;
+    if (static_cast<long long>(R) * num_q_heads > kNaSlots)
+        return ZP_ERR_UNSUPPORTED;  // more (request, head) pairs than the fixed array holds
+    if (static_cast<long long>(bt_stride) * zp::kBlk >= (1ll << 31))
+        return ZP_ERR_UNSUPPORTED;
+    if (R == 0)
+        return ZP_OK;
+    int device = 0, sms = 0;
+    if (cudaGetDevice(&device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return ZP_ERR_CUDA;
+    float *part = nullptr;
+    if (na_scratch(device, &part) != cudaSuccess)
+        return ZP_ERR_CUDA;
+
+    // splits: about four CTAs per SM, bounded by the array and by 16
+    const int heads = R * num_q_heads;
+    int splits = (4 * sms + heads - 1) / heads;
+    splits = splits < 1 ? 1 : splits > kNaMaxSplits ? kNaMaxSplits : splits;
+    while (splits > 1 && static_cast<long long>(heads) * splits > kNaSlots)
+        --splits;
+    const int max_tokens = bt_stride * zp::kBlk;
+    NaArgs a{};
+    a.kpool = static_cast<const __nv_bfloat16 *>(k_pool);
+    a.vpool = static_cast<const __nv_bfloat16 *>(v_pool);
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.tables = block_tables;
+    a.lengths = lengths;
+    a.req_idx = req_idx;
+    a.stride = bt_stride;
+    a.num_rows = num_rows;
+    a.num_blocks = num_blocks;
+    a.R = R;
+    a.Hkv = num_kv_heads;
+    a.Hq = num_q_heads;
+    a.splits = splits;
+    a.tps = (max_tokens + splits - 1) / splits;
+    a.logit_scale = scale * 1.4426950408889634f;
+    a.part = part;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.status = status;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const dim3 grid(static_cast<unsigned>(splits), static_cast<unsigned>(num_q_heads),
+                    static_cast<unsigned>(R));
+    if (head_dim == 64) {
+        na_decode_split<64><<<grid, kNaThreads, 0, s>>>(a);
+        na_decode_combine<64><<<static_cast<unsigned>(heads), 64, 0, s>>>(a);
+    } else {
+        na_decode_split<128><<<grid, kNaThreads, 0, s>>>(a);
+        na_decode_combine<128><<<static_cast<unsigned>(heads), 128, 0, s>>>(a);
+    }
+    return cudaGetLastError() == cudaSuccess ? ZP_OK : ZP_ERR_CUDA;
+}

@@ -73,6 +73,9 @@ def lib():
         L.zp_paged_decode_attn.argtypes = [P, I32, P, P, I32, I32, P, P, I32, ctypes.c_float, P,
                                            P]
         L.zp_paged_decode_attn.restype = I32
+        L.zp_paged_decode_attn_noalloc.argtypes = [P, P, I32, I32, I32, I32, P, P, I32, I32, P,
+                                                   P, I32, ctypes.c_float, P, P, P]
+        L.zp_paged_decode_attn_noalloc.restype = I32
         L.zp_cache_status.argtypes = [P, P, ctypes.POINTER(I32)]
         L.zp_cache_status.restype = I32
         L.zp_status_string.argtypes = [I32]
@@ -117,6 +120,17 @@ def zp_paged_decode_attn(handle, layer, q, block_tables, bt_stride, num_rows, le
     return lib().zp_paged_decode_attn(P(handle), layer, P(q), P(block_tables), bt_stride,
                                       num_rows, P(lengths), P(req_idx or None), R, float(scale),
                                       P(out), P(stream or None))
+
+
+def zp_paged_decode_attn_noalloc(k_pool, v_pool, num_blocks, num_kv_heads, num_q_heads, head_dim,
+                                 q, block_tables, bt_stride, num_rows, lengths, req_idx, R, scale,
+                                 out, status, stream) -> int:
+    """Decode attention without a handle and without any allocation (for
+    callers that cannot call cudaMalloc); see include/zp.h."""
+    return lib().zp_paged_decode_attn_noalloc(
+        P(k_pool), P(v_pool), num_blocks, num_kv_heads, num_q_heads, head_dim, P(q),
+        P(block_tables), bt_stride, num_rows, P(lengths), P(req_idx or None), R, float(scale),
+        P(out), P(status or None), P(stream or None))
 
 
 def zp_cache_status(handle, stream) -> tuple[int, int]:

@@ -166,6 +166,36 @@ zp_status zp_paged_decode_attn(zp_cache *cache, int32_t layer, const void *q,
                                const int32_t *lengths, const int32_t *req_idx, int32_t R,
                                float scale, void *out, void *stream);
 
+/* Paged decode attention for callers that cannot allocate device memory.
+ * The paper has no counterpart: this is a deployment variant of
+ * zp_paged_decode_attn.  Callers that cannot call cudaMalloc (code inside a
+ * CUDA graph being captured, an allocator or memory-pool callback, a plug-in
+ * in a process that owns all device memory, a real-time path that must not
+ * wait on the allocator) can still run decode attention: this call needs no
+ * zp_cache handle and allocates nothing.  Its split-K partial results live in
+ * one fixed device array compiled into the library (about 16.3 MiB, held on
+ * every GPU that loads the library until the process exits).
+ *
+ *  k_pool, v_pool  device bf16 pools of one layer, [num_blocks][num_kv_heads][16][head_dim]
+ *  q, out          device bf16 [R][num_q_heads][head_dim]; other arguments as in
+ *                  zp_paged_decode_attn
+ *  status          nullable device int32: device-detected errors (a length or
+ *                  block id out of range) are recorded there with atomicCAS from 0
+ * Limits: head_dim 64 or 128, block size 16, R * num_q_heads <= 32768
+ * (ZP_ERR_UNSUPPORTED beyond).  The first call on a device looks up the
+ * array's device address (once per device, with that device current): make
+ * that first call before any stream capture.  Every call shares the array and
+ * each call overwrites the slots it reads, so nothing needs clearing between
+ * calls; calls that overlap on the GPU (two streams, or two threads) race on
+ * it and must be serialised by the caller. */
+zp_status zp_paged_decode_attn_noalloc(const void *k_pool, const void *v_pool, int32_t num_blocks,
+                                       int32_t num_kv_heads, int32_t num_q_heads,
+                                       int32_t head_dim, const void *q,
+                                       const int32_t *block_tables, int32_t bt_stride,
+                                       int32_t num_rows, const int32_t *lengths,
+                                       const int32_t *req_idx, int32_t R, float scale, void *out,
+                                       int32_t *status, void *stream);
+
 /* Synchronises `stream`, returns the handle's sticky device status in
  * *out_status (ZP_OK or the first device-detected error since the last
  * read) and clears it.  Returns ZP_ERR_CUDA if the stream reports an error. */
