@@ -163,6 +163,23 @@ def device_index(torch):
     return idx
 
 
+# ------------------------------------------------------------ multi-rank
+def replica_seed(wl, rank: int) -> int:
+    """Each rank compresses its own replica of the workload (units are
+    independent: no collective on the data path)."""
+    return wl.seed + 7919 * rank
+
+
+def reduce_max(values, world: int, device=None):
+    """Max over ranks of a list of floats (the step timings); identity for 1."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def run_gpu(args, world, rank, local):
@@ -179,7 +196,7 @@ def run_gpu(args, world, rank, local):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     wl = W.WORKLOADS[args.workload]
-    st = W.build_cache(wl, dev, seed=wl.seed + 7919 * rank)
+    st = W.build_cache(wl, dev, seed=replica_seed(wl, rank))
     host_snap = W.snapshot(st) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     cache = zp.Cache(st.k_pools, st.v_pools, wl.Hq, max_requests=st.block_tables.shape[0],
                      max_blocks_per_req=st.block_tables.shape[1])
@@ -306,11 +323,8 @@ def run_gpu(args, world, rank, local):
     status2 = cache.status()
 
     # max over ranks
-    vals = torch.tensor([step_ms, comp_avg, dec_avg, e2e_ms, t_wall], dtype=torch.float64,
-                        device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    step_ms, comp_avg, dec_avg, e2e_ms, t_wall = vals.tolist()
+    step_ms, comp_avg, dec_avg, e2e_ms, t_wall = reduce_max(
+        [step_ms, comp_avg, dec_avg, e2e_ms, t_wall], world, dev)
 
     if rank != 0:
         if world > 1:

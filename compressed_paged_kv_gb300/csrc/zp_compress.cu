@@ -110,41 +110,33 @@ __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
 
     // destinations: refcount 1 -> in place, > 1 -> pop a fresh target.  The
     // k-th needing entry in (request, block) order pops free_ids[fc-1-k].
+    // Thread t owns the contiguous entries [t*per, (t+1)*per): its loads are
+    // independent, and one block scan orders the pops.
     const int E = a.R * a.N;
-    int pops = 0;
-    for (int base = 0; base < E; base += kPlanThreads) {
-        const int e = base + tid;
-        int need = 0, blk = -1;
-        if (e < E) {
-            const int r = e / a.N, p = e - r * a.N;
-            const int row = a.req_idx ? a.req_idx[r] : r;
-            blk = a.tables[(size_t)row * a.stride + p];
-            if (blk < 0 || blk >= a.num_blocks) {
-                atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
-                blk = -1;
-            } else {
-                const int rc = a.refcount[blk];
-                if (rc < 1)
-                    atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
-                need = rc > 1;
-            }
+    const int per = (E + kPlanThreads - 1) / kPlanThreads;
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    auto src_of = [&](int e) {
+        const int r = e / a.N, p = e - r * a.N;
+        const int row = a.req_idx ? a.req_idx[r] : r;
+        return a.tables[(size_t)row * a.stride + p];
+    };
+    int my_need = 0;
+    for (int e = e0; e < e1; ++e) {
+        const int blk = src_of(e);
+        if (blk < 0 || blk >= a.num_blocks) {
+            atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
+            continue;
         }
-        int total;
-        const int k = block_excl_scan<kPlanThreads>(need, s_scan, total) + pops;
-        if (blk >= 0) {
-            int dst = blk;
-            if (need) {
-                if (k >= fc) {
-                    atomicCAS(&s_err, 0, ZP_ERR_OUT_OF_BLOCKS);
-                } else {
-                    dst = a.free_ids[fc - 1 - k];
-                    if (dst < 0 || dst >= a.num_blocks || a.refcount[dst] != 0)
-                        atomicCAS(&s_err, 0, ZP_ERR_DEVICE_CHECK);
-                }
-            }
-            a.ws.dst_table[e] = dst;
-        }
-        pops += total;
+        const int rc = a.refcount[blk];
+        if (rc < 1)
+            atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
+        my_need += rc > 1;
+    }
+    int pops;
+    int k = block_excl_scan<kPlanThreads>(my_need, s_scan, pops);
+    if (s_err == 0 && pops > fc) {
+        if (tid == 0)
+            atomicCAS(&s_err, 0, ZP_ERR_OUT_OF_BLOCKS);
     }
     __syncthreads();
     if (s_err != 0) {
@@ -152,49 +144,62 @@ __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
             *a.ws.call = s_err;
         return;
     }
+    for (int e = e0; e < e1; ++e) {
+        const int blk = src_of(e);
+        int dst = blk;
+        if (a.refcount[blk] > 1) {
+            dst = a.free_ids[fc - 1 - k];
+            ++k;
+            if (dst < 0 || dst >= a.num_blocks || a.refcount[dst] != 0)
+                atomicCAS(&s_err, 0, ZP_ERR_DEVICE_CHECK);
+        }
+        a.ws.dst_table[e] = dst;
+    }
+    __syncthreads();
+    if (s_err != 0 || pops == 0) {
+        // nothing shared: no reference is released, nothing is pushed
+        if (tid == 0) {
+            a.ws.counters[0] = pops;
+            a.ws.counters[1] = 0;
+            *a.ws.call = s_err;
+        }
+        return;
+    }
 
     // released blocks: a replaced block loses one reference per holder in this
     // call; it is freed at its last holder when that empties it.
-    for (int e = tid; e < E; e += kPlanThreads) {
-        const int r = e / a.N, p = e - r * a.N;
-        const int row = a.req_idx ? a.req_idx[r] : r;
-        const int src = a.tables[(size_t)row * a.stride + p];
+    for (int e = e0; e < e1; ++e) {
+        const int src = src_of(e);
         if (a.ws.dst_table[e] != src) {
             a.ws.occ[src] = 0;
             a.ws.last[src] = -1;
         }
     }
     __syncthreads();
-    for (int e = tid; e < E; e += kPlanThreads) {
-        const int r = e / a.N, p = e - r * a.N;
-        const int row = a.req_idx ? a.req_idx[r] : r;
-        const int src = a.tables[(size_t)row * a.stride + p];
+    for (int e = e0; e < e1; ++e) {
+        const int src = src_of(e);
         if (a.ws.dst_table[e] != src) {
             atomicAdd(&a.ws.occ[src], 1);
             atomicMax(&a.ws.last[src], e);
         }
     }
     __syncthreads();
-    int pushes = 0;
-    for (int base = 0; base < E; base += kPlanThreads) {
-        const int e = base + tid;
-        int flag = 0, src = -1;
-        if (e < E) {
-            const int r = e / a.N, p = e - r * a.N;
-            const int row = a.req_idx ? a.req_idx[r] : r;
-            src = a.tables[(size_t)row * a.stride + p];
-            if (a.ws.dst_table[e] != src && a.ws.last[src] == e) {
-                const int occ = a.ws.occ[src], rc = a.refcount[src];
-                if (occ > rc)
-                    atomicCAS(&s_err, 0, ZP_ERR_DEVICE_CHECK);
-                flag = occ == rc;
-            }
+    int my_push = 0;
+    for (int e = e0; e < e1; ++e) {
+        const int src = src_of(e);
+        if (a.ws.dst_table[e] != src && a.ws.last[src] == e) {
+            const int occ = a.ws.occ[src], rc = a.refcount[src];
+            if (occ > rc)
+                atomicCAS(&s_err, 0, ZP_ERR_DEVICE_CHECK);
+            my_push += occ == rc;
         }
-        int total;
-        const int pos = block_excl_scan<kPlanThreads>(flag, s_scan, total) + pushes;
-        if (flag)
-            a.ws.push_list[pos] = src;
-        pushes += total;
+    }
+    int pushes;
+    int pos = block_excl_scan<kPlanThreads>(my_push, s_scan, pushes);
+    for (int e = e0; e < e1; ++e) {
+        const int src = src_of(e);
+        if (a.ws.dst_table[e] != src && a.ws.last[src] == e && a.ws.occ[src] == a.refcount[src])
+            a.ws.push_list[pos++] = src;
     }
     __syncthreads();
     if (tid == 0) {
@@ -222,7 +227,7 @@ __global__ void __launch_bounds__(kPlanThreads) zp_finalize_kernel(const Finaliz
         s_fc = *a.free_count;
     __syncthreads();
     const int pops = a.ws.counters[0], pushes = a.ws.counters[1];
-    const int E = a.R * a.N;
+    const int E = pops > 0 ? a.R * a.N : 0;  // nothing shared: tables unchanged
     for (int e = tid; e < E; e += kPlanThreads) {
         const int r = e / a.N, p = e - r * a.N;
         const int row = a.req_idx ? a.req_idx[r] : r;
