@@ -69,7 +69,6 @@ struct zp_cache {
     int L = 0, Hkv = 0, Hq = 0, d = 0, b = 0, num_blocks = 0;
     int max_requests = 0, max_blocks = 0;
     int num_sms = 0;
-    bool cluster16 = false;  // 16-CTA clusters of the compression kernel schedulable
     int32_t gen = 0;
     void *base = nullptr;
     Workspace ws{};
@@ -196,7 +195,6 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
         delete c;
         return ZP_ERR_CUDA;
     }
-    c->cluster16 = zp::compress_cluster16_ok();
     *out = c;
     return ZP_OK;
 }
@@ -235,19 +233,14 @@ zp_status zp_compress(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int
     const int G = c->Hq / c->Hkv;
     const int T = n_max * c->b;
     const int rows = window * G;
-    zp::CompressShape shape{};
-    if (n_max > c->max_blocks || !zp::compress_config(T, true, &shape) || rows > zp::kMaxRows)
+    const int cs = zp::compress_cluster_size(T);
+    if (n_max > c->max_blocks || cs == 0 || rows > zp::kMaxRows)
         return ZP_ERR_UNSUPPORTED;
     if (R == 0)
         return ZP_OK;
     if (!on_device(c))
         return ZP_ERR_INVALID_ARG;
-    if (shape.cs > 8 && !c->cluster16) {
-        if (!zp::compress_config(T, false, &shape))
-            return ZP_ERR_UNSUPPORTED;
-    }
     const int mt = rows <= 16 ? 1 : rows <= 32 ? 2 : 4;
-    const int cs = shape.cs;
     const long long units = static_cast<long long>(R) * c->L * c->Hkv;
     if (units * cs >= (1ll << 31))
         return ZP_ERR_UNSUPPORTED;
@@ -296,7 +289,7 @@ zp_status zp_compress(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int
     ca.lambda = lambda;
     ca.inv_rows = 1.0f / static_cast<float>(rows);
     ca.logit_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c->d)));
-    if (zp::launch_compress(ca, c->d, shape, mt, static_cast<int>(units), s) != cudaSuccess)
+    if (zp::launch_compress(ca, c->d, mt, static_cast<int>(units), s) != cudaSuccess)
         return ZP_ERR_CUDA;
 
     zp::FinalizeArgs fa{};

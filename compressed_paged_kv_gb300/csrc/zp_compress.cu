@@ -14,8 +14,8 @@
 //   zp_plan_kernel      1 CTA: validates, picks destination blocks, computes
 //                       the refcount/free-stack update; writes nothing the
 //                       caller owns.
-//   zp_compress_kernel  (zp_compress_kernel.cuh) one thread-block cluster of
-//                       `cs` CTAs per unit
+//   zp_compress_stream_kernel  (zp_compress_stream.cuh) one thread-block
+//                       cluster of `cs` CTAs per unit
 //                       (request, layer, kv head); CTA c owns tokens
 //                       [c*TPC, (c+1)*TPC).  K chunk -> shared memory by TMA
 //                       (128B swizzle); window logits and the intra-block
@@ -266,38 +266,22 @@ cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s)
     return cudaGetLastError();
 }
 
-// Chunking of T tokens over a cluster: 4-warp CTAs of 128 tokens (or 256
-// above 2048 tokens) in clusters of up to 16 when this device can schedule
-// them, else 8-warp CTAs of 256 (or 512) tokens in clusters of up to 8.
-bool compress_config(int T, bool allow16, CompressShape *out)
+int compress_cluster_size(int T)
 {
-    CompressShape c{};
-    if (T <= 0 || T % 128 != 0)
-        return false;
-    if (T / 128 <= 8) {
-        c = {4, 2, T / 128};
-    } else if (allow16 && T / 128 <= 16) {
-        c = {4, 2, T / 128};
-    } else if (allow16 && T % 256 == 0 && T / 256 <= 16) {
-        c = {4, 4, T / 256};
-    } else if (T % 256 == 0 && T / 256 <= 8) {
-        c = {8, 2, T / 256};
-    } else if (T % 512 == 0 && T / 512 <= 8) {
-        c = {8, 4, T / 512};
-    } else {
-        return false;
-    }
-    *out = c;
-    return true;
+    // the fewest CTAs per unit with at most 1024 tokens each, every chunk a
+    // whole number of 128-token stages
+    for (int cs = 1; cs <= kMaxCluster; ++cs)
+        if (T % cs == 0 && T / cs <= 1024 && (T / cs) % 128 == 0)
+            return cs;
+    return 0;
 }
 
-cudaError_t launch_compress(const CompressArgs &a, int d, CompressShape shape, int mt, int units,
-                            cudaStream_t s)
+cudaError_t launch_compress(const CompressArgs &a, int d, int mt, int units, cudaStream_t s)
 {
     if (d == 64)
-        return launch_compress_d64(a, shape, mt, units, s);
+        return launch_compress_d64(a, mt, units, s);
     if (d == 128)
-        return launch_compress_d128(a, shape, mt, units, s);
+        return launch_compress_d128(a, mt, units, s);
     return cudaErrorInvalidValue;
 }
 

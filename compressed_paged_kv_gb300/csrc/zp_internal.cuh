@@ -100,19 +100,11 @@ struct DecodeArgs {
 // Launchers (defined next to their kernels).
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s);
-// Chunking of one unit's T tokens: `nw` warps per CTA, `tw` 16-key tiles per
-// warp (tokens per CTA = 16 * nw * tw), `cs` CTAs per cluster.
-struct CompressShape {
-    int nw, tw, cs;
-};
-bool compress_config(int T, bool allow16, CompressShape *out);
-bool compress_cluster16_ok();  // can this device schedule the 16-CTA clusters?
-cudaError_t launch_compress(const CompressArgs &a, int d, CompressShape shape, int mt, int units,
-                            cudaStream_t s);
-cudaError_t launch_compress_d64(const CompressArgs &a, CompressShape shape, int mt, int units,
-                                cudaStream_t s);
-cudaError_t launch_compress_d128(const CompressArgs &a, CompressShape shape, int mt, int units,
-                                 cudaStream_t s);
+// CTAs per unit of the fused compression kernel for T tokens (0: unsupported).
+int compress_cluster_size(int T);
+cudaError_t launch_compress(const CompressArgs &a, int d, int mt, int units, cudaStream_t s);
+cudaError_t launch_compress_d64(const CompressArgs &a, int mt, int units, cudaStream_t s);
+cudaError_t launch_compress_d128(const CompressArgs &a, int mt, int units, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t s);
 
 // ------------------------------------------------------------ device helpers
@@ -195,6 +187,101 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until every committed bulk copy of this thread has read its source.
+__device__ __forceinline__ void bulk_wait_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// L2 cache policies for the copies below.
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, int x, int y,
+                                                 uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes,
+                                              uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_s2g_hint(void *dst, const void *src, uint32_t bytes,
+                                              uint64_t policy)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+                 ::"l"(dst), "r"(smem_u32(src)), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+
+// Plain arrive (no transaction bytes) on a barrier of this CTA.
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Arrive on the barrier at a shared::cluster address (another CTA's barrier).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+// Bounded wait with cluster-scope acquire (pairs with mbar_arrive_remote).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    const uint32_t addr = smem_u32(bar);
+    for (uint32_t i = 0; i < kWaitSpins; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done)
+            return true;
+        if (i > 64)
+            __nanosleep(64);
+    }
+    return false;
+}
+
+// Barrier over the first `threads` threads of the CTA (named barrier 1).
+__device__ __forceinline__ void named_sync(uint32_t threads)
+{
+    asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
 }
 
 // ldmatrix / mma ---------------------------------------------------------------
