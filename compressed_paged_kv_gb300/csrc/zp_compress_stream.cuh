@@ -168,7 +168,7 @@ __device__ __forceinline__ uint32_t blk_swz(int row, int ch)
 }
 
 template <int D, int MT, int NS>
-__global__ void __launch_bounds__(kSThreads, 1) zp_compress_stream_kernel(const CompressArgs a)
+__global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const CompressArgs a)
 {
     using S = StreamSmem<D, MT, NS>;
     constexpr int ROWS = S::ROWS, SLAB = S::SLAB, STAGE = S::STAGE;
@@ -709,7 +709,7 @@ cudaError_t launch_stream_t(const CompressArgs &a, int units, cudaStream_t s)
 template <int D>
 cudaError_t launch_stream_for_d(const CompressArgs &a, int mt, int units, cudaStream_t s)
 {
-    constexpr int NS = 3;
+    constexpr int NS = 2;  // two stages: two CTAs fit on an SM
     switch (mt) {
     case 1: return launch_stream_t<D, 1, NS>(a, units, s);
     case 2: return launch_stream_t<D, 2, NS>(a, units, s);
