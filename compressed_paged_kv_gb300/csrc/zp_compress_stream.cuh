@@ -9,8 +9,9 @@
 // One unit = (request, layer, kv head) = T = N_max * b cached tokens.  A
 // cluster of `cs` CTAs owns the unit (cs = 1 up to 1024 tokens); CTA c owns
 // the chunk of TC = T / cs tokens starting at c * TC.  Each CTA is 8
-// consumer warps and one producer warp.  The producer streams the chunk
-// through a ring of NS shared-memory stages with TMA in three passes:
+// consumer warps (two groups of four taking alternate stages) and one
+// producer warp.  The producer streams the chunk through a ring of NS
+// shared-memory stages with TMA in three passes:
 //   pass 1  K blocks (tensor maps, 128-byte swizzle, kept in L2 for the
 //           next passes): window logits and the b x b Gram of every block on
 //           the tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate);
@@ -127,10 +128,11 @@ __device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2
     m = M;
 }
 
-constexpr int kSW = 8;                     // consumer warps
+constexpr int kSW = 8;                     // consumer warps, in two groups of four
+constexpr int kSGroupWarps = 4;            // the groups take alternate stages
 constexpr int kSThreads = (kSW + 1) * 32;  // + one producer warp
-constexpr int kSScoreBlocks = 8;           // blocks per stage in passes 1 and 2 (one per warp)
-constexpr int kSMoveBlocks = 4;            // blocks per stage in pass 3 (K and V slabs)
+constexpr int kSScoreBlocks = 4;           // blocks per stage in passes 1 and 2 (one per warp)
+constexpr int kSMoveBlocks = 2;            // blocks per stage in pass 3 (K and V slabs)
 constexpr int kSMaxTC = 1024;              // tokens per CTA at most
 constexpr int kSKeysPerLane = kSMaxTC / kSW / 32;
 
@@ -138,7 +140,7 @@ template <int D, int MT, int NS>
 struct StreamSmem {
     static constexpr int ROWS = MT * 16;
     static constexpr int SLAB = kBlk * D * 2;          // one (block, kv head) slab
-    static constexpr int STAGE = kSScoreBlocks * SLAB;  // 32 KB at d = 128
+    static constexpr int STAGE = kSScoreBlocks * SLAB;  // 16 KB at d = 128
     static constexpr int off_ring = 0;
     static constexpr int off_q = off_ring + NS * STAGE;         // bf16 [ROWS][D], swizzled
     static constexpr int off_tail = off_q + ROWS * D * 2;       // K slab, V slab of the last block
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kSW);
+            mbar_init(&empty[s], kSGroupWarps);
         }
         mbar_init(tailb, 1);
         mbar_init(xb1, cs);
@@ -315,6 +317,7 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
         bool bad = false;
         int idx = 0;
         const int mi = lane >> 3;
+        const int grp = wi / kSGroupWarps, gw = wi % kSGroupWarps;  // group, warp in group
         const uint32_t qb_base = smem_u32(sQ);
         int slot_of[MT][2];
 #pragma unroll
@@ -341,7 +344,7 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     gram[nt][e] = 0.f;
-            const uint32_t kb = smem_u32(sRing + s * STAGE + wi * SLAB);
+            const uint32_t kb = smem_u32(sRing + s * STAGE + gw * SLAB);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
                 uint32_t kf[4];
@@ -385,9 +388,11 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                 rsum[mt][hh] = 0.f;
             }
         for (int g = 0; g < n_score; ++g, ++idx) {
+            if ((g & 1) != grp)
+                continue;
             const int s = idx % NS;
             bad |= !mbar_wait(&full[s], (idx / NS) & 1);
-            const int key0 = (g * kSScoreBlocks + wi) * kBlk;
+            const int key0 = (g * kSScoreBlocks + gw) * kBlk;
             float acc[MT][2][4], gram[2][4];
             block_logits(s, key0, acc, gram, true);
             __syncwarp();
@@ -505,9 +510,11 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
         // ---- pass 2: importance and score of every key
         const size_t uo = ((size_t)l * a.R + r) * a.Hkv + h;
         for (int g = 0; g < n_score; ++g, ++idx) {
+            if ((g & 1) != grp)
+                continue;
             const int s = idx % NS;
             bad |= !mbar_wait(&full[s], (idx / NS) & 1);
-            const int key0 = (g * kSScoreBlocks + wi) * kBlk;
+            const int key0 = (g * kSScoreBlocks + gw) * kBlk;
             float acc[MT][2][4], gram[2][4];
             block_logits(s, key0, acc, gram, false);
             __syncwarp();
@@ -607,11 +614,13 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
         __nv_bfloat16 *vpool = static_cast<__nv_bfloat16 *>(a.vpools[l]);
         const uint64_t once = policy_evict_first();
         for (int g = 0; g < n_move; ++g, ++idx) {
+            if ((g & 1) != grp)
+                continue;
             const int s = idx % NS;
             bad |= !mbar_wait(&full[s], (idx / NS) & 1);
-            const int bi = wi >> 1;              // block of the stage
+            const int bi = gw >> 1;              // block of the stage
             const int q = g * kSMoveBlocks + bi;  // block of the chunk
-            const int r8 = (wi & 1) * 8 + lane;   // row of the block (lanes 0..7)
+            const int r8 = (gw & 1) * 8 + lane;   // row of the block (lanes 0..7)
             const bool tail = cs > 1 && q == nblk - 1;
             int dp = 0, dblk = -1;
             bool moved = false;
@@ -709,7 +718,7 @@ cudaError_t launch_stream_t(const CompressArgs &a, int units, cudaStream_t s)
 template <int D>
 cudaError_t launch_stream_for_d(const CompressArgs &a, int mt, int units, cudaStream_t s)
 {
-    constexpr int NS = 2;  // two stages: two CTAs fit on an SM
+    constexpr int NS = 4;  // four 16 KB stages: two CTAs fit on an SM
     switch (mt) {
     case 1: return launch_stream_t<D, 1, NS>(a, units, s);
     case 2: return launch_stream_t<D, 2, NS>(a, units, s);
