@@ -156,7 +156,9 @@ struct StreamSmem {
     static constexpr int off_pub = off_cand + kSW * kBlk * 8;   // u64 [b] sorted (remote-read)
     static constexpr int off_all = off_pub + kBlk * 8;          // u64 [kMaxCluster * b]
     static constexpr int off_ev = off_all + kMaxCluster * kBlk * 8;  // int [b]
-    static constexpr int off_bar = (off_ev + kBlk * 4 + 7) / 8 * 8;
+    static constexpr int off_sblk = off_ev + kBlk * 4;          // int [kSMaxTC / b] source blocks
+    static constexpr int off_dblk = off_sblk + kSMaxTC / kBlk * 4;  // int [.. + 1] destinations
+    static constexpr int off_bar = (off_dblk + (kSMaxTC / kBlk + 1) * 4 + 7) / 8 * 8;
     static constexpr int NBAR = 2 * NS + 3;  // full[NS], empty[NS], tail, exchange 1, exchange 2
     static constexpr int BYTES = off_bar + NBAR * 8;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024 B
@@ -197,6 +199,8 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
     uint64_t *sPub = reinterpret_cast<uint64_t *>(sm + S::off_pub);
     uint64_t *sAll = reinterpret_cast<uint64_t *>(sm + S::off_all);
     int *sEv = reinterpret_cast<int *>(sm + S::off_ev);
+    int *sSblk = reinterpret_cast<int *>(sm + S::off_sblk);  // chunk block q -> source block
+    int *sDblk = reinterpret_cast<int *>(sm + S::off_dblk);  // dst block of chunk block q-1+i
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::off_bar);
     uint64_t *full = bars, *empty = bars + NS;
     uint64_t *tailb = bars + 2 * NS, *xb1 = tailb + 1, *xb2 = tailb + 2;
@@ -227,6 +231,15 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
     const __nv_bfloat16 *kpool_in = static_cast<const __nv_bfloat16 *>(a.kpools[l]);
     const __nv_bfloat16 *vpool_in = static_cast<const __nv_bfloat16 *>(a.vpools[l]);
 
+    // the chunk's block ids, read once: source blocks of chunk blocks 0..nblk-1
+    // and destination blocks of logical blocks blk0-1 .. blk0+nblk-1 (a row
+    // moves at most one block down)
+    for (int q = tid; q < nblk; q += kSThreads)
+        sSblk[q] = src_row[blk0 + q];
+    for (int q = tid; q <= nblk; q += kSThreads) {
+        const int lb = blk0 - 1 + q;
+        sDblk[q] = (lb >= 0 && lb < a.N - 1) ? dst_row[lb] : -1;
+    }
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
@@ -247,7 +260,7 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
             const uint64_t keep = policy_evict_last(), once = policy_evict_first();
             bool ok = true;
             if (cs > 1) {
-                const int blk = src_row[blk0 + nblk - 1];
+                const int blk = sSblk[nblk - 1];
                 const size_t off = ((size_t)blk * a.Hkv + h) * kBlk * D;
                 mbar_arrive_expect_tx(tailb, 2 * SLAB);
                 bulk_g2s_hint(sTail, kpool_in + off, SLAB, tailb, once);
@@ -263,7 +276,7 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                     mbar_arrive_expect_tx(&full[s], STAGE);
                     uint8_t *dst = sRing + s * STAGE;
                     for (int i = 0; i < kSScoreBlocks; ++i) {
-                        const int blk = src_row[blk0 + g * kSScoreBlocks + i];
+                        const int blk = sSblk[g * kSScoreBlocks + i];
                         const int y = (blk * a.Hkv + h) * kBlk;
 #pragma unroll
                         for (int hf = 0; hf < HALVES; ++hf)
@@ -285,7 +298,7 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                     const int q = g * kSMoveBlocks + i;
                     if (cs > 1 && q == nblk - 1)
                         continue;  // the staged last block stands in for it
-                    const int blk = src_row[blk0 + q];
+                    const int blk = sSblk[q];
                     const size_t off = ((size_t)blk * a.Hkv + h) * kBlk * D;
                     bulk_g2s_hint(dst + i * SLAB, kpool_in + off, SLAB, &full[s], once);
                     bulk_g2s_hint(dst + (kSMoveBlocks + i) * SLAB, vpool_in + off, SLAB, &full[s],
@@ -363,17 +376,20 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                     mma_bf16(gram[1], kf[0], kf[2], kf[1], kf[3], kf[2], kf[3]);
                 }
             }
+            const bool masked_block = t0 + key0 + kBlk - 1 > C;  // holds window keys
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int slot = slot_of[mt][e >> 1];
-                        const int tok = t0 + key0 + nt * 8 + (lane & 3) * 2 + (e & 1);
                         float v = acc[mt][nt][e] * a.logit_scale;
-                        if (slot >= 0 && tok > C + slot)
-                            v = -INFINITY;
+                        if (masked_block) {
+                            const int slot = slot_of[mt][e >> 1];
+                            const int tok = t0 + key0 + nt * 8 + (lane & 3) * 2 + (e & 1);
+                            if (slot >= 0 && tok > C + slot)
+                                v = -INFINITY;
+                        }
                         acc[mt][nt][e] = v;
                     }
         };
@@ -636,8 +652,8 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                 }
                 if (!ev) {
                     dp = tok - before;
-                    dblk = dst_row[dp >> 4];
-                    moved = dp != tok || dblk != src_row[blk0 + q];
+                    dblk = sDblk[(dp >> 4) - blk0 + 1];
+                    moved = dp != tok || dblk != sSblk[q];
                     if (a.kept_out)
                         a.kept_out[uo * (size_t)(T - kBlk) + dp] = tok;
                 }
