@@ -268,10 +268,13 @@ cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s)
 
 int compress_cluster_size(int T)
 {
-    // the fewest CTAs per unit with at most 1024 tokens each, every chunk a
+    // the fewest CTAs per unit with at most ZP_STREAM_MAX_TC tokens each, every chunk a
     // whole number of 128-token stages
+#ifndef ZP_STREAM_MAX_TC
+#define ZP_STREAM_MAX_TC 1024
+#endif
     for (int cs = 1; cs <= kMaxCluster; ++cs)
-        if (T % cs == 0 && T / cs <= 1024 && (T / cs) % 128 == 0)
+        if (T % cs == 0 && T / cs <= ZP_STREAM_MAX_TC && (T / cs) % 128 == 0)
             return cs;
     return 0;
 }

@@ -27,8 +27,9 @@
 // remote mbarrier arrivals (the producer never waits on them).  The b evicted
 // tokens: a warp radix select (MSB first, one bit per step by ballot) over
 // 64-bit keys = order-preserving image of the fp32 score bits above the
-// complemented index, a per-CTA rank merge into a sorted list, and b steps of
-// a k-way merge of the cluster's sorted lists.
+// complemented index, a per-CTA rank merge into a sorted list, and a merge
+// of the cluster's sorted lists (ranks by binary search for up to four
+// lists, else b steps of a k-way merge).
 //
 // In-place safety: exactly b tokens are evicted, so destination j reads
 // source kept[j] with j <= kept[j] <= j + b.  Pass 3 handles the chunk's
@@ -118,6 +119,23 @@ __device__ __forceinline__ void warp_compact_keys(const uint64_t (&key)[KPL],
     }
 }
 
+// Number of entries of the ascending 16-entry list `a` below `key`.
+__device__ __forceinline__ int count_below16(const uint64_t *a, uint64_t key)
+{
+    int p = 0;
+    if (a[p + 7] < key)
+        p += 8;
+    if (a[p + 3] < key)
+        p += 4;
+    if (a[p + 1] < key)
+        p += 2;
+    if (a[p] < key)
+        p += 1;
+    if (p == 15 && a[15] < key)
+        p = 16;
+    return p;
+}
+
 // Merge of two online-softmax partials (m, s) in base 2 (-inf m: empty).
 __device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2)
 {
@@ -133,7 +151,10 @@ constexpr int kSGroupWarps = 4;            // the groups take alternate stages
 constexpr int kSThreads = (kSW + 1) * 32;  // + one producer warp
 constexpr int kSScoreBlocks = 4;           // blocks per stage in passes 1 and 2 (one per warp)
 constexpr int kSMoveBlocks = 2;            // blocks per stage in pass 3 (K and V slabs)
-constexpr int kSMaxTC = 1024;              // tokens per CTA at most
+#ifndef ZP_STREAM_MAX_TC
+#define ZP_STREAM_MAX_TC 1024
+#endif
+constexpr int kSMaxTC = ZP_STREAM_MAX_TC;  // tokens per CTA at most
 constexpr int kSKeysPerLane = kSMaxTC / kSW / 32;
 
 template <int D, int MT, int NS>
@@ -251,8 +272,11 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
         fence_mbar_init();
     }
     __syncthreads();
+    // Peers' barriers must exist before a remote arrive: every thread arrives
+    // here and waits only right before its first remote access, so the
+    // producer starts streaming at once.
     if (cs > 1)
-        cluster_sync();  // every peer's barriers exist before any remote arrive
+        cluster_arrive();
 
     if (wi == kSW) {
         // ------------------------------------------------------- producer
@@ -311,6 +335,8 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
             }
         }
         __syncwarp();
+        if (cs > 1)
+            cluster_wait();  // (the arrive right after set-up)
     } else {
         // ------------------------------------------------------- consumers
         {
@@ -498,6 +524,7 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
         }
         named_sync(NCT);
         if (cs > 1) {
+            cluster_wait();  // (the arrive right after set-up)
             if (tid == 0)
                 for (int c = 0; c < cs; ++c)
                     mbar_arrive_remote(dsmem_addr(xb1, c));
@@ -604,7 +631,20 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
             for (int e = tid; e < cs * kBlk; e += NCT)
                 sAll[e] = ld_dsmem_u64(dsmem_addr(sPub + (e & (kBlk - 1)), e / kBlk));
             named_sync(NCT);
-            if (wi == 0) {  // b steps of a k-way merge of the sorted lists
+            if (cs <= 4) {
+                // rank of each candidate: its place in its own sorted list plus
+                // a binary search in each other list
+                for (int e = tid; e < cs * kBlk; e += NCT) {
+                    const uint64_t k0 = sAll[e];
+                    const int c0 = e / kBlk;
+                    int rank = e % kBlk;
+                    for (int c = 0; c < cs; ++c)
+                        if (c != c0)
+                            rank += count_below16(sAll + c * kBlk, k0);
+                    if (rank < kBlk)
+                        sEv[rank] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k0));
+                }
+            } else if (wi == 0) {  // b steps of a k-way merge of the sorted lists
                 int ptr = 0;
                 for (int step = 0; step < kBlk; ++step) {
                     const uint64_t head =
