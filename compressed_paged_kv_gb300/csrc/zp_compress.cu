@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
         return a.tables[(size_t)row * a.stride + p];
     };
     int my_need = 0;
+#pragma unroll 8
     for (int e = e0; e < e1; ++e) {
         const int blk = src_of(e);
         if (blk < 0 || blk >= a.num_blocks) {
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
             *a.ws.call = s_err;
         return;
     }
+#pragma unroll 8
     for (int e = e0; e < e1; ++e) {
         const int blk = src_of(e);
         int dst = blk;
@@ -271,7 +273,7 @@ int compress_cluster_size(int T)
     // the fewest CTAs per unit with at most ZP_STREAM_MAX_TC tokens each, every chunk a
     // whole number of 128-token stages
 #ifndef ZP_STREAM_MAX_TC
-#define ZP_STREAM_MAX_TC 1024
+#define ZP_STREAM_MAX_TC 2048
 #endif
     for (int cs = 1; cs <= kMaxCluster; ++cs)
         if (T % cs == 0 && T / cs <= ZP_STREAM_MAX_TC && (T / cs) % 128 == 0)

@@ -152,7 +152,7 @@ constexpr int kSThreads = (kSW + 1) * 32;  // + one producer warp
 constexpr int kSScoreBlocks = 4;           // blocks per stage in passes 1 and 2 (one per warp)
 constexpr int kSMoveBlocks = 2;            // blocks per stage in pass 3 (K and V slabs)
 #ifndef ZP_STREAM_MAX_TC
-#define ZP_STREAM_MAX_TC 1024
+#define ZP_STREAM_MAX_TC 2048
 #endif
 constexpr int kSMaxTC = ZP_STREAM_MAX_TC;  // tokens per CTA at most
 constexpr int kSKeysPerLane = kSMaxTC / kSW / 32;
