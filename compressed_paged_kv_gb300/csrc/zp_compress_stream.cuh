@@ -16,7 +16,9 @@
 //           next passes): window logits and the b x b Gram of every block on
 //           the tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate);
 //           online row max / sum per window row; Lightning Redundancy Score;
-//   pass 2  the same K blocks again (from L2): logits again, importance =
+//   pass 2  the same K blocks again, in reverse order so that they come from
+//           L2 (an LRU cache reused cyclically would evict each block just
+//           before its reuse): logits again, importance =
 //           mean over the w*G window rows of exp(l - m) / S with the
 //           statistics of all T keys, score = importance - lambda * redundancy;
 //   pass 3  K and V slabs (bulk copies, plain layout): the kept rows of each
@@ -299,8 +301,12 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                         ok &= mbar_wait(&empty[s], ((idx / NS) - 1) & 1);
                     mbar_arrive_expect_tx(&full[s], STAGE);
                     uint8_t *dst = sRing + s * STAGE;
+                    // pass 2 walks the chunk backwards: it starts on the blocks
+                    // pass 1 read last (still in L2), and pass 3, forwards,
+                    // starts on the blocks pass 2 read last
+                    const int gg = pass == 0 ? g : n_score - 1 - g;
                     for (int i = 0; i < kSScoreBlocks; ++i) {
-                        const int blk = sSblk[g * kSScoreBlocks + i];
+                        const int blk = sSblk[gg * kSScoreBlocks + i];
                         const int y = (blk * a.Hkv + h) * kBlk;
 #pragma unroll
                         for (int hf = 0; hf < HALVES; ++hf)
@@ -557,7 +563,7 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                 continue;
             const int s = idx % NS;
             bad |= !mbar_wait(&full[s], (idx / NS) & 1);
-            const int key0 = (g * kSScoreBlocks + gw) * kBlk;
+            const int key0 = ((n_score - 1 - g) * kSScoreBlocks + gw) * kBlk;  // backwards
             float acc[MT][2][4], gram[2][4];
             block_logits(s, key0, acc, gram, false);
             __syncwarp();
