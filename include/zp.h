@@ -127,8 +127,10 @@ void zp_cache_destroy(zp_cache *cache);
  *  window_q      device bf16 [L][R][Hq][w][d]: window queries of request r
  *                (row g*w + i of kv head h's group is query head h*G+g at
  *                window slot i, the query of token T - w + i)
- *  n_max         blocks per request at compression; n_max*b a multiple of 128,
- *                at most 4096
+ *  n_max         blocks per request at compression; T = n_max*b must split
+ *                into at most 16 equal chunks of at most 2048 tokens, each a
+ *                multiple of 128 (every multiple of 128 up to 2048; 4096, 8192,
+ *                ... up to 32768 when divisible accordingly)
  *  window        w, 1 <= w <= b, w * (Hq/Hkv) <= 64
  *  lambda        redundancy weight
  *  pool          free stack + refcounts, updated in place

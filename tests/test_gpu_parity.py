@@ -107,6 +107,8 @@ SHAPES = [
     ("T512_cluster4", dict(N=32, R=3)),
     ("T1024_cluster8", dict(N=64, R=2)),
     ("T4096_wide", dict(N=256, R=2)),
+    ("T8192_cluster4", dict(N=512, R=1)),
+    ("T10240_cluster5_kway", dict(N=640, R=1)),
     ("T384_single_cta", dict(N=24, R=2)),
     ("d64_rows64", dict(d=64, N=32, w=16, R=2)),
     ("w1_G1", dict(Hq=8, w=1, N=16, R=3)),
@@ -272,3 +274,43 @@ def test_decode_bad_length_is_flagged(orc):
     out = torch.zeros_like(q)
     assert cache.decode(0, q, st.block_tables, lens, 0.125, out) == zp.OK
     assert cache.status() == zp.ERR_DEVICE_CHECK
+
+
+def test_overlapped_compress_and_decode_match_serial(orc):
+    """Compression of the requests at N_max on one stream while the others
+    decode on a second stream (disjoint requests) gives exactly the results of
+    running the two calls one after the other."""
+    wl = W.scaled(W.WORKLOADS["mixed"], name="overlap", L=3, R=40, mixed_compress=6)
+
+    def run(overlap):
+        st = W.build_cache(wl, DEV)
+        cache = H.make_cache(st)
+        drows = st.decode_rows
+        outs = [torch.empty((drows.numel(), wl.Hq, wl.d), dtype=torch.bfloat16, device=DEV)
+                for _ in range(wl.L)]
+        main = torch.cuda.current_stream()
+        s_dec = torch.cuda.Stream(priority=-1) if overlap else main
+        s_cmp = torch.cuda.Stream() if overlap else main
+        ev = torch.cuda.Event()
+        ev.record(main)
+        s_dec.wait_event(ev)
+        s_cmp.wait_event(ev)
+        for l in range(wl.L):
+            q = st.decode_q[l][drows.long()].contiguous()
+            cache.decode(l, q, st.block_tables, st.lengths, 1.0 / math.sqrt(wl.d), outs[l],
+                         req_idx=drows, stream=s_dec)
+        cache.compress(st.block_tables, st.lengths, st.window_q, wl.N, wl.w, wl.lam,
+                       st.free_ids, st.free_count, st.refcount, req_idx=st.compress_rows,
+                       stream=s_cmp)
+        torch.cuda.synchronize()
+        assert cache.status() == zp.OK
+        return st, outs
+
+    st_o, out_o = run(True)
+    st_s, out_s = run(False)
+    for a, b in zip(out_o, out_s):
+        assert torch.equal(a, b)
+    for a, b in zip(st_o.k_pools + st_o.v_pools, st_s.k_pools + st_s.v_pools):
+        assert torch.equal(a, b)
+    for name in ("block_tables", "lengths", "refcount", "free_ids", "free_count"):
+        assert torch.equal(getattr(st_o, name), getattr(st_s, name)), name
