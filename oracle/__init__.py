@@ -79,6 +79,10 @@ def _declare(lib):
     lib.zpo_compress.restype = I
     lib.zpo_decode_attn.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, D, P, P]
     lib.zpo_decode_attn.restype = I
+    lib.zpo_append_slots.argtypes = [I, I, I, I, I, P, P, P, I, I, P, P, I, I, P, P, P, I, P, P]
+    lib.zpo_append_slots.restype = I
+    lib.zpo_append_kv.argtypes = [I, I, I, I, P, P, P, I, I, P, P, I, P, P]
+    lib.zpo_append_kv.restype = I
     return lib
 
 
@@ -251,3 +255,58 @@ class Oracle:
                                       _p(lengths), R, Hq, Hkv, d, b, num_blocks, float(scale),
                                       _p(out64), _p(out16))
         return st, out64, out16
+
+    # -- decode-side append ---------------------------------------------------
+    def append_slots(self, kpools, vpools, tables, lengths, free_ids, free_count, refcount,
+                     n_max, req_idx=None):
+        """Reserves each listed request's next slot on host copies.
+
+        Returns dict(status, kpools, vpools, tables, lengths, free_ids,
+        free_count, refcount, triggers) -- the inputs unchanged when status != 0.
+        """
+        L = len(kpools)
+        num_blocks, Hkv, b, d = kpools[0].shape
+        kout = [_c(k, np.uint16).copy() for k in kpools]
+        vout = [_c(v, np.uint16).copy() for v in vpools]
+        tables = _c(tables, np.int32).copy()
+        lengths = _c(lengths, np.int32).copy()
+        free_ids = _c(free_ids, np.int32).copy()
+        refcount = _c(refcount, np.int32).copy()
+        num_rows, stride = tables.shape
+        if req_idx is not None:
+            req_idx = _c(req_idx, np.int32)
+            R = req_idx.shape[0]
+        else:
+            R = num_rows
+        arr = ctypes.c_void_p * L
+        kp = arr(*[k.ctypes.data for k in kout])
+        vp = arr(*[v.ctypes.data for v in vout])
+        fc = ctypes.c_int32(int(free_count))
+        trig = np.zeros(max(R, 1), dtype=np.int32)
+        nt = ctypes.c_int32(0)
+        st = self.lib.zpo_append_slots(L, Hkv, d, b, num_blocks, kp, vp, _p(tables), stride,
+                                       num_rows, _p(lengths), _p(req_idx), R, int(n_max),
+                                       _p(refcount), _p(free_ids), ctypes.byref(fc),
+                                       free_ids.shape[0], _p(trig), ctypes.byref(nt))
+        return dict(status=st, kpools=kout, vpools=vout, tables=tables, lengths=lengths,
+                    free_ids=free_ids, free_count=fc.value, refcount=refcount,
+                    triggers=trig[:nt.value].copy())
+
+    def append_kv(self, kpool, vpool, tables, lengths, k_new, v_new, req_idx=None):
+        """Writes one layer's new-token rows into copies of its pools; returns
+        (status, kpool, vpool)."""
+        kpool = _c(kpool, np.uint16).copy()
+        vpool = _c(vpool, np.uint16).copy()
+        tables = _c(tables, np.int32)
+        lengths = _c(lengths, np.int32)
+        k_new = _c(k_new, np.uint16)
+        v_new = _c(v_new, np.uint16)
+        num_blocks, Hkv, b, d = kpool.shape
+        num_rows, stride = tables.shape
+        R = k_new.shape[0]
+        if req_idx is not None:
+            req_idx = _c(req_idx, np.int32)
+        st = self.lib.zpo_append_kv(Hkv, d, b, num_blocks, _p(kpool), _p(vpool), _p(tables),
+                                    stride, num_rows, _p(lengths), _p(req_idx), R, _p(k_new),
+                                    _p(v_new))
+        return st, kpool, vpool

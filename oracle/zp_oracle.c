@@ -29,6 +29,11 @@
  *   commit     [ZP-nl Methodologie §1, §3; PKV]: tables, lengths, refcounts,
  *              released blocks back to the free stack.
  *   decode     [PKV]: attention of one query per head over the block table.
+ *   append     [PKV; ZP-nl Methodologie §1]: the slot of each decoding request's
+ *              next token (a new block only when the last one is full,
+ *              copy-on-write of a shared block), the new token's K/V written
+ *              there, and the requests whose cache just reached N_max full
+ *              blocks (the compression trigger).
  *
  * Every floating-point quantity is computed in double from the exact widening
  * of the bf16 inputs.  No blocking, fusion or reordering beyond the definitions.
@@ -526,5 +531,152 @@ int zpo_decode_attn(const uint16_t *q, const uint16_t *kpool, const uint16_t *vp
     }
     free(logit);
     free(acc);
+    return ZPO_OK;
+}
+
+/* -------------------------------------------------------------- append */
+
+/* Reserves the slot of the next token of each listed request, one request
+ * after the other in list order [PKV, "How it works": a new block is taken
+ * only when the previous ones are full; a request about to write into a
+ * shared block first copies it to a fresh block and drops one reference to
+ * the original (copy-on-write); ZP-nl Methodologie §1: a request that holds
+ * N_max full blocks is due for compression].
+ *
+ * For request r (row = req_idx[r], or r), p = lengths[row] is the position of
+ * its new token, in block e = p / b, slot p % b:
+ *   - table entry e < 0 (only allowed at slot 0): pop a fresh block;
+ *   - else, if the block's CURRENT refcount is > 1: pop a fresh block, copy
+ *     slots 0 .. p%b - 1 of every layer and kv head (K and V) into it, and
+ *     take one reference off the original;
+ *   - else the block is written in place.
+ * A popped block comes from the top of the free stack and gets refcount 1.
+ * Then lengths[row] = p + 1, and when n_max > 0 and p + 1 == n_max * b the
+ * row is appended to trigger_rows.  Because refcounts are updated as the
+ * loop goes, the last of several writers of one shared block in this call
+ * finds it unshared and writes in place.
+ *
+ * Checked before anything changes (all or nothing): rows in range and
+ * distinct, 0 <= p < stride*b, p < n_max*b when n_max > 0, the tail entry a
+ * valid block (or negative at slot 0) with refcount >= 1 -> INVALID_ARG; the
+ * free stack long enough -> OUT_OF_BLOCKS; a popped id in range with
+ * refcount 0, free_count within [0, capacity] -> DEVICE_CHECK.
+ * kpool/vpool: L pools [num_blocks][Hkv][b][d], modified in place. */
+int zpo_append_slots(int L, int Hkv, int d, int b, int num_blocks, uint16_t *const *kpool,
+                     uint16_t *const *vpool, int32_t *tables, int stride, int num_rows,
+                     int32_t *lengths, const int32_t *req_idx, int R, int n_max,
+                     int32_t *refcount, int32_t *free_ids, int32_t *free_count, int capacity,
+                     int32_t *trigger_rows, int32_t *trigger_count)
+{
+    if (R < 0 || b < 1 || stride < 1 || n_max < 0)
+        return ZPO_ERR_INVALID_ARG;
+    int fc = *free_count;
+    if (fc < 0 || fc > capacity)
+        return ZPO_ERR_DEVICE_CHECK;
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        if (row < 0 || row >= num_rows)
+            return ZPO_ERR_INVALID_ARG;
+        for (int r2 = 0; r2 < r; ++r2)
+            if ((req_idx ? req_idx[r2] : r2) == row)
+                return ZPO_ERR_INVALID_ARG;
+        int p = lengths[row];
+        if (p < 0 || p >= stride * b || (n_max > 0 && p >= n_max * b))
+            return ZPO_ERR_INVALID_ARG;
+        int32_t blk = tables[(size_t)row * stride + p / b];
+        if (blk >= num_blocks || (blk < 0 && p % b != 0) || (blk >= 0 && refcount[blk] < 1))
+            return ZPO_ERR_INVALID_ARG;
+    }
+
+    /* dry run on a copy of the refcounts: the pops this call needs */
+    int32_t *rc = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_blocks > 0 ? num_blocks : 1));
+    memcpy(rc, refcount, sizeof(int32_t) * (size_t)num_blocks);
+    int pops = 0;
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        int p = lengths[row];
+        int32_t blk = tables[(size_t)row * stride + p / b];
+        if (blk < 0) {
+            ++pops;
+        } else if (rc[blk] > 1) {
+            rc[blk] -= 1;
+            ++pops;
+        }
+    }
+    free(rc);
+    if (pops > fc)
+        return ZPO_ERR_OUT_OF_BLOCKS;
+    for (int k = 0; k < pops; ++k) {
+        int32_t t = free_ids[fc - 1 - k];
+        if (t < 0 || t >= num_blocks || refcount[t] != 0)
+            return ZPO_ERR_DEVICE_CHECK;
+    }
+
+    /* the real pass */
+    int ntrig = 0;
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        int p = lengths[row], e = p / b, slot = p % b;
+        int32_t *entry = tables + (size_t)row * stride + e;
+        int32_t blk = *entry;
+        if (blk < 0 || refcount[blk] > 1) {
+            int32_t fresh = free_ids[--fc];
+            if (blk >= 0) {
+                for (int l = 0; l < L; ++l)
+                    for (int h = 0; h < Hkv; ++h) {
+                        size_t from = ((size_t)blk * Hkv + h) * (size_t)b * d;
+                        size_t to = ((size_t)fresh * Hkv + h) * (size_t)b * d;
+                        memcpy(kpool[l] + to, kpool[l] + from, sizeof(uint16_t) * (size_t)slot * d);
+                        memcpy(vpool[l] + to, vpool[l] + from, sizeof(uint16_t) * (size_t)slot * d);
+                    }
+                refcount[blk] -= 1;
+            }
+            refcount[fresh] = 1;
+            *entry = fresh;
+        }
+        lengths[row] = p + 1;
+        if (n_max > 0 && p + 1 == n_max * b) {
+            if (trigger_rows)
+                trigger_rows[ntrig] = row;
+            ++ntrig;
+        }
+    }
+    *free_count = fc;
+    if (trigger_count)
+        *trigger_count = ntrig;
+    return ZPO_OK;
+}
+
+/* Writes the new token of each listed request into one layer's pools [PKV]:
+ * the token at position p = lengths[row] - 1 (the slot zpo_append_slots
+ * reserved) gets k_new[r][h] and v_new[r][h] for every kv head h.
+ * k_new, v_new: [R][Hkv][d].  Checked first: rows in range, 1 <= lengths[row]
+ * <= stride*b, the block at p / b in range -> INVALID_ARG, nothing written. */
+int zpo_append_kv(int Hkv, int d, int b, int num_blocks, uint16_t *kpool, uint16_t *vpool,
+                  const int32_t *tables, int stride, int num_rows, const int32_t *lengths,
+                  const int32_t *req_idx, int R, const uint16_t *k_new, const uint16_t *v_new)
+{
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        if (row < 0 || row >= num_rows)
+            return ZPO_ERR_INVALID_ARG;
+        int p = lengths[row] - 1;
+        if (p < 0 || p >= stride * b)
+            return ZPO_ERR_INVALID_ARG;
+        int32_t blk = tables[(size_t)row * stride + p / b];
+        if (blk < 0 || blk >= num_blocks)
+            return ZPO_ERR_INVALID_ARG;
+    }
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        int p = lengths[row] - 1;
+        int32_t blk = tables[(size_t)row * stride + p / b];
+        for (int h = 0; h < Hkv; ++h) {
+            size_t to = (((size_t)blk * Hkv + h) * b + p % b) * d;
+            size_t from = ((size_t)r * Hkv + h) * d;
+            memcpy(kpool + to, k_new + from, sizeof(uint16_t) * (size_t)d);
+            memcpy(vpool + to, v_new + from, sizeof(uint16_t) * (size_t)d);
+        }
+    }
     return ZPO_OK;
 }

@@ -581,4 +581,207 @@ def pin_decode_compacted_equals_masked(orc):
             close(o64[r, hq], o.numpy(), 1e-12, "compacted vs masked attention")
 
 
+# ------------------------------------------------------------ decode append
+
+def _logical(pool, table, length, h, b):
+    """Rows 0 .. length-1 of kv head h, gathered through a block table."""
+    return np.stack([pool[table[t // b], h, t % b] for t in range(length)]) if length else \
+        np.zeros((0, pool.shape[3]), dtype=pool.dtype)
+
+
+def pin_append_fork_handworked(orc):
+    """The hand-worked fork of tests/golden/append_fork_handworked.json."""
+    with open(os.path.join(GOLDEN, "append_fork_handworked.json")) as f:
+        gd = json.load(f)
+    b, nb, L, Hkv, d = gd["b"], gd["num_blocks"], 2, 2, 3
+    g = rng(110)
+    kp = [bf16(g.standard_normal((nb, Hkv, b, d))) for _ in range(L)]
+    vp = [bf16(g.standard_normal((nb, Hkv, b, d))) for _ in range(L)]
+    for case in gd["cases"]:
+        res = orc.append_slots(kp, vp, gd["tables"], gd["lengths"], gd["free_ids"],
+                               len(gd["free_ids"]), gd["refcount"], gd["n_max"],
+                               req_idx=np.array(case["req_idx"], dtype=np.int32))
+        assert res["status"] == 0
+        assert res["tables"].tolist() == case["tables"]
+        assert res["lengths"].tolist() == case["lengths"]
+        assert res["refcount"].tolist() == case["refcount"]
+        assert res["free_count"] == case["free_count"]
+        assert res["free_ids"][:res["free_count"]].tolist() == gd["free_ids"][:case["free_count"]]
+        assert res["triggers"].tolist() == case["triggers"]
+        for src, dst, rows in case["copied"]:
+            for l in range(L):
+                assert np.array_equal(res["kpools"][l][dst, :, :rows], kp[l][src, :, :rows])
+                assert np.array_equal(res["vpools"][l][dst, :, :rows], vp[l][src, :, :rows])
+                assert np.array_equal(res["kpools"][l][src], kp[l][src])
+                assert np.array_equal(res["vpools"][l][src], vp[l][src])
+
+
+def _fork_cache(seed, R=10, b=4, nmax=5, L=2, Hkv=2, d=4, spare=40):
+    """A random cache with samples that share their prompt blocks (a partial
+    tail included), some full tails and some reserved (allocated, empty) tail
+    blocks.  Table entries beyond a row's blocks are -1."""
+    g = rng(seed)
+    num_blocks = R * nmax + spare
+    perm = g.permutation(num_blocks).astype(np.int32)
+    tables = np.full((R, nmax + 1), -1, dtype=np.int32)
+    lengths = np.zeros(R, dtype=np.int32)
+    nxt = 0
+    r = 0
+    while r < R:
+        fan = min(int(g.integers(1, 4)), R - r)      # samples of one prompt
+        length = int(g.integers(0, nmax * b))
+        nblk = -(-length // b)
+        blocks = perm[nxt:nxt + nblk]
+        nxt += nblk
+        for k in range(fan):
+            tables[r + k, :nblk] = blocks
+            lengths[r + k] = length
+        r += fan
+    for r in range(R):                                 # some rows hold a reserved empty block
+        p = int(lengths[r])
+        if p % b == 0 and p // b < nmax and g.random() < 0.4:
+            tables[r, p // b] = perm[nxt]
+            nxt += 1
+    rc = np.zeros(num_blocks, dtype=np.int32)
+    for x in tables.reshape(-1):
+        if x >= 0:
+            rc[x] += 1
+    free = np.full(num_blocks, -1, dtype=np.int32)
+    nfree = num_blocks - nxt
+    free[:nfree] = perm[nxt:]
+    kp = [bf16(g.standard_normal((num_blocks, Hkv, b, d))) for _ in range(L)]
+    vp = [bf16(g.standard_normal((num_blocks, Hkv, b, d))) for _ in range(L)]
+    return dict(tables=tables, lengths=lengths, rc=rc, free=free, nfree=nfree, kp=kp, vp=vp,
+                b=b, nmax=nmax, L=L, Hkv=Hkv, num_blocks=num_blocks)
+
+
+def pin_append_invariants(orc):
+    """On random forked caches: the logical content of every row is unchanged,
+    a row writes only unshared blocks, refcounts equal table references, free
+    and used blocks partition the pool, and the number of copies of a block
+    with m writers in the call and refcount c at the start is min(m, c - 1)
+    (every writer but the last copies unless other holders remain)."""
+    for seed in range(120, 126):
+        c = _fork_cache(seed)
+        b, nmax = c["b"], c["nmax"]
+        R = c["tables"].shape[0]
+        req = rng(seed + 1000).permutation(R).astype(np.int32)
+        res = orc.append_slots(c["kp"], c["vp"], c["tables"], c["lengths"], c["free"],
+                               c["nfree"], c["rc"], nmax, req_idx=req)
+        assert res["status"] == 0
+        writers = {}
+        unalloc = 0
+        for r in req:
+            p = int(c["lengths"][r])
+            x = int(c["tables"][r, p // b])
+            if x < 0:
+                unalloc += 1
+            else:
+                writers[x] = writers.get(x, 0) + 1
+        copies = sum(min(m, int(c["rc"][x]) - 1) for x, m in writers.items())
+        assert c["nfree"] - res["free_count"] == unalloc + copies
+        for x, m in writers.items():
+            assert res["refcount"][x] == c["rc"][x] - min(m, int(c["rc"][x]) - 1)
+        for r in range(R):
+            p = int(c["lengths"][r])
+            assert res["lengths"][r] == p + 1
+            for l in range(c["L"]):
+                for h in range(c["Hkv"]):
+                    assert np.array_equal(_logical(res["kpools"][l], res["tables"][r], p, h, b),
+                                          _logical(c["kp"][l], c["tables"][r], p, h, b))
+                    assert np.array_equal(_logical(res["vpools"][l], res["tables"][r], p, h, b),
+                                          _logical(c["vp"][l], c["tables"][r], p, h, b))
+        # the block each row will write is exclusively its own
+        tails = [int(res["tables"][r, int(c["lengths"][r]) // b]) for r in range(R)]
+        assert len(set(tails)) == R
+        assert all(res["refcount"][x] == 1 for x in tails)
+        ref = np.zeros_like(res["refcount"])
+        for x in res["tables"].reshape(-1):
+            if x >= 0:
+                ref[x] += 1
+        assert np.array_equal(ref, res["refcount"])
+        fc = res["free_count"]
+        assert fc + int(np.count_nonzero(res["refcount"] >= 1)) == c["num_blocks"]
+        assert np.all(res["refcount"][res["free_ids"][:fc]] == 0)
+        for l in range(c["L"]):                       # blocks still referenced are untouched
+            used = [x for x in range(c["num_blocks"]) if c["rc"][x] > 0]
+            assert np.array_equal(res["kpools"][l][used], c["kp"][l][used])
+            assert np.array_equal(res["vpools"][l][used], c["vp"][l][used])
+        trig = [int(r) for r in req if c["lengths"][r] + 1 == nmax * b]
+        assert res["triggers"].tolist() == trig
+
+
+def pin_append_errors(orc):
+    """All or nothing: a row already holding N_max full blocks, a partial tail
+    with no block, a duplicate row or too few free blocks change nothing."""
+    b, nmax = 4, 2
+    kp = [bf16(np.ones((6, 1, b, 2)))]
+    vp = [bf16(np.ones((6, 1, b, 2)))]
+    base = dict(tables=np.array([[0, 1, -1], [0, 2, -1]], dtype=np.int32),
+                lengths=np.array([6, 6], dtype=np.int32),
+                rc=np.array([2, 1, 1, 0, 0, 0], dtype=np.int32),
+                free=np.array([5, 4, 3, -1, -1, -1], dtype=np.int32))
+
+    def run(tables=None, lengths=None, rc=None, fc=3, req=None):
+        t = base["tables"] if tables is None else np.array(tables, dtype=np.int32)
+        ln = base["lengths"] if lengths is None else np.array(lengths, dtype=np.int32)
+        r = base["rc"] if rc is None else np.array(rc, dtype=np.int32)
+        res = orc.append_slots(kp, vp, t, ln, base["free"], fc, r, nmax,
+                               req_idx=None if req is None else np.array(req, dtype=np.int32))
+        if res["status"] != 0:
+            assert np.array_equal(res["tables"], t) and np.array_equal(res["lengths"], ln)
+            assert np.array_equal(res["refcount"], r) and res["free_count"] == fc
+        return res["status"]
+
+    assert run() == 0
+    assert run(lengths=[8, 6]) == -1          # due for compression first
+    assert run(lengths=[6, 9]) == -1          # beyond the table row
+    assert run(tables=[[0, 1, -1], [0, -1, -1]], rc=[2, 1, 0, 0, 0, 0]) == -1  # partial, no block
+    assert run(req=[1, 1]) == -1              # duplicate row
+    assert run(rc=[2, 0, 1, 0, 0, 0]) == -1   # a tail block with no reference
+    # two new blocks needed (row 0's tail 1 is shared with nothing; make it shared)
+    t = [[0, 1, -1], [0, 1, -1]]
+    assert run(tables=t, rc=[2, 2, 0, 0, 0, 0], lengths=[4, 5], fc=0) == -3
+    assert run(tables=t, rc=[2, 2, 0, 0, 0, 0], lengths=[5, 5], fc=0) == -3
+
+
+def pin_append_kv_then_decode(orc):
+    """After the slots are reserved and each layer's new K/V row written, the
+    new row sits at position p of the row's table, nothing else moved, and
+    decode attention over the grown cache equals torch SDPA over the old
+    logical rows with the new one appended."""
+    c = _fork_cache(140, R=8, L=2, Hkv=2, d=8)
+    b, nmax, Hkv, d = c["b"], c["nmax"], c["Hkv"], 8
+    R = c["tables"].shape[0]
+    res = orc.append_slots(c["kp"], c["vp"], c["tables"], c["lengths"], c["free"], c["nfree"],
+                           c["rc"], nmax)
+    assert res["status"] == 0
+    g = rng(141)
+    G = 2
+    scale = 1.0 / math.sqrt(d)
+    for l in range(c["L"]):
+        kn = bf16(g.standard_normal((R, Hkv, d)))
+        vn = bf16(g.standard_normal((R, Hkv, d)))
+        st, kpool, vpool = orc.append_kv(res["kpools"][l], res["vpools"][l], res["tables"],
+                                         res["lengths"], kn, vn)
+        assert st == 0
+        q = bf16(g.standard_normal((R, Hkv * G, d)))
+        st, o64, _ = orc.decode_attn(q, kpool, vpool, res["tables"], res["lengths"], scale)
+        assert st == 0
+        for r in range(R):
+            p = int(c["lengths"][r])
+            for h in range(Hkv):
+                K = _logical(kpool, res["tables"][r], p + 1, h, b)
+                V = _logical(vpool, res["tables"][r], p + 1, h, b)
+                assert np.array_equal(K[:p], _logical(c["kp"][l], c["tables"][r], p, h, b))
+                assert np.array_equal(V[:p], _logical(c["vp"][l], c["tables"][r], p, h, b))
+                assert np.array_equal(K[p], kn[r, h]) and np.array_equal(V[p], vn[r, h])
+                for gq in range(G):
+                    hq = h * G + gq
+                    o = torch.nn.functional.scaled_dot_product_attention(
+                        torch.tensor(widen(q[r, hq]))[None, None, :], torch.tensor(widen(K))[None],
+                        torch.tensor(widen(V))[None], scale=scale)[0, 0]
+                    close(o64[r, hq], o.numpy(), 1e-12, "decode after append")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -50,6 +50,26 @@ MUTANTS = [
     ("decode wrong kv head", "int h = hq / G;", "int h = hq % Hkv;"),
     ("bf16 rounding truncates", "double q = rint(ax / spacing);",
      "double q = floor(ax / spacing);"),
+    ("append: shared tail written in place", "if (blk < 0 || refcount[blk] > 1) {\n            int32_t fresh",
+     "if (blk < 0) {\n            int32_t fresh"),
+    ("append: copy-on-write one row short",
+     "memcpy(kpool[l] + to, kpool[l] + from, sizeof(uint16_t) * (size_t)slot * d);",
+     "memcpy(kpool[l] + to, kpool[l] + from, sizeof(uint16_t) * (size_t)(slot > 0 ? slot - 1 : 0) * d);"),
+    ("append: V not copied on write",
+     "memcpy(vpool[l] + to, vpool[l] + from, sizeof(uint16_t) * (size_t)slot * d);", ""),
+    ("append: original keeps its reference",
+     "                refcount[blk] -= 1;\n            }\n            refcount[fresh] = 1;",
+     "            }\n            refcount[fresh] = 1;"),
+    ("append: pop from the bottom", "int32_t fresh = free_ids[--fc];",
+     "int32_t fresh = free_ids[*free_count - fc--];"),
+    ("append: trigger one token early", "if (n_max > 0 && p + 1 == n_max * b) {",
+     "if (n_max > 0 && p + 2 == n_max * b) {"),
+    ("append: length not advanced", "lengths[row] = p + 1;", "lengths[row] = p;"),
+    ("append: full row accepted", "if (p < 0 || p >= stride * b || (n_max > 0 && p >= n_max * b))",
+     "if (p < 0 || p >= stride * b)"),
+    ("append: new row in the next slot",
+     "size_t to = (((size_t)blk * Hkv + h) * b + p % b) * d;",
+     "size_t to = (((size_t)blk * Hkv + h) * b + (p + 1) % b) * d;"),
     ("length check dropped", "if (lengths[row] != N * b)\n            return ZPO_ERR_INVALID_ARG;",
      ""),
 ]
