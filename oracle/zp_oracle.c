@@ -558,7 +558,8 @@ int zpo_decode_attn(const uint16_t *q, const uint16_t *kpool, const uint16_t *vp
  *
  * Checked before anything changes (all or nothing): rows in range and
  * distinct, 0 <= p < stride*b, p < n_max*b when n_max > 0, the tail entry a
- * valid block (or negative at slot 0) with refcount >= 1 -> INVALID_ARG; the
+ * valid block (or negative at slot 0) with at least as many references as
+ * rows of this call write into it -> INVALID_ARG; the
  * free stack long enough -> OUT_OF_BLOCKS; a popped id in range with
  * refcount 0, free_count within [0, capacity] -> DEVICE_CHECK.
  * kpool/vpool: L pools [num_blocks][Hkv][b][d], modified in place. */
@@ -585,6 +586,15 @@ int zpo_append_slots(int L, int Hkv, int d, int b, int num_blocks, uint16_t *con
             return ZPO_ERR_INVALID_ARG;
         int32_t blk = tables[(size_t)row * stride + p / b];
         if (blk >= num_blocks || (blk < 0 && p % b != 0) || (blk >= 0 && refcount[blk] < 1))
+            return ZPO_ERR_INVALID_ARG;
+        /* every writer of a block holds one of its references */
+        int writers = 1;
+        for (int r2 = 0; r2 < r && blk >= 0; ++r2) {
+            int row2 = req_idx ? req_idx[r2] : r2;
+            if (tables[(size_t)row2 * stride + lengths[row2] / b] == blk)
+                ++writers;
+        }
+        if (blk >= 0 && writers > refcount[blk])
             return ZPO_ERR_INVALID_ARG;
     }
 

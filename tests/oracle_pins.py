@@ -739,6 +739,7 @@ def pin_append_errors(orc):
     assert run(tables=[[0, 1, -1], [0, -1, -1]], rc=[2, 1, 0, 0, 0, 0]) == -1  # partial, no block
     assert run(req=[1, 1]) == -1              # duplicate row
     assert run(rc=[2, 0, 1, 0, 0, 0]) == -1   # a tail block with no reference
+    assert run(tables=[[0, 1, -1], [0, 1, -1]], rc=[2, 1, 0, 0, 0, 0]) == -1  # 2 writers, 1 ref
     # two new blocks needed (row 0's tail 1 is shared with nothing; make it shared)
     t = [[0, 1, -1], [0, 1, -1]]
     assert run(tables=t, rc=[2, 2, 0, 0, 0, 0], lengths=[4, 5], fc=0) == -3
