@@ -70,6 +70,8 @@ struct zp_cache {
     int max_requests = 0, max_blocks = 0;
     int num_sms = 0;
     int32_t gen = 0;
+    int32_t ap_gen = 0;
+    std::vector<void *> kpools, vpools;  // host copies of the pool pointers
     void *base = nullptr;
     Workspace ws{};
 };
@@ -149,6 +151,12 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
     const size_t o_last = A.take(4 * static_cast<size_t>(D.num_blocks));
     const size_t o_rowmark = A.take(4 * static_cast<size_t>(D.max_requests));
     const size_t o_part = A.take(4 * part);
+    const size_t o_ap_call = A.take(4);
+    const size_t o_ap_cnt = A.take(16);
+    const size_t o_ap_rowmark = A.take(4 * static_cast<size_t>(D.max_requests));
+    const size_t o_ap_occ = A.take(4 * static_cast<size_t>(D.num_blocks));
+    const size_t o_ap_last = A.take(4 * static_cast<size_t>(D.num_blocks));
+    const size_t o_ap_plan = A.take(16 * static_cast<size_t>(D.max_requests));
     const size_t total = A.take(0);
 
     if (cudaMalloc(&c->base, total) != cudaSuccess) {
@@ -172,6 +180,14 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
     ws.rowmark = reinterpret_cast<int32_t *>(b + o_rowmark);
     ws.dec_part = reinterpret_cast<float *>(b + o_part);
     ws.dec_part_floats = part;
+    ws.ap_call = reinterpret_cast<int32_t *>(b + o_ap_call);
+    ws.ap_counters = reinterpret_cast<int32_t *>(b + o_ap_cnt);
+    ws.ap_rowmark = reinterpret_cast<int32_t *>(b + o_ap_rowmark);
+    ws.ap_occ = reinterpret_cast<int32_t *>(b + o_ap_occ);
+    ws.ap_last = reinterpret_cast<int32_t *>(b + o_ap_last);
+    ws.ap_plan = reinterpret_cast<int4 *>(b + o_ap_plan);
+    c->kpools.assign(D.k_pools, D.k_pools + D.num_layers);
+    c->vpools.assign(D.v_pools, D.v_pools + D.num_layers);
 
     std::vector<CUtensorMap> kmaps(D.num_layers), vmaps(D.num_layers);
     bool ok = true;
@@ -181,6 +197,7 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
     }
     ok = ok && cudaMemset(c->base, 0, o_kmaps) == cudaSuccess &&
          cudaMemset(b + o_rowmark, 0, 4 * static_cast<size_t>(D.max_requests)) == cudaSuccess &&
+         cudaMemset(b + o_ap_call, 0, o_ap_occ - o_ap_call) == cudaSuccess &&
          cudaMemcpy(ws.kmaps, kmaps.data(), sizeof(CUtensorMap) * D.num_layers,
                     cudaMemcpyHostToDevice) == cudaSuccess &&
          cudaMemcpy(ws.vmaps, vmaps.data(), sizeof(CUtensorMap) * D.num_layers,
@@ -359,6 +376,90 @@ zp_status zp_paged_decode_attn(zp_cache *c, int32_t layer, const void *q,
     if (zp::launch_decode(da, c->d, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ZP_ERR_CUDA;
     return ZP_OK;
+}
+
+zp_status zp_append_slots(zp_cache *c, int32_t *block_tables, int32_t bt_stride,
+                          int32_t num_rows, int32_t *lengths, const int32_t *req_idx, int32_t R,
+                          int32_t n_max, const zp_block_pool *pool, void *stream,
+                          int32_t *trigger_rows, int32_t *trigger_count)
+{
+    if (!c || !block_tables || !lengths || !pool || !pool->free_ids || !pool->free_count ||
+        !pool->refcount)
+        return ZP_ERR_INVALID_ARG;
+    if (R < 0 || num_rows < 1 || num_rows > c->max_requests || R > num_rows || bt_stride < 1 ||
+        n_max < 0 || pool->capacity < 1)
+        return ZP_ERR_INVALID_ARG;
+    if (!aligned(trigger_rows, 4) || !aligned(trigger_count, 4))
+        return ZP_ERR_INVALID_ARG;
+    if (static_cast<long long>(bt_stride) * c->b >= (1ll << 31) ||
+        static_cast<long long>(n_max) * c->b >= (1ll << 31))
+        return ZP_ERR_UNSUPPORTED;
+    if (!on_device(c))
+        return ZP_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (R == 0) {
+        if (trigger_count && cudaMemsetAsync(trigger_count, 0, 4, s) != cudaSuccess)
+            return ZP_ERR_CUDA;
+        return ZP_OK;
+    }
+    c->ap_gen = c->ap_gen >= 0x7ffffff0 ? 1 : c->ap_gen + 1;
+    zp::AppendArgs a{};
+    a.tables = block_tables;
+    a.stride = bt_stride;
+    a.num_rows = num_rows;
+    a.lengths = lengths;
+    a.req_idx = req_idx;
+    a.R = R;
+    a.n_max = n_max;
+    a.num_blocks = c->num_blocks;
+    a.L = c->L;
+    a.Hkv = c->Hkv;
+    a.d = c->d;
+    a.refcount = pool->refcount;
+    a.free_ids = pool->free_ids;
+    a.free_count = pool->free_count;
+    a.capacity = pool->capacity;
+    a.gen = c->ap_gen;
+    a.trigger_rows = trigger_rows;
+    a.trigger_count = trigger_count;
+    a.ws = c->ws;
+    return zp::launch_append_slots(a, s) == cudaSuccess ? ZP_OK : ZP_ERR_CUDA;
+}
+
+zp_status zp_append_kv(zp_cache *c, int32_t layer, const void *k_new, const void *v_new,
+                       const int32_t *block_tables, int32_t bt_stride, int32_t num_rows,
+                       const int32_t *lengths, const int32_t *req_idx, int32_t R, void *stream)
+{
+    if (!c || !k_new || !v_new || !block_tables || !lengths)
+        return ZP_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= c->L || R < 0 || R > c->max_requests || num_rows < 1 ||
+        bt_stride < 1)
+        return ZP_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16))
+        return ZP_ERR_INVALID_ARG;
+    if (static_cast<long long>(bt_stride) * c->b >= (1ll << 31))
+        return ZP_ERR_UNSUPPORTED;
+    if (R == 0)
+        return ZP_OK;
+    if (!on_device(c))
+        return ZP_ERR_INVALID_ARG;
+    zp::AppendKvArgs a{};
+    a.kpool = static_cast<__nv_bfloat16 *>(c->kpools[layer]);
+    a.vpool = static_cast<__nv_bfloat16 *>(c->vpools[layer]);
+    a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    a.tables = block_tables;
+    a.stride = bt_stride;
+    a.num_rows = num_rows;
+    a.lengths = lengths;
+    a.req_idx = req_idx;
+    a.R = R;
+    a.Hkv = c->Hkv;
+    a.d = c->d;
+    a.num_blocks = c->num_blocks;
+    a.sticky = c->ws.sticky;
+    return zp::launch_append_kv(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ZP_OK
+                                                                                      : ZP_ERR_CUDA;
 }
 
 zp_status zp_cache_status(zp_cache *c, void *stream, int32_t *out_status)

@@ -30,49 +30,7 @@
 
 namespace zp {
 
-// ============================================================ block scans
-
-// Exclusive prefix sum over the threads of a CTA in thread order.  `scratch`
-// holds NW + 1 ints.  Returns the exclusive prefix; `total` gets the sum.
-template <int NT>
-__device__ __forceinline__ int block_excl_scan(int v, int *scratch, int &total)
-{
-    constexpr int NW = NT / 32;
-    const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o)
-            x += y;
-    }
-    if (lane == 31)
-        scratch[wi] = x;
-    __syncthreads();
-    if (wi == 0) {
-        int s = lane < NW ? scratch[lane] : 0;
-        int incl = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o)
-                incl += y;
-        }
-        if (lane < NW)
-            scratch[lane] = incl - s;
-        if (lane == NW - 1)
-            scratch[NW] = incl;
-    }
-    __syncthreads();
-    const int res = scratch[wi] + x - v;
-    total = scratch[NW];
-    __syncthreads();
-    return res;
-}
-
 // ================================================================== plan
-
-constexpr int kPlanThreads = 1024;
 
 __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
 {

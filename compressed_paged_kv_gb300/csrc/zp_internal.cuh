@@ -15,6 +15,7 @@ constexpr int kBlk = 16;            // tokens per block (the only supported size
 constexpr int kMaxRows = 64;        // window rows per unit: w * (Hq / Hkv)
 constexpr int kMaxCluster = 16;     // CTAs per unit in the compression kernel
 constexpr uint32_t kWaitSpins = 1u << 22;  // bound on every mbarrier wait
+constexpr int kPlanThreads = 1024;  // the one-CTA bookkeeping kernels
 
 // ----------------------------------------------------------------- workspace
 // Device memory the handle owns (allocated once in zp_cache_create).
@@ -33,6 +34,13 @@ struct Workspace {
     int32_t *rowmark;    // [max_requests] generation stamps (duplicate-row check)
     float *dec_part;     // decode split partials
     size_t dec_part_floats;
+    // slot reservation (zp_append_slots) keeps its own scratch
+    int32_t *ap_call;     // [1]  status of the reservation call in flight
+    int32_t *ap_counters; // [4]  pops, triggers, free count after the pops
+    int32_t *ap_rowmark;  // [max_requests] generation stamps
+    int32_t *ap_occ;      // [num_blocks] writers of a block in this call
+    int32_t *ap_last;     // [num_blocks] last writer of a block in this call
+    int4 *ap_plan;        // [max_requests] tail block, fresh block, rows to copy, trigger slot
 };
 
 // ------------------------------------------------------------ launch args
@@ -97,7 +105,36 @@ struct DecodeArgs {
     int32_t *sticky;
 };
 
+struct AppendArgs {
+    int32_t *tables;
+    int32_t stride, num_rows;
+    int32_t *lengths;
+    const int32_t *req_idx;
+    int32_t R, n_max, num_blocks, L, Hkv, d;
+    int32_t *refcount;
+    const int32_t *free_ids;
+    int32_t *free_count;
+    int32_t capacity;
+    int32_t gen;
+    int32_t *trigger_rows;   // nullable
+    int32_t *trigger_count;  // nullable
+    Workspace ws;
+};
+
+struct AppendKvArgs {
+    __nv_bfloat16 *kpool, *vpool;
+    const __nv_bfloat16 *k_new, *v_new;
+    const int32_t *tables;
+    int32_t stride, num_rows;
+    const int32_t *lengths;
+    const int32_t *req_idx;
+    int32_t R, Hkv, d, num_blocks;
+    int32_t *sticky;
+};
+
 // Launchers (defined next to their kernels).
+cudaError_t launch_append_slots(const AppendArgs &a, cudaStream_t s);
+cudaError_t launch_append_kv(const AppendKvArgs &a, cudaStream_t s);
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s);
 // CTAs per unit of the fused compression kernel for T tokens (0: unsupported).
@@ -118,6 +155,45 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
 __device__ __forceinline__ void set_error(int32_t *word, int32_t code)
 {
     atomicCAS(word, 0, code);
+}
+
+// block scan ----------------------------------------------------------------
+// Exclusive prefix sum over the threads of a CTA in thread order.  `scratch`
+// holds NW + 1 ints.  Returns the exclusive prefix; `total` gets the sum.
+template <int NT>
+__device__ __forceinline__ int block_excl_scan(int v, int *scratch, int &total)
+{
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x += y;
+    }
+    if (lane == 31)
+        scratch[wi] = x;
+    __syncthreads();
+    if (wi == 0) {
+        int s = lane < NW ? scratch[lane] : 0;
+        int incl = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        if (lane < NW)
+            scratch[lane] = incl - s;
+        if (lane == NW - 1)
+            scratch[NW] = incl;
+    }
+    __syncthreads();
+    const int res = scratch[wi] + x - v;
+    total = scratch[NW];
+    __syncthreads();
+    return res;
 }
 
 // mbarrier ------------------------------------------------------------------

@@ -295,6 +295,57 @@ def build_cache(wl: Workload, device="cpu", seed=None, with_decode_q=True) -> Ca
         compress_rows=compress_rows.to(**i32), decode_rows=decode_rows.to(**i32))
 
 
+def fork_cache(seed: int, R: int, n_max: int, L: int = 2, Hkv: int = 2, d: int = 128,
+               b: int = 16, spare: int = 64, len_lo: int = 0, max_fan: int = 3,
+               reserve_prob: float = 0.4, device="cpu") -> dict:
+    """A decode-time cache with parallel samples of shared prompts.
+
+    Rows come in groups of 1..max_fan samples that share every block of one
+    prompt (its last block possibly partial, so refcount = group size);
+    lengths are uniform in [len_lo, n_max*b); a row whose length is a
+    multiple of b may already hold its next, empty block (as zp_compress
+    leaves it); table entries beyond a row's blocks are -1.  Physical ids are
+    a seeded permutation, the rest of the pool is the free stack.  K/V pools
+    [num_blocks][Hkv][b][d] are N(0,1) rounded to bf16.
+
+    Returns dict(tables, lengths, rc, free, nfree: numpy int32 / int;
+    k_pools, v_pools: lists of L bf16 tensors on `device`; plus the sizes).
+    """
+    import numpy as np
+    g = np.random.default_rng(seed)
+    num_blocks = R * n_max + spare
+    perm = g.permutation(num_blocks).astype(np.int32)
+    tables = np.full((R, n_max), -1, dtype=np.int32)
+    lengths = np.zeros(R, dtype=np.int32)
+    nxt = 0
+    r = 0
+    while r < R:
+        fan = min(int(g.integers(1, max_fan + 1)), R - r)
+        length = int(g.integers(len_lo, n_max * b))
+        nblk = -(-length // b)
+        tables[r:r + fan, :nblk] = perm[nxt:nxt + nblk]
+        lengths[r:r + fan] = length
+        nxt += nblk
+        r += fan
+    for r in range(R):
+        p = int(lengths[r])
+        if p % b == 0 and p // b < n_max and g.random() < reserve_prob:
+            tables[r, p // b] = perm[nxt]
+            nxt += 1
+    rc = np.zeros(num_blocks, dtype=np.int32)
+    for x in tables.reshape(-1):
+        if x >= 0:
+            rc[x] += 1
+    free = np.full(num_blocks, -1, dtype=np.int32)
+    nfree = num_blocks - nxt
+    free[:nfree] = perm[nxt:]
+    shape = (num_blocks, Hkv, b, d)
+    k_pools = [_normal(shape, device, derive_seed(seed, 1, l)).to(torch.bfloat16) for l in range(L)]
+    v_pools = [_normal(shape, device, derive_seed(seed, 2, l)).to(torch.bfloat16) for l in range(L)]
+    return dict(tables=tables, lengths=lengths, rc=rc, free=free, nfree=nfree, k_pools=k_pools,
+                v_pools=v_pools, num_blocks=num_blocks, b=b, n_max=n_max, L=L, Hkv=Hkv, d=d)
+
+
 def bf16_bits(t: torch.Tensor):
     """Raw uint16 bit patterns of a bf16 tensor, as a host numpy array."""
     import numpy as np

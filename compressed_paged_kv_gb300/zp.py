@@ -4,8 +4,8 @@ kernels.  There is no fallback: if the library is missing or fails to load,
 every call raises.
 
 The functions keep the C names (``zp_cache_create``, ``zp_compress``,
-``zp_paged_decode_attn``, ``zp_cache_status``, ``zp_cache_destroy``,
-``zp_status_string``) and take raw integers (device pointers, a cudaStream_t
+``zp_paged_decode_attn``, ``zp_append_slots``, ``zp_append_kv``,
+``zp_cache_status``, ``zp_cache_destroy``, ``zp_status_string``) and take raw integers (device pointers, a cudaStream_t
 as an int).  ``Cache`` wraps them for torch tensors: it reads ``data_ptr()``
 and the current stream, and keeps the pool tensors alive.
 """
@@ -76,6 +76,11 @@ def lib():
         L.zp_paged_decode_attn_noalloc.argtypes = [P, P, I32, I32, I32, I32, P, P, I32, I32, P,
                                                    P, I32, ctypes.c_float, P, P, P]
         L.zp_paged_decode_attn_noalloc.restype = I32
+        L.zp_append_slots.argtypes = [P, P, I32, I32, P, P, I32, I32,
+                                      ctypes.POINTER(zp_block_pool), P, P, P]
+        L.zp_append_slots.restype = I32
+        L.zp_append_kv.argtypes = [P, I32, P, P, P, I32, I32, P, P, I32, P]
+        L.zp_append_kv.restype = I32
         L.zp_cache_status.argtypes = [P, P, ctypes.POINTER(I32)]
         L.zp_cache_status.restype = I32
         L.zp_status_string.argtypes = [I32]
@@ -131,6 +136,20 @@ def zp_paged_decode_attn_noalloc(k_pool, v_pool, num_blocks, num_kv_heads, num_q
         P(k_pool), P(v_pool), num_blocks, num_kv_heads, num_q_heads, head_dim, P(q),
         P(block_tables), bt_stride, num_rows, P(lengths), P(req_idx or None), R, float(scale),
         P(out), P(status or None), P(stream or None))
+
+
+def zp_append_slots(handle, block_tables, bt_stride, num_rows, lengths, req_idx, R, n_max,
+                    pool: zp_block_pool, stream, trigger_rows=0, trigger_count=0) -> int:
+    return lib().zp_append_slots(P(handle), P(block_tables), bt_stride, num_rows, P(lengths),
+                                 P(req_idx or None), R, n_max, ctypes.byref(pool),
+                                 P(stream or None), P(trigger_rows or None),
+                                 P(trigger_count or None))
+
+
+def zp_append_kv(handle, layer, k_new, v_new, block_tables, bt_stride, num_rows, lengths,
+                 req_idx, R, stream) -> int:
+    return lib().zp_append_kv(P(handle), layer, P(k_new), P(v_new), P(block_tables), bt_stride,
+                              num_rows, P(lengths), P(req_idx or None), R, P(stream or None))
 
 
 def zp_cache_status(handle, stream) -> tuple[int, int]:
@@ -204,6 +223,29 @@ class Cache:
                                   out.data_ptr(), _stream(stream))
         if check and st != OK:
             raise ZpError(st, "zp_paged_decode_attn")
+        return st
+
+    def append_slots(self, block_tables, lengths, n_max, free_ids, free_count, refcount,
+                     req_idx=None, R=None, trigger_rows=None, trigger_count=None, stream=None,
+                     check=True):
+        pool = zp_block_pool(free_ids.data_ptr(), free_count.data_ptr(), refcount.data_ptr(),
+                             free_ids.numel())
+        if R is None:
+            R = req_idx.numel() if req_idx is not None else block_tables.shape[0]
+        st = zp_append_slots(self.handle, block_tables.data_ptr(), block_tables.shape[1],
+                             block_tables.shape[0], lengths.data_ptr(), _ptr(req_idx), R, n_max,
+                             pool, _stream(stream), _ptr(trigger_rows), _ptr(trigger_count))
+        if check and st != OK:
+            raise ZpError(st, "zp_append_slots")
+        return st
+
+    def append_kv(self, layer, k_new, v_new, block_tables, lengths, req_idx=None, stream=None,
+                  check=True):
+        st = zp_append_kv(self.handle, layer, k_new.data_ptr(), v_new.data_ptr(),
+                          block_tables.data_ptr(), block_tables.shape[1], block_tables.shape[0],
+                          lengths.data_ptr(), _ptr(req_idx), k_new.shape[0], _stream(stream))
+        if check and st != OK:
+            raise ZpError(st, "zp_append_kv")
         return st
 
     def status(self, stream=None) -> int:

@@ -22,9 +22,12 @@
  *    length or block id read from device memory, an empty free stack) are
  *    recorded in the handle's sticky status word, and every later kernel of
  *    the same call skips its writes; read the word with zp_cache_status.
- *  - A handle serves at most one zp_compress and one zp_paged_decode_attn in
- *    flight at a time (they may run concurrently on two streams when they
- *    touch disjoint requests).  More concurrency needs more handles.
+ *  - A handle serves at most one call of each entry point in flight at a
+ *    time.  zp_compress may run concurrently with zp_paged_decode_attn and
+ *    zp_append_kv on another stream when they touch disjoint requests.
+ *    zp_compress and zp_append_slots both change the free stack and
+ *    refcounts: order them (one stream, or events).  More concurrency needs
+ *    more handles.
  *
  * KV pool layout (one K pool and one V pool per layer, caller-owned):
  *     pool[num_blocks][num_kv_heads][block_size][head_dim]   bf16, contiguous
@@ -197,6 +200,63 @@ zp_status zp_paged_decode_attn_noalloc(const void *k_pool, const void *v_pool, i
                                        int32_t num_rows, const int32_t *lengths,
                                        const int32_t *req_idx, int32_t R, float scale, void *out,
                                        int32_t *status, void *stream);
+
+/* Reserves the slot of each listed request's next decode token, request
+ * after request in list order ("Paged KV cache and continuous batching for
+ * LLMs", "How it works": a block is taken only when the previous ones are
+ * full; a write into a shared block first copies it, block-level
+ * copy-on-write), and lists the requests that become due for compression
+ * (Dutch summary "Methodologie" §1: N_max blocks held and the last one full).
+ * For request i (row = req_idx[i], or i) with p = lengths[row], the new
+ * token goes to block entry e = p / 16, slot p % 16:
+ *   - block_tables[row][e] < 0 (allowed only at slot 0): a fresh block is
+ *     popped and becomes the entry;
+ *   - else, if that block's refcount, as updated by the requests before this
+ *     one, is > 1: a fresh block is popped, slots 0 .. p%16 - 1 of every
+ *     layer and kv head (K and V) are copied into it, it becomes the entry,
+ *     and the original loses one reference;
+ *   - else the block is written in place (nothing to do here).
+ * Popped blocks come from the top of the free stack, in list order, and get
+ * refcount 1.  Then lengths[row] = p + 1, and when n_max > 0 and p + 1 ==
+ * n_max * 16 the row is listed in trigger_rows (list order).  A table entry
+ * beyond a row's filled blocks must be < 0 unless it holds a block already
+ * reserved for the row (the empty last block zp_compress leaves).
+ *
+ *  block_tables  device int32 [num_rows][bt_stride], in/out
+ *  lengths       device int32 [num_rows], in/out: 0 <= p < bt_stride * 16,
+ *                and p < n_max * 16 when n_max > 0 (a full request is
+ *                compressed first)
+ *  req_idx       device int32 [R] distinct rows, or NULL for rows 0..R-1
+ *  n_max         blocks per request at compression, or 0 for no limit
+ *  pool          free stack + refcounts, updated in place
+ *  trigger_rows  NULL or device int32 [R]: rows that reached n_max * 16
+ *  trigger_count NULL or device int32 [1]: how many (0 after an error)
+ * All-or-nothing: a row out of range or repeated, a length out of range, a
+ * tail entry out of range (or < 0 at slot > 0), a tail block with fewer
+ * references than rows of this call writing it -> ZP_ERR_INVALID_ARG; too few
+ * free blocks -> ZP_ERR_OUT_OF_BLOCKS; a popped id out of range or with a
+ * nonzero refcount -> ZP_ERR_DEVICE_CHECK; all recorded in the sticky status,
+ * with nothing written.  R == 0 only zeroes *trigger_count. */
+zp_status zp_append_slots(zp_cache *cache, int32_t *block_tables, int32_t bt_stride,
+                          int32_t num_rows, int32_t *lengths, const int32_t *req_idx, int32_t R,
+                          int32_t n_max, const zp_block_pool *pool, void *stream,
+                          int32_t *trigger_rows, int32_t *trigger_count);
+
+/* Writes one layer's new-token keys and values into the slots zp_append_slots
+ * reserved ("Paged KV cache and continuous batching for LLMs", "How it
+ * works"): for request i (row = req_idx[i], or i), token p = lengths[row] - 1
+ * in block block_tables[row][p / 16], slot p % 16, gets k_new[i][h] and
+ * v_new[i][h] for every kv head h.  Call it for each layer after
+ * zp_append_slots, before that layer's zp_paged_decode_attn.
+ *
+ *  layer         0 <= layer < L
+ *  k_new, v_new  device bf16 [R][num_kv_heads][head_dim], 16-byte aligned
+ *  block_tables, lengths, req_idx as after zp_append_slots (read only)
+ * A row, length or block id out of range is recorded as ZP_ERR_DEVICE_CHECK
+ * in the sticky status and that row is skipped. */
+zp_status zp_append_kv(zp_cache *cache, int32_t layer, const void *k_new, const void *v_new,
+                       const int32_t *block_tables, int32_t bt_stride, int32_t num_rows,
+                       const int32_t *lengths, const int32_t *req_idx, int32_t R, void *stream);
 
 /* Synchronises `stream`, returns the handle's sticky device status in
  * *out_status (ZP_OK or the first device-detected error since the last

@@ -22,6 +22,8 @@ import os
 import numpy as np
 import torch
 
+from compressed_paged_kv_gb300 import workloads as W
+
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
@@ -617,42 +619,13 @@ def pin_append_fork_handworked(orc):
 
 
 def _fork_cache(seed, R=10, b=4, nmax=5, L=2, Hkv=2, d=4, spare=40):
-    """A random cache with samples that share their prompt blocks (a partial
-    tail included), some full tails and some reserved (allocated, empty) tail
-    blocks.  Table entries beyond a row's blocks are -1."""
-    g = rng(seed)
-    num_blocks = R * nmax + spare
-    perm = g.permutation(num_blocks).astype(np.int32)
-    tables = np.full((R, nmax + 1), -1, dtype=np.int32)
-    lengths = np.zeros(R, dtype=np.int32)
-    nxt = 0
-    r = 0
-    while r < R:
-        fan = min(int(g.integers(1, 4)), R - r)      # samples of one prompt
-        length = int(g.integers(0, nmax * b))
-        nblk = -(-length // b)
-        blocks = perm[nxt:nxt + nblk]
-        nxt += nblk
-        for k in range(fan):
-            tables[r + k, :nblk] = blocks
-            lengths[r + k] = length
-        r += fan
-    for r in range(R):                                 # some rows hold a reserved empty block
-        p = int(lengths[r])
-        if p % b == 0 and p // b < nmax and g.random() < 0.4:
-            tables[r, p // b] = perm[nxt]
-            nxt += 1
-    rc = np.zeros(num_blocks, dtype=np.int32)
-    for x in tables.reshape(-1):
-        if x >= 0:
-            rc[x] += 1
-    free = np.full(num_blocks, -1, dtype=np.int32)
-    nfree = num_blocks - nxt
-    free[:nfree] = perm[nxt:]
-    kp = [bf16(g.standard_normal((num_blocks, Hkv, b, d))) for _ in range(L)]
-    vp = [bf16(g.standard_normal((num_blocks, Hkv, b, d))) for _ in range(L)]
-    return dict(tables=tables, lengths=lengths, rc=rc, free=free, nfree=nfree, kp=kp, vp=vp,
-                b=b, nmax=nmax, L=L, Hkv=Hkv, num_blocks=num_blocks)
+    """A small forked decode-time cache from the shared input generator, with
+    the pools as bf16 bit patterns."""
+    c = W.fork_cache(seed, R, nmax, L=L, Hkv=Hkv, d=d, b=b, spare=spare)
+    c["kp"] = [W.bf16_bits(k).copy() for k in c.pop("k_pools")]
+    c["vp"] = [W.bf16_bits(v).copy() for v in c.pop("v_pools")]
+    c["nmax"] = c.pop("n_max")
+    return c
 
 
 def pin_append_invariants(orc):
