@@ -68,12 +68,20 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the files the compression kernel is compiled from: the recorded DRAM
+# traffic stays valid while none of them changes
+COMPRESS_KERNEL_SOURCES = ["zp_compress_stream.cuh", "zp_internal.cuh", "zp_compress_d64.cu",
+                           "zp_compress_d128.cu"]
+
+
 def kernel_source_digest():
     from compressed_paged_kv_gb300 import _build
     h = hashlib.sha256()
-    for name in sorted(os.listdir(_build.CSRC)):
-        with open(os.path.join(_build.CSRC, name), "rb") as f:
-            h.update(name.encode())
+    paths = [os.path.join(_build.CSRC, n) for n in COMPRESS_KERNEL_SOURCES]
+    paths.append(os.path.join(os.path.dirname(os.path.abspath(__file__)), "include", "zp.h"))
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -183,9 +191,10 @@ def reduce_max(values, world: int, device=None):
 # ------------------------------------------------------------------ GPU arm
 
 def run_mixed(args, world, rank, local):
-    """The mixed decode step: paged decode attention of the decoding requests
-    (every layer) on a high-priority stream while the requests that reached
-    N_max compress on a second stream; timed overlapped and serialised."""
+    """The mixed decode step: the decoding requests reserve their next slot,
+    then, on a high-priority stream, every layer writes their new K/V rows and
+    runs paged decode attention, while the requests that reached N_max
+    compress on a second stream; timed overlapped and serialised."""
     import torch
     import torch.distributed as dist
 
@@ -209,6 +218,13 @@ def run_mixed(args, world, rank, local):
     drows = st.decode_rows
     q = [st.decode_q[l][drows.long()].contiguous() for l in range(wl.L)]
     out = [torch.empty_like(x) for x in q]
+    # the new token's K/V rows of every decoding request (seeded, per layer)
+    gkv = torch.Generator(device=dev)
+    gkv.manual_seed(replica_seed(wl, rank) + 7)
+    k_new = [torch.randn(drows.numel(), wl.Hkv, wl.d, generator=gkv, device=dev)
+             .to(torch.bfloat16) for _ in range(wl.L)]
+    v_new = [torch.randn(drows.numel(), wl.Hkv, wl.d, generator=gkv, device=dev)
+             .to(torch.bfloat16) for _ in range(wl.L)]
     s_dec = torch.cuda.Stream(device=dev, priority=-1)
     s_cmp = torch.cuda.Stream(device=dev)
     main = torch.cuda.current_stream()
@@ -217,8 +233,14 @@ def run_mixed(args, world, rank, local):
         cache.compress(st.block_tables, st.lengths, st.window_q, wl.N, wl.w, wl.lam, st.free_ids,
                        st.free_count, st.refcount, req_idx=st.compress_rows, stream=stream)
 
+    def append_slots(stream):
+        cache.append_slots(st.block_tables, st.lengths, wl.N, st.free_ids, st.free_count,
+                           st.refcount, req_idx=drows, stream=stream)
+
     def decode(stream):
         for l in range(wl.L):
+            cache.append_kv(l, k_new[l], v_new[l], st.block_tables, st.lengths, req_idx=drows,
+                            stream=stream)
             cache.decode(l, q[l], st.block_tables, st.lengths, scale, out[l], req_idx=drows,
                          stream=stream)
 
@@ -233,11 +255,15 @@ def run_mixed(args, world, rank, local):
         for p, saved in zip(st.k_pools + st.v_pools, pristine_slabs):
             p.index_copy_(0, cblk, saved)
         flush.zero_()
-        e0, ed, ec, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+        e0, ea, ed, ec, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(5))
         e0.record(main)
+        # slot reservation and compression both update the free stack and the
+        # refcounts: the reservation goes first, then the two streams fork
+        append_slots(main)
+        ea.record(main)
         if overlap:
-            s_dec.wait_event(e0)
-            s_cmp.wait_event(e0)
+            s_dec.wait_event(ea)
+            s_cmp.wait_event(ea)
             decode(s_dec)
             ed.record(s_dec)
             compress(s_cmp)
@@ -250,7 +276,7 @@ def run_mixed(args, world, rank, local):
             compress(main)
             ec.record(main)
         e1.record(main)
-        return e0, ed, ec, e1
+        return e0, ea, ed, ec, e1
 
     for _ in range(args.warmup):
         step(True)
@@ -263,35 +289,42 @@ def run_mixed(args, world, rank, local):
         res_s.append(step(False))
     torch.cuda.synchronize()
     assert cache.status() == zp.OK
-    ov = sum(e0.elapsed_time(e1) for e0, _, _, e1 in res_o) / K
-    se = sum(e0.elapsed_time(e1) for e0, _, _, e1 in res_s) / K
-    dec_ms = sum(e0.elapsed_time(ed) for e0, ed, _, _ in res_s) / K
-    cmp_ms = sum(ed.elapsed_time(ec) for _, ed, ec, _ in res_s) / K
-    ov, se, dec_ms, cmp_ms = reduce_max([ov, se, dec_ms, cmp_ms], world, dev)
+    ov = sum(e0.elapsed_time(e1) for e0, _, _, _, e1 in res_o) / K
+    se = sum(e0.elapsed_time(e1) for e0, _, _, _, e1 in res_s) / K
+    slot_ms = sum(e0.elapsed_time(ea) for e0, ea, _, _, _ in res_s) / K
+    dec_ms = sum(ea.elapsed_time(ed) for _, ea, ed, _, _ in res_s) / K
+    cmp_ms = sum(ed.elapsed_time(ec) for _, _, ed, ec, _ in res_s) / K
+    ov, se, slot_ms, dec_ms, cmp_ms = reduce_max([ov, se, slot_ms, dec_ms, cmp_ms], world, dev)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return None
     Rc = st.window_q.shape[1]
     row = wl.d * 2
-    dec_bytes = int(st.lengths[drows.long()].sum().item()) * wl.L * wl.Hkv * row * 2
+    # attention reads every cached K and V row, the new token included; the
+    # append reads and writes one K and one V row per (request, layer, kv head)
+    dec_len = int(pristine[1][drows.long()].sum().item()) + drows.numel()
+    dec_bytes = dec_len * wl.L * wl.Hkv * row * 2 + drows.numel() * wl.L * wl.Hkv * row * 4
     peak, peak_src = peaks()
     res = {
         "metric": METRIC, "value": world * Rc * wl.T / (ov * 1e-3), "unit": UNIT,
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ov,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; shapes of the named model, no weights)",
-        "config": {"workload": f"{wl.name}: L={wl.L} decode {drows.numel()} requests (lengths "
-                               f"{wl.mixed_len_lo}..{wl.T}) on a high-priority stream, "
+        "config": {"workload": f"{wl.name}: L={wl.L} decode step of {drows.numel()} requests "
+                               f"(lengths {wl.mixed_len_lo}..{wl.T - 1}: slot reservation, then "
+                               f"new K/V rows + attention per layer) on a high-priority stream, "
                                f"{Rc} requests at N_max={wl.N} compressing on a second stream",
                    "global_batch": world * wl.R, "seq_len": wl.T,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps"},
-        "overlap_ms": ov, "serial_ms": se, "decode_ms": dec_ms, "compress_ms": cmp_ms,
+        "overlap_ms": ov, "serial_ms": se, "slot_reservation_ms": slot_ms,
+        "decode_ms": dec_ms, "compress_ms": cmp_ms,
         "overlap_gain": se / ov, "decode_gbs": dec_bytes / (dec_ms * 1e-3) / 1e9,
         "decode_frac_of_measured": dec_bytes / (dec_ms * 1e-3) / 1e9 / peak,
         "compression_share_of_serial_step": cmp_ms / se,
-        "gpu_launches": 2 * K * (3 + wl.L * (1 if cache_splits_one(wl, drows.numel(), cache) else 2)),
+        "gpu_launches": 2 * K * (2 + 3 + wl.L * (
+            2 if cache_splits_one(wl, drows.numel(), cache) else 3)),
     }
     if world > 1:
         dist.destroy_process_group()

@@ -16,7 +16,7 @@ DeepSeek-R1-Distill-Llama-8B, KV budget 2048 tokens):
                prompt prefix (refcount 8); K AR(1) rho 0.9 + 1% heavy hitters
                (x8); V, Q N(0,1).
   long4k       36 layers, N_max 256, 128 requests, K AR(1) rho 0.95, V N(0,1).
-  mixed        32 layers, 512 requests, lengths uniform in [1024, 2048]; 51
+  mixed        32 layers, 512 requests, lengths uniform in [1024, 2048); 51
                of them forced to 2048 (they compress); the rest decode.
 
 All tensors are generated in fp32 from torch generators seeded per (tensor,
@@ -195,7 +195,10 @@ def build_cache(wl: Workload, device="cpu", seed=None, with_decode_q=True) -> Ca
     R = wl.R
     gcpu = _gen("cpu", derive_seed(master, TENSOR_LEN))
     if wl.mixed:
-        lengths = torch.randint(wl.mixed_len_lo, N * b + 1, (R,), generator=gcpu, dtype=torch.int64)
+        # decoding requests are never full (a full request is due for
+        # compression) unless the workload asks for full lengths only
+        hi = N * b if wl.mixed_len_lo < N * b else N * b + 1
+        lengths = torch.randint(wl.mixed_len_lo, hi, (R,), generator=gcpu, dtype=torch.int64)
         perm = torch.randperm(R, generator=gcpu)
         compress_rows = torch.sort(perm[:wl.mixed_compress]).values
         lengths[compress_rows] = N * b
@@ -216,7 +219,7 @@ def build_cache(wl: Workload, device="cpu", seed=None, with_decode_q=True) -> Ca
     num_blocks = used + wl.spare_blocks
     gperm = _gen("cpu", derive_seed(master, TENSOR_TABLE))
     phys = torch.randperm(num_blocks, generator=gperm).to(torch.int32)
-    tables = torch.zeros((R, N), dtype=torch.int32)
+    tables = torch.full((R, N), -1, dtype=torch.int32)  # -1: no block (yet)
     refcount = torch.zeros(num_blocks, dtype=torch.int32)
     nxt = 0
     for gi in range(n_groups):
