@@ -69,8 +69,6 @@ struct zp_cache {
     int L = 0, Hkv = 0, Hq = 0, d = 0, b = 0, num_blocks = 0;
     int max_requests = 0, max_blocks = 0;
     int num_sms = 0;
-    int32_t gen = 0;
-    int32_t ap_gen = 0;
     std::vector<void *> kpools, vpools;  // host copies of the pool pointers
     void *base = nullptr;
     Workspace ws{};
@@ -140,6 +138,7 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
     Alloc A;
     const size_t o_sticky = A.take(4);
     const size_t o_call = A.take(4);
+    const size_t o_gens = A.take(8);
     const size_t o_kmaps = A.take(sizeof(CUtensorMap) * D.num_layers, 128);
     const size_t o_vmaps = A.take(sizeof(CUtensorMap) * D.num_layers, 128);
     const size_t o_kp = A.take(sizeof(void *) * D.num_layers);
@@ -168,6 +167,7 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
     Workspace &ws = c->ws;
     ws.sticky = reinterpret_cast<int32_t *>(b + o_sticky);
     ws.call = reinterpret_cast<int32_t *>(b + o_call);
+    ws.gens = reinterpret_cast<int32_t *>(b + o_gens);
     ws.kmaps = reinterpret_cast<CUtensorMap *>(b + o_kmaps);
     ws.vmaps = reinterpret_cast<CUtensorMap *>(b + o_vmaps);
     ws.kpools = reinterpret_cast<void **>(b + o_kp);
@@ -263,7 +263,6 @@ zp_status zp_compress(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int
         return ZP_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    c->gen = c->gen >= 0x7ffffff0 ? 1 : c->gen + 1;
     zp::PlanArgs pa{};
     pa.tables = block_tables;
     pa.stride = bt_stride;
@@ -277,7 +276,6 @@ zp_status zp_compress(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int
     pa.free_ids = pool->free_ids;
     pa.free_count = pool->free_count;
     pa.capacity = pool->capacity;
-    pa.gen = c->gen;
     pa.ws = c->ws;
     if (zp::launch_plan(pa, s) != cudaSuccess)
         return ZP_ERR_CUDA;
@@ -402,7 +400,6 @@ zp_status zp_append_slots(zp_cache *c, int32_t *block_tables, int32_t bt_stride,
             return ZP_ERR_CUDA;
         return ZP_OK;
     }
-    c->ap_gen = c->ap_gen >= 0x7ffffff0 ? 1 : c->ap_gen + 1;
     zp::AppendArgs a{};
     a.tables = block_tables;
     a.stride = bt_stride;
@@ -419,7 +416,6 @@ zp_status zp_append_slots(zp_cache *c, int32_t *block_tables, int32_t bt_stride,
     a.free_ids = pool->free_ids;
     a.free_count = pool->free_count;
     a.capacity = pool->capacity;
-    a.gen = c->ap_gen;
     a.trigger_rows = trigger_rows;
     a.trigger_count = trigger_count;
     a.ws = c->ws;

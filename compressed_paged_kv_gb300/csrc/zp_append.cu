@@ -38,10 +38,13 @@ constexpr int kKvThreads = 128;
 __global__ void __launch_bounds__(kPlanThreads) zp_append_plan_kernel(const AppendArgs a)
 {
     __shared__ int s_err;
-    __shared__ int s_fc;
+    __shared__ int s_fc, s_gen;
     __shared__ int s_scan[kPlanThreads / 32 + 1];
     const int tid = threadIdx.x;
     if (tid == 0) {
+        const int g = a.ws.gens[1];
+        s_gen = g >= 0x7ffffff0 ? 1 : g + 1;
+        a.ws.gens[1] = s_gen;
         s_err = 0;
         s_fc = *a.free_count;
         if (s_fc < 0 || s_fc > a.capacity)
@@ -66,7 +69,7 @@ __global__ void __launch_bounds__(kPlanThreads) zp_append_plan_kernel(const Appe
             atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
             continue;
         }
-        if (atomicExch(&a.ws.ap_rowmark[row], a.gen) == a.gen)
+        if (atomicExch(&a.ws.ap_rowmark[row], s_gen) == s_gen)
             atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
         const int p = a.lengths[row];
         if (p < 0 || p >= a.stride * kBlk || (a.n_max > 0 && p >= a.n_max * kBlk)) {

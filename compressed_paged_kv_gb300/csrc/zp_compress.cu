@@ -35,10 +35,13 @@ namespace zp {
 __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
 {
     __shared__ int s_err;
-    __shared__ int s_fc;
+    __shared__ int s_fc, s_gen;
     __shared__ int s_scan[kPlanThreads / 32 + 1];
     const int tid = threadIdx.x;
     if (tid == 0) {
+        const int g = a.ws.gens[0];
+        s_gen = g >= 0x7ffffff0 ? 1 : g + 1;
+        a.ws.gens[0] = s_gen;
         s_err = 0;
         s_fc = *a.free_count;
         if (s_fc < 0 || s_fc > a.capacity)
@@ -54,7 +57,7 @@ __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
             atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
             continue;
         }
-        if (atomicExch(&a.ws.rowmark[row], a.gen) == a.gen)
+        if (atomicExch(&a.ws.rowmark[row], s_gen) == s_gen)
             atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
         if (a.lengths[row] != a.N * kBlk)
             atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);

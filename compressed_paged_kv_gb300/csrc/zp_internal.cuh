@@ -22,6 +22,9 @@ constexpr int kPlanThreads = 1024;  // the one-CTA bookkeeping kernels
 struct Workspace {
     int32_t *sticky;     // [1]  first device-detected error since last read
     int32_t *call;       // [1]  status of the compression call in flight
+    int32_t *gens;       // [2]  generation counters of the duplicate-row stamps
+                         //      (compression, reservation), advanced on the device so
+                         //      that a captured CUDA graph stamps afresh on every replay
     CUtensorMap *kmaps;  // [L]  K pool maps, 128B swizzle, box {64, 16}
     CUtensorMap *vmaps;  // [L]  V pool maps, same
     void **kpools;       // [L]  device copies of the pool pointers
@@ -54,7 +57,6 @@ struct PlanArgs {
     const int32_t *free_ids;
     const int32_t *free_count;
     int32_t capacity;
-    int32_t gen;
     Workspace ws;
 };
 
@@ -115,7 +117,6 @@ struct AppendArgs {
     const int32_t *free_ids;
     int32_t *free_count;
     int32_t capacity;
-    int32_t gen;
     int32_t *trigger_rows;   // nullable
     int32_t *trigger_count;  // nullable
     Workspace ws;

@@ -300,12 +300,12 @@ def build_cache(wl: Workload, device="cpu", seed=None, with_decode_q=True) -> Ca
 
 def fork_cache(seed: int, R: int, n_max: int, L: int = 2, Hkv: int = 2, d: int = 128,
                b: int = 16, spare: int = 64, len_lo: int = 0, max_fan: int = 3,
-               reserve_prob: float = 0.4, device="cpu") -> dict:
+               reserve_prob: float = 0.4, len_hi: int | None = None, device="cpu") -> dict:
     """A decode-time cache with parallel samples of shared prompts.
 
     Rows come in groups of 1..max_fan samples that share every block of one
     prompt (its last block possibly partial, so refcount = group size);
-    lengths are uniform in [len_lo, n_max*b); a row whose length is a
+    lengths are uniform in [len_lo, len_hi) (len_hi defaults to n_max*b); a row whose length is a
     multiple of b may already hold its next, empty block (as zp_compress
     leaves it); table entries beyond a row's blocks are -1.  Physical ids are
     a seeded permutation, the rest of the pool is the free stack.  K/V pools
@@ -324,7 +324,7 @@ def fork_cache(seed: int, R: int, n_max: int, L: int = 2, Hkv: int = 2, d: int =
     r = 0
     while r < R:
         fan = min(int(g.integers(1, max_fan + 1)), R - r)
-        length = int(g.integers(len_lo, n_max * b))
+        length = int(g.integers(len_lo, n_max * b if len_hi is None else len_hi))
         nblk = -(-length // b)
         tables[r:r + fan, :nblk] = perm[nxt:nxt + nblk]
         lengths[r:r + fan] = length
