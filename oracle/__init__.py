@@ -79,6 +79,13 @@ def _declare(lib):
     lib.zpo_compress.restype = I
     lib.zpo_decode_attn.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, D, P, P]
     lib.zpo_decode_attn.restype = I
+    lib.zpo_plan_prefill.argtypes = [P, I, P, P, I, I, I, I, I, P, P, I, P, P]
+    lib.zpo_plan_prefill.restype = I
+    lib.zpo_commit_prefill.argtypes = [P, I, P, P, I, I, I, P, P, I, P, I]
+    lib.zpo_commit_prefill.restype = I
+    lib.zpo_compress_prefill.argtypes = [I, I, I, I, I, I, P, P, P, P, P, I, P, P, I, I, P, I, I,
+                                         D, P, P, P, P, P, I]
+    lib.zpo_compress_prefill.restype = I
     lib.zpo_append_slots.argtypes = [I, I, I, I, I, P, P, P, I, I, P, P, I, I, P, P, P, I, P, P]
     lib.zpo_append_slots.restype = I
     lib.zpo_append_kv.argtypes = [I, I, I, I, P, P, P, I, I, P, P, I, P, P]
@@ -235,6 +242,50 @@ class Oracle:
                                    stride, _p(lengths), _p(req_idx), R, num_rows, _p(window_q),
                                    N, w, float(lam), _p(free_ids), ctypes.byref(fc),
                                    _p(refcount), _p(scores), _p(kept), int(nthreads))
+        return dict(status=st, kpools=kout, vpools=vout, tables=tables, lengths=lengths,
+                    free_ids=free_ids, free_count=fc.value, refcount=refcount, scores=scores,
+                    kept=kept)
+
+    def compress_prefill(self, kpools, vpools, tables, lengths, window_q, N, w, lam, free_ids,
+                         free_count, refcount, Hq, req_idx=None, want_scores=True,
+                         want_kept=True, nthreads=None):
+        """Compression at admission on host copies (lengths >= N*b).
+
+        Same inputs and dict as ``compress``; scores are [L][R][Hkv][stride*b]
+        with NaN where nothing is written (positions at and beyond a request's
+        length)."""
+        L = len(kpools)
+        num_blocks, Hkv, b, d = kpools[0].shape
+        kin = [_c(k, np.uint16) for k in kpools]
+        vin = [_c(v, np.uint16) for v in vpools]
+        kout = [k.copy() for k in kin]
+        vout = [v.copy() for v in vin]
+        tables = _c(tables, np.int32).copy()
+        lengths = _c(lengths, np.int32).copy()
+        free_ids = _c(free_ids, np.int32).copy()
+        refcount = _c(refcount, np.int32).copy()
+        window_q = _c(window_q, np.uint16)
+        num_rows, stride = tables.shape
+        if req_idx is not None:
+            req_idx = _c(req_idx, np.int32)
+            R = req_idx.shape[0]
+        else:
+            R = num_rows
+        scores = (np.full((L, R, Hkv, stride * b), np.nan, dtype=np.float64)
+                  if want_scores else None)
+        kept = np.zeros((L, R, Hkv, (N - 1) * b), dtype=np.int32) if want_kept else None
+        arr = ctypes.c_void_p * L
+        kp = arr(*[k.ctypes.data for k in kin])
+        vp = arr(*[v.ctypes.data for v in vin])
+        ko = arr(*[k.ctypes.data for k in kout])
+        vo = arr(*[v.ctypes.data for v in vout])
+        fc = ctypes.c_int32(int(free_count))
+        nthreads = nthreads or os.cpu_count() or 1
+        st = self.lib.zpo_compress_prefill(L, Hkv, Hq, d, b, num_blocks, kp, vp, ko, vo,
+                                           _p(tables), stride, _p(lengths), _p(req_idx), R,
+                                           num_rows, _p(window_q), N, w, float(lam),
+                                           _p(free_ids), ctypes.byref(fc), _p(refcount),
+                                           _p(scores), _p(kept), int(nthreads))
         return dict(status=st, kpools=kout, vpools=vout, tables=tables, lengths=lengths,
                     free_ids=free_ids, free_count=fc.value, refcount=refcount, scores=scores,
                     kept=kept)

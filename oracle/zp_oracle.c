@@ -29,6 +29,9 @@
  *   commit     [ZP-nl Methodologie §1, §3; PKV]: tables, lengths, refcounts,
  *              released blocks back to the free stack.
  *   decode     [PKV]: attention of one query per head over the block table.
+ *   prefill    [ZP-nl Methodologie §1, §3]: the same scoring, selection and
+ *              compaction for a request admitted with more than N*b tokens;
+ *              its excess blocks are released.
  *   append     [PKV; ZP-nl Methodologie §1]: the slot of each decoding request's
  *              next token (a new block only when the last one is full,
  *              copy-on-write of a shared block), the new token's K/V written
@@ -143,21 +146,24 @@ void zpo_importance(const uint16_t *K, const uint16_t *Q, int T, int d, int w, i
 /* ---------------------------------------------------------- redundancy */
 
 /* Lightning Redundancy Score [ZP-nl Methodologie §5; ZP-ko 방법론 E]: only the
- * b keys of the same block are compared, O(N*b^2) per unit.
- * red[j] = (1/(b-1)) * sum_{k in block(j), k != j} cos(K_j, K_k), where a
+ * keys of the same block are compared, O(N*b^2) per unit.
+ * red[j] = (1/(f-1)) * sum_{k in block(j), k != j} cos(K_j, K_k), where f is
+ * the number of filled slots of the block (b, except for a partial last block
+ * when T is not a multiple of b; a block with one key gives 0) and a
  * zero-norm key has cosine 0 with every key.  All T keys get a value; window
  * keys count as "other keys" of their block. */
 void zpo_redundancy(const uint16_t *K, int T, int d, int b, double *red)
 {
     double *norm = (double *)malloc(sizeof(double) * (size_t)b);
     for (int base = 0; base < T; base += b) {
-        for (int j = 0; j < b; ++j) {
+        int f = T - base < b ? T - base : b;
+        for (int j = 0; j < f; ++j) {
             const uint16_t *kj = K + (size_t)(base + j) * d;
             norm[j] = sqrt(dot_bf16(kj, kj, d));
         }
-        for (int j = 0; j < b; ++j) {
+        for (int j = 0; j < f; ++j) {
             double sum = 0.0;
-            for (int k = 0; k < b; ++k) {
+            for (int k = 0; k < f; ++k) {
                 if (k == j)
                     continue;
                 double c = 0.0;
@@ -166,7 +172,7 @@ void zpo_redundancy(const uint16_t *K, int T, int d, int b, double *red)
                         (norm[j] * norm[k]);
                 sum += c;
             }
-            red[base + j] = sum / (double)(b - 1);
+            red[base + j] = f > 1 ? sum / (double)(f - 1) : 0.0;
         }
     }
     free(norm);
@@ -339,8 +345,10 @@ typedef struct {
     double lambda;
     const uint16_t *window_q; /* [L][R][Hq][w][d] */
     const int32_t *dst_table;
-    double *scores_out; /* [L][R][Hkv][T] or NULL */
+    double *scores_out; /* [L][R][Hkv][score_stride] or NULL */
     int32_t *kept_out;  /* [L][R][Hkv][(N-1)b] or NULL */
+    const int32_t *unit_len; /* tokens of each request row (prefill) or NULL: T = N*b */
+    int score_stride;
     int next_unit;
     pthread_mutex_t mu;
 } compress_job;
@@ -357,7 +365,8 @@ static void compress_unit(compress_job *J, int unit)
     int r = unit / (J->Hkv * J->L);
     int row = J->req_idx ? J->req_idx[r] : r;
     int b = J->b, d = J->d, N = J->N, w = J->w;
-    int T = N * b, C = T - w, G = J->Hq / J->Hkv;
+    int T = J->unit_len ? J->unit_len[row] : N * b;
+    int C = T - w, G = J->Hq / J->Hkv;
     int n_keep = (N - 1) * b - w;
     const int32_t *src_row = J->tables + (size_t)row * J->stride;
     const int32_t *dst_row = J->dst_table + (size_t)r * N;
@@ -386,10 +395,11 @@ static void compress_unit(compress_job *J, int unit)
     }
     size_t u = ((size_t)l * J->R + r) * J->Hkv + h;
     if (J->scores_out) {
+        size_t so = u * (size_t)J->score_stride;
         for (int j = 0; j < C; ++j)
-            J->scores_out[u * T + j] = score[j];
+            J->scores_out[so + j] = score[j];
         for (int j = C; j < T; ++j)
-            J->scores_out[u * T + j] = INFINITY;
+            J->scores_out[so + j] = INFINITY;
     }
     if (J->kept_out)
         memcpy(J->kept_out + u * (size_t)(N - 1) * b, kept, sizeof(int32_t) * (size_t)(N - 1) * b);
@@ -414,6 +424,22 @@ static void *compress_worker(void *arg)
         compress_unit(J, u);
     }
     return NULL;
+}
+
+/* Runs compress_unit on every unit of J over `nthreads` threads. */
+static void run_units(compress_job *J, int nthreads)
+{
+    J->next_unit = 0;
+    pthread_mutex_init(&J->mu, NULL);
+    if (nthreads < 1)
+        nthreads = 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    for (int i = 0; i < nthreads; ++i)
+        pthread_create(&th[i], NULL, compress_worker, J);
+    for (int i = 0; i < nthreads; ++i)
+        pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J->mu);
 }
 
 /* Whole compression of R requests over all L layers and Hkv heads.
@@ -447,19 +473,135 @@ int zpo_compress(int L, int Hkv, int Hq, int d, int b, int num_blocks,
     J.tables = tables; J.stride = stride; J.req_idx = req_idx;
     J.R = R; J.N = N; J.w = w; J.lambda = lambda; J.window_q = window_q;
     J.dst_table = dst; J.scores_out = scores_out; J.kept_out = kept_out;
-    J.next_unit = 0;
-    pthread_mutex_init(&J.mu, NULL);
-    if (nthreads < 1)
-        nthreads = 1;
-    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
-    for (int i = 0; i < nthreads; ++i)
-        pthread_create(&th[i], NULL, compress_worker, &J);
-    for (int i = 0; i < nthreads; ++i)
-        pthread_join(th[i], NULL);
-    free(th);
-    pthread_mutex_destroy(&J.mu);
+    J.unit_len = NULL; J.score_stride = N * b;
+    run_units(&J, nthreads);
     *free_count = zpo_commit(tables, stride, lengths, req_idx, R, N, b, refcount, free_ids,
                              *free_count, dst, pops);
+    free(dst);
+    return ZPO_OK;
+}
+
+/* ------------------------------------------------------------- prefill */
+
+/* Destination blocks of a compression at admission [ZP-nl Methodologie §1,
+ * §3]: request r holds T_r = lengths[row] >= N*b tokens in blocks
+ * 0 .. ceil(T_r/b)-1.  Blocks 0 .. N-1 get destinations by the rule of
+ * zpo_plan (refcount 1 at call start: in place; > 1: a fresh target from the
+ * top of the free stack, in (request, block) order); blocks N .. are excess
+ * and will be released.  Checks: rows in range and distinct,
+ * N*b <= T_r <= stride*b, every block of the request valid with refcount >= 1.
+ * dst_table[r*N + p] receives the destination of (r, p < N). */
+int zpo_plan_prefill(const int32_t *tables, int stride, const int32_t *lengths,
+                     const int32_t *req_idx, int R, int num_rows, int N, int b, int num_blocks,
+                     const int32_t *refcount, const int32_t *free_ids, int free_count,
+                     int32_t *dst_table, int *n_pops)
+{
+    *n_pops = 0;
+    if (R < 0 || N < 2 || b < 2 || stride < N)
+        return ZPO_ERR_INVALID_ARG;
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        if (row < 0 || row >= num_rows)
+            return ZPO_ERR_INVALID_ARG;
+        for (int r2 = 0; r2 < r; ++r2)
+            if ((req_idx ? req_idx[r2] : r2) == row)
+                return ZPO_ERR_INVALID_ARG;
+        int T = lengths[row];
+        if (T < N * b || T > stride * b)
+            return ZPO_ERR_INVALID_ARG;
+        for (int p = 0; p < (T + b - 1) / b; ++p) {
+            int32_t blk = tables[(size_t)row * stride + p];
+            if (blk < 0 || blk >= num_blocks || refcount[blk] < 1)
+                return ZPO_ERR_INVALID_ARG;
+        }
+    }
+    int taken = 0;
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        for (int p = 0; p < N; ++p) {
+            int32_t src = tables[(size_t)row * stride + p];
+            int32_t target = src;
+            if (refcount[src] > 1) {
+                if (taken >= free_count)
+                    return ZPO_ERR_OUT_OF_BLOCKS;
+                target = free_ids[free_count - 1 - taken];
+                if (target < 0 || target >= num_blocks || refcount[target] != 0)
+                    return ZPO_ERR_DEVICE_CHECK;
+                ++taken;
+            }
+            dst_table[(size_t)r * N + p] = target;
+        }
+    }
+    *n_pops = taken;
+    return ZPO_OK;
+}
+
+/* Applies a prefill plan [ZP-nl Methodologie §1 "the excess blocks are
+ * released", §3; PKV reference counts]: one request after the other, blocks
+ * 0 .. N-1 as in zpo_commit, then every excess block N .. ceil(T_r/b)-1 loses
+ * one reference, is pushed onto the free stack (after the pops) when that
+ * empties it, and its table entry becomes -1.  Lengths become (N-1)*b.
+ * Returns the new free count. */
+int zpo_commit_prefill(int32_t *tables, int stride, int32_t *lengths, const int32_t *req_idx,
+                       int R, int N, int b, int32_t *refcount, int32_t *free_ids, int free_count,
+                       const int32_t *dst_table, int n_pops)
+{
+    int next_free = free_count - n_pops;
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        int nblk = (lengths[row] + b - 1) / b;
+        for (int p = 0; p < nblk; ++p) {
+            int32_t *entry = tables + (size_t)row * stride + p;
+            int32_t src = *entry;
+            int32_t dst = p < N ? dst_table[(size_t)r * N + p] : -1;
+            if (dst == src)
+                continue;
+            refcount[src] -= 1;
+            if (refcount[src] == 0)
+                free_ids[next_free++] = src;
+            if (dst >= 0)
+                refcount[dst] = 1;
+            *entry = dst;
+        }
+        lengths[row] = (N - 1) * b;
+    }
+    return next_free;
+}
+
+/* Compression at admission of requests longer than the budget: per unit the
+ * scores of zpo_unit_scores over its T_r tokens (window = the last w), the
+ * (N-1)*b - w best candidates kept with the window (zpo_select), compacted
+ * into the destinations of zpo_plan_prefill; then zpo_commit_prefill.
+ * scores_out: [L][R][Hkv][stride*b] (+inf at window positions, entries at
+ * T_r and beyond not written); other arguments as zpo_compress. */
+int zpo_compress_prefill(int L, int Hkv, int Hq, int d, int b, int num_blocks,
+                         const uint16_t *const *kpool, const uint16_t *const *vpool,
+                         uint16_t *const *kout, uint16_t *const *vout, int32_t *tables,
+                         int stride, int32_t *lengths, const int32_t *req_idx, int R,
+                         int num_rows, const uint16_t *window_q, int N, int w, double lambda,
+                         int32_t *free_ids, int32_t *free_count, int32_t *refcount,
+                         double *scores_out, int32_t *kept_out, int nthreads)
+{
+    if (L < 1 || Hkv < 1 || Hq < Hkv || Hq % Hkv || d < 1 || w < 1 || w > b)
+        return ZPO_ERR_INVALID_ARG;
+    int32_t *dst = (int32_t *)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1) * N);
+    int pops = 0;
+    int st = zpo_plan_prefill(tables, stride, lengths, req_idx, R, num_rows, N, b, num_blocks,
+                              refcount, free_ids, *free_count, dst, &pops);
+    if (st != ZPO_OK) {
+        free(dst);
+        return st;
+    }
+    compress_job J;
+    J.L = L; J.Hkv = Hkv; J.Hq = Hq; J.d = d; J.b = b; J.num_blocks = num_blocks;
+    J.kpool = kpool; J.vpool = vpool; J.kout = kout; J.vout = vout;
+    J.tables = tables; J.stride = stride; J.req_idx = req_idx;
+    J.R = R; J.N = N; J.w = w; J.lambda = lambda; J.window_q = window_q;
+    J.dst_table = dst; J.scores_out = scores_out; J.kept_out = kept_out;
+    J.unit_len = lengths; J.score_stride = stride * b;
+    run_units(&J, nthreads);
+    *free_count = zpo_commit_prefill(tables, stride, lengths, req_idx, R, N, b, refcount,
+                                     free_ids, *free_count, dst, pops);
     free(dst);
     return ZPO_OK;
 }

@@ -80,7 +80,8 @@ def torch_redundancy(K, b):
         cos[zero, :] = 0.0
         cos[:, zero] = 0.0
         cos.fill_diagonal_(0.0)
-        out[base:base + b] = (cos.sum(dim=1) / (b - 1)).numpy()
+        f = blk.shape[0]                            # filled slots (a partial last block)
+        out[base:base + f] = (cos.sum(dim=1) / (f - 1)).numpy() if f > 1 else 0.0
     return out
 
 
@@ -478,6 +479,192 @@ def pin_compress_rows_and_shared_blocks(orc):
     assert res["lengths"].tolist() == [(N - 1) * b] * R
     assert res["tables"][0, 0] != shared and res["tables"][1, 0] != shared
     assert res["refcount"][shared] == 0
+
+
+# ------------------------------------------------------------------ prefill
+
+def _prefill_cache(seed, lens, N=3, b=4, d=8, Hkv=2, G=2, L=2, w=2, share=0, spare=12):
+    """Requests of the given lengths in random blocks (entries beyond a
+    request's blocks -1); requests 0 and 1 share their first `share` blocks."""
+    g = rng(seed)
+    R = len(lens)
+    nblk = [-(-T // b) for T in lens]
+    stride = max(nblk)
+    num_blocks = sum(nblk) + spare
+    perm = g.permutation(num_blocks).astype(np.int32)
+    tables = np.full((R, stride), -1, dtype=np.int32)
+    nxt = 0
+    for r, n in enumerate(nblk):
+        s0 = share if r == 1 else 0
+        tables[r, :s0] = tables[0, :s0]
+        tables[r, s0:n] = perm[nxt:nxt + n - s0]
+        nxt += n - s0
+    rc = np.zeros(num_blocks, dtype=np.int32)
+    for x in tables.reshape(-1):
+        if x >= 0:
+            rc[x] += 1
+    free = np.full(num_blocks, -1, dtype=np.int32)
+    free[:num_blocks - nxt] = perm[nxt:]
+    kp = [bf16(g.standard_normal((num_blocks, Hkv, b, d))) for _ in range(L)]
+    vp = [bf16(g.standard_normal((num_blocks, Hkv, b, d))) for _ in range(L)]
+    wq = bf16(g.standard_normal((L, R, Hkv * G, w, d)))
+    return dict(kp=kp, vp=vp, tables=tables, lengths=np.array(lens, dtype=np.int32), rc=rc,
+                free=free, free_count=num_blocks - nxt, wq=wq, N=N, b=b, d=d, Hkv=Hkv, G=G, L=L,
+                R=R, w=w, num_blocks=num_blocks)
+
+
+def _run_prefill(orc, c, lam=0.5, **kw):
+    return orc.compress_prefill(c["kp"], c["vp"], c["tables"], c["lengths"], c["wq"], c["N"],
+                                c["w"], lam, c["free"], c["free_count"], c["rc"],
+                                Hq=c["Hkv"] * c["G"], **kw)
+
+
+def pin_prefill_handworked_release(orc):
+    """The hand-worked release of tests/golden/prefill_release_handworked.json."""
+    with open(os.path.join(GOLDEN, "prefill_release_handworked.json")) as f:
+        gd = json.load(f)
+    b, N, w, nb = gd["b"], gd["N"], gd["w"], gd["num_blocks"]
+    g = rng(150)
+    kp = [bf16(g.standard_normal((nb, 1, b, 4)))]
+    vp = [bf16(g.standard_normal((nb, 1, b, 4)))]
+    wq = bf16(g.standard_normal((1, 2, 1, w, 4)))
+    res = orc.compress_prefill(kp, vp, gd["tables"], gd["lengths"], wq, N, w, 0.5,
+                               gd["free_ids"], gd["free_count"], gd["refcount"], Hq=1)
+    assert res["status"] == 0
+    ex = gd["expect"]
+    assert res["tables"].tolist() == ex["tables"]
+    assert res["lengths"].tolist() == ex["lengths"]
+    assert res["refcount"].tolist() == ex["refcount"]
+    assert res["free_count"] == len(ex["free_ids"])
+    assert res["free_ids"][:res["free_count"]].tolist() == ex["free_ids"]
+
+
+def pin_prefill_at_budget_equals_compress(orc):
+    """Requests of exactly N*b tokens: compression at admission is the
+    decode-time compression, byte for byte."""
+    c = _tiny_cache(151)
+    N, b, w = c["N"], c["b"], c["w"]
+    a = orc.compress(c["kp"], c["vp"], c["tables"], c["lengths"], c["wq"], N, w, 0.5, c["free"],
+                     c["free_count"], c["rc"], Hq=c["Hkv"] * c["G"])
+    p = orc.compress_prefill(c["kp"], c["vp"], c["tables"], c["lengths"], c["wq"], N, w, 0.5,
+                             c["free"], c["free_count"], c["rc"], Hq=c["Hkv"] * c["G"])
+    assert a["status"] == p["status"] == 0
+    for k in ("tables", "lengths", "refcount", "free_ids", "kept"):
+        assert np.array_equal(a[k], p[k]), k
+    assert a["free_count"] == p["free_count"]
+    assert np.array_equal(a["scores"], p["scores"][..., :N * b])
+    for l in range(c["L"]):
+        assert np.array_equal(a["kpools"][l], p["kpools"][l])
+        assert np.array_equal(a["vpools"][l], p["vpools"][l])
+
+
+def pin_prefill_partial_block_redundancy(orc):
+    """A partial last block compares only its filled keys: two keys (1,0) and
+    (1,1) have redundancy cos = 1/sqrt2 each, a single key 0."""
+    K = bf16([[1, 0], [0, 1], [1, 1], [-1, 0], [1, 0], [1, 1]])
+    red = orc.redundancy(K, 4)
+    close(red[4:], [2 ** -0.5] * 2, 1e-12, "two-key block")
+    red5 = orc.redundancy(K[:5], 4)
+    close(red5[4:], [0.0], 0.0, "one-key block")
+    close(red5[:4], red[:4], 0.0, "full block unchanged")
+
+
+def pin_prefill_rows_scores_and_release(orc):
+    """Ragged requests longer than the budget, two sharing a prefix: the
+    scores equal torch's fp64 importance and cosine redundancy over each
+    request's own T tokens, the kept set is the top of a library sort by
+    (score desc, index asc) plus the window, every compacted row equals its
+    source row, shared blocks keep their bytes, every excess block loses one
+    reference, and blocks are conserved."""
+    lens = [23, 17, 12, 30]
+    c = _prefill_cache(152, lens, N=3, b=4, d=8, w=2, share=2)
+    N, b, w, G, d = c["N"], c["b"], c["w"], c["G"], c["d"]
+    res = _run_prefill(orc, c)
+    assert res["status"] == 0
+    n_keep = (N - 1) * b - w
+    for l in range(c["L"]):
+        for r, T in enumerate(lens):
+            C = T - w
+            n = -(-T // b)
+            for h in range(c["Hkv"]):
+                K = _gather(c["kp"][l], c["tables"][r, :n], h, b)[:T]
+                V = _gather(c["vp"][l], c["tables"][r, :n], h, b)[:T]
+                Q = c["wq"][l, r, h * G:(h + 1) * G].reshape(-1, d)
+                score = torch_importance(K, Q, w, G) - 0.5 * torch_redundancy(K, b)[:C]
+                close(res["scores"][l, r, h, :C], score, 1e-12, "prefill scores")
+                assert np.all(np.isinf(res["scores"][l, r, h, C:T]))
+                order = np.lexsort((np.arange(C), -res["scores"][l, r, h, :C]))
+                want = sorted(order[:n_keep].tolist()) + list(range(C, T))
+                kept = res["kept"][l, r, h]
+                assert kept.tolist() == want
+                new_row = res["tables"][r, :N - 1]
+                assert np.array_equal(_gather(res["kpools"][l], new_row, h, b), K[kept])
+                assert np.array_equal(_gather(res["vpools"][l], new_row, h, b), V[kept])
+    shared = c["tables"][0, :2]
+    for l in range(c["L"]):
+        assert np.array_equal(res["kpools"][l][shared], c["kp"][l][shared])
+    assert res["lengths"].tolist() == [(N - 1) * b] * len(lens)
+    assert np.all(res["tables"][:, N:] == -1)
+    ref = np.zeros_like(res["refcount"])
+    for x in res["tables"].reshape(-1):
+        if x >= 0:
+            ref[x] += 1
+    assert np.array_equal(ref, res["refcount"])
+    fc = res["free_count"]
+    assert fc + int(np.count_nonzero(res["refcount"])) == c["num_blocks"]
+    assert np.all(res["refcount"][res["free_ids"][:fc]] == 0)
+    assert len(set(res["free_ids"][:fc].tolist())) == fc
+
+
+def pin_prefill_attention_masked(orc):
+    """Attention over the cache compressed at admission equals attention over
+    the original rows restricted to the kept indices."""
+    lens = [29, 18]
+    c = _prefill_cache(153, lens, N=3, b=4, d=8, L=1, w=2)
+    res = _run_prefill(orc, c)
+    assert res["status"] == 0
+    q = bf16(rng(154).standard_normal((2, c["Hkv"] * c["G"], c["d"])))
+    scale = 1.0 / math.sqrt(c["d"])
+    st, o64, _ = orc.decode_attn(q, res["kpools"][0], res["vpools"][0], res["tables"],
+                                 res["lengths"], scale)
+    assert st == 0
+    for r, T in enumerate(lens):
+        n = -(-T // c["b"])
+        for hq in range(c["Hkv"] * c["G"]):
+            h = hq // c["G"]
+            K = torch.tensor(widen(_gather(c["kp"][0], c["tables"][r, :n], h, c["b"])[:T]))
+            V = torch.tensor(widen(_gather(c["vp"][0], c["tables"][r, :n], h, c["b"])[:T]))
+            mask = torch.zeros(T, dtype=torch.bool)
+            mask[torch.tensor(res["kept"][0, r, h], dtype=torch.long)] = True
+            o = torch.nn.functional.scaled_dot_product_attention(
+                torch.tensor(widen(q[r, hq]))[None, None, :], K[None], V[None],
+                attn_mask=mask[None, None, :], scale=scale)[0, 0]
+            close(o64[r, hq], o.numpy(), 1e-12, "prefill compacted vs masked")
+
+
+def pin_prefill_errors(orc):
+    """All or nothing: a request shorter than N*b, longer than its table row,
+    with a missing block, or too few free blocks changes nothing."""
+    base = _prefill_cache(155, [20, 14], N=3, b=4, d=4, L=1, w=2, share=2, spare=2)
+
+    def run(**ch):
+        c = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in base.items()}
+        c.update(ch)
+        res = _run_prefill(orc, c)
+        if res["status"] != 0:
+            assert np.array_equal(res["tables"], c["tables"])
+            assert np.array_equal(res["lengths"], c["lengths"])
+            assert np.array_equal(res["refcount"], c["rc"])
+            assert res["free_count"] == c["free_count"]
+        return res["status"]
+
+    assert run() == 0
+    assert run(lengths=np.array([20, 11], dtype=np.int32)) == -1
+    assert run(lengths=np.array([21, 14], dtype=np.int32)) == -1
+    t = base["tables"].copy()
+    t[0, 3] = -1
+    assert run(tables=t) == -1
+    assert run(free_count=1) == -3
 
 
 # ------------------------------------------------------------------- decode

@@ -26,8 +26,21 @@ MUTANTS = [
     ("softmax sum over candidates only",
      "for (int j = 0; j < visible; ++j)\n                S += exp(logit[j] - m);",
      "for (int j = 0; j < C; ++j)\n                S += exp(logit[j] - m);"),
-    ("redundancy divided by b", "red[base + j] = sum / (double)(b - 1);",
-     "red[base + j] = sum / (double)b;"),
+    ("redundancy divided by b", "red[base + j] = f > 1 ? sum / (double)(f - 1) : 0.0;",
+     "red[base + j] = f > 1 ? sum / (double)f : 0.0;"),
+    ("partial block divided by b-1", "red[base + j] = f > 1 ? sum / (double)(f - 1) : 0.0;",
+     "red[base + j] = f > 1 ? sum / (double)(b - 1) : 0.0;"),
+    ("prefill: excess blocks kept", "int32_t dst = p < N ? dst_table[(size_t)r * N + p] : -1;",
+     "int32_t dst = p < N ? dst_table[(size_t)r * N + p] : src;"),
+    ("prefill: length rounded up to whole blocks",
+     "int T = J->unit_len ? J->unit_len[row] : N * b;",
+     "int T = J->unit_len ? (J->unit_len[row] + b - 1) / b * b : N * b;"),
+    ("prefill: short request accepted", "if (T < N * b || T > stride * b)",
+     "if (T > stride * b)"),
+    ("prefill: released blocks pushed before the pops", "int next_free = free_count - n_pops;",
+     "int next_free = free_count;"),
+    ("prefill: shared block rewritten in place", "if (refcount[src] > 1) {\n                if (taken",
+     "if (refcount[src] > 2) {\n                if (taken"),
     ("self included in redundancy", "if (k == j)\n                    continue;", ""),
     ("squared norm", "norm[j] = sqrt(dot_bf16(kj, kj, d));", "norm[j] = dot_bf16(kj, kj, d);"),
     ("zero-norm guard one-sided", "if (norm[j] > 0.0 && norm[k] > 0.0)", "if (norm[j] > 0.0)"),
