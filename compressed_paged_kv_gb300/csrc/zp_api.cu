@@ -271,6 +271,8 @@ zp_status zp_compress(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int
     pa.req_idx = req_idx;
     pa.R = R;
     pa.N = n_max;
+    pa.M = n_max;
+    pa.prefill = 0;
     pa.num_blocks = c->num_blocks;
     pa.refcount = pool->refcount;
     pa.free_ids = pool->free_ids;
@@ -314,6 +316,137 @@ zp_status zp_compress(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int
     fa.req_idx = req_idx;
     fa.R = R;
     fa.N = n_max;
+    fa.M = n_max;
+    fa.prefill = 0;
+    fa.refcount = pool->refcount;
+    fa.free_ids = pool->free_ids;
+    fa.free_count = pool->free_count;
+    fa.ws = c->ws;
+    if (zp::launch_finalize(fa, s) != cudaSuccess)
+        return ZP_ERR_CUDA;
+    return ZP_OK;
+}
+
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+zp_status zp_compress_prefill_workspace_size(const zp_cache *c, int32_t R, int32_t bt_stride,
+                                             size_t *bytes)
+{
+    if (!c || !bytes || R < 0 || bt_stride < 1)
+        return ZP_ERR_INVALID_ARG;
+    const size_t units = static_cast<size_t>(R) * c->L * c->Hkv;
+    const size_t T_cap = static_cast<size_t>(bt_stride) * c->b;
+    const size_t NC = (T_cap + zp::kPrefillChunk - 1) / zp::kPrefillChunk;
+    *bytes = align256(units * NC * zp::kMaxRows * sizeof(float2)) +  // chunk statistics
+             2 * align256(units * T_cap * 4) +                        // redundancy, scores
+             align256(units * T_cap * 4);                             // kept positions
+    return ZP_OK;
+}
+
+zp_status zp_compress_prefill(zp_cache *c, int32_t *block_tables, int32_t bt_stride,
+                              int32_t num_rows, int32_t *lengths, const int32_t *req_idx,
+                              int32_t R, const void *window_q, int32_t n_max, int32_t window,
+                              float lambda, const zp_block_pool *pool, void *workspace,
+                              size_t workspace_bytes, void *stream, float *scores_out,
+                              int32_t *kept_out)
+{
+    if (!c || !block_tables || !lengths || !window_q || !pool || !pool->free_ids ||
+        !pool->free_count || !pool->refcount)
+        return ZP_ERR_INVALID_ARG;
+    if (R < 0 || num_rows < 1 || num_rows > c->max_requests || R > num_rows)
+        return ZP_ERR_INVALID_ARG;
+    if (n_max < 2 || bt_stride < n_max || pool->capacity < 1)
+        return ZP_ERR_INVALID_ARG;
+    if (window < 1 || window > c->b || !std::isfinite(lambda))
+        return ZP_ERR_INVALID_ARG;
+    if (!aligned(window_q, 16) || !aligned(scores_out, 4) || !aligned(kept_out, 4) ||
+        !aligned(workspace, 256))
+        return ZP_ERR_INVALID_ARG;
+    const int G = c->Hq / c->Hkv;
+    const int rows = window * G;
+    if (bt_stride > c->max_blocks || static_cast<long long>(bt_stride) * c->b > zp::kPrefillMaxTokens ||
+        rows > zp::kMaxRows)
+        return ZP_ERR_UNSUPPORTED;
+    size_t need = 0;
+    zp_compress_prefill_workspace_size(c, R, bt_stride, &need);
+    if (R > 0 && (!workspace || workspace_bytes < need))
+        return ZP_ERR_INVALID_ARG;
+    if (R == 0)
+        return ZP_OK;
+    if (!on_device(c))
+        return ZP_ERR_INVALID_ARG;
+    const long long units = static_cast<long long>(R) * c->L * c->Hkv;
+    if (units >= (1ll << 31))
+        return ZP_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int mt = rows <= 16 ? 1 : rows <= 32 ? 2 : 4;
+    const int T_cap = bt_stride * c->b;
+    const int NC = (T_cap + zp::kPrefillChunk - 1) / zp::kPrefillChunk;
+
+    zp::PlanArgs pa{};
+    pa.tables = block_tables;
+    pa.stride = bt_stride;
+    pa.num_rows = num_rows;
+    pa.lengths = lengths;
+    pa.req_idx = req_idx;
+    pa.R = R;
+    pa.N = n_max;
+    pa.M = bt_stride;
+    pa.prefill = 1;
+    pa.num_blocks = c->num_blocks;
+    pa.refcount = pool->refcount;
+    pa.free_ids = pool->free_ids;
+    pa.free_count = pool->free_count;
+    pa.capacity = pool->capacity;
+    pa.ws = c->ws;
+    if (zp::launch_plan(pa, s) != cudaSuccess)
+        return ZP_ERR_CUDA;
+
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    const size_t U = static_cast<size_t>(units);
+    zp::PrefillArgs a{};
+    a.kmaps = c->ws.kmaps;
+    a.kpools = c->ws.kpools;
+    a.vpools = c->ws.vpools;
+    a.tables = block_tables;
+    a.stride = bt_stride;
+    a.lengths = lengths;
+    a.req_idx = req_idx;
+    a.dst_table = c->ws.dst_table;
+    a.window_q = static_cast<const __nv_bfloat16 *>(window_q);
+    a.stats = reinterpret_cast<float2 *>(w);
+    w += align256(U * NC * zp::kMaxRows * sizeof(float2));
+    a.red = reinterpret_cast<float *>(w);
+    w += align256(U * T_cap * 4);
+    a.scores = scores_out ? scores_out : reinterpret_cast<float *>(w);
+    w += align256(U * T_cap * 4);
+    a.kept = kept_out ? kept_out : reinterpret_cast<int32_t *>(w);
+    a.call = c->ws.call;
+    a.sticky = c->ws.sticky;
+    a.L = c->L;
+    a.Hkv = c->Hkv;
+    a.Hq = c->Hq;
+    a.R = R;
+    a.N = n_max;
+    a.w = window;
+    a.rows = rows;
+    a.T_cap = T_cap;
+    a.NC = NC;
+    a.lambda = lambda;
+    a.inv_rows = 1.0f / static_cast<float>(rows);
+    a.logit_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c->d)));
+    if (zp::launch_prefill(a, c->d, mt, static_cast<int>(units), s) != cudaSuccess)
+        return ZP_ERR_CUDA;
+
+    zp::FinalizeArgs fa{};
+    fa.tables = block_tables;
+    fa.stride = bt_stride;
+    fa.lengths = lengths;
+    fa.req_idx = req_idx;
+    fa.R = R;
+    fa.N = n_max;
+    fa.M = bt_stride;
+    fa.prefill = 1;
     fa.refcount = pool->refcount;
     fa.free_ids = pool->free_ids;
     fa.free_count = pool->free_count;

@@ -50,7 +50,8 @@ __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
     __syncthreads();
     const int fc = s_fc;
 
-    // rows: in range, distinct, full (the trigger needs N_max full blocks)
+    // rows: in range, distinct, full (the trigger needs N_max full blocks;
+    // at admission at least N_max*b tokens, within the table row)
     for (int r = tid; r < a.R; r += kPlanThreads) {
         const int row = a.req_idx ? a.req_idx[r] : r;
         if (row < 0 || row >= a.num_rows) {
@@ -59,7 +60,8 @@ __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
         }
         if (atomicExch(&a.ws.rowmark[row], s_gen) == s_gen)
             atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
-        if (a.lengths[row] != a.N * kBlk)
+        const int len = a.lengths[row];
+        if (a.prefill ? (len < a.N * kBlk || len > a.stride * kBlk) : len != a.N * kBlk)
             atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
     }
     __syncthreads();
@@ -71,19 +73,33 @@ __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
 
     // destinations: refcount 1 -> in place, > 1 -> pop a fresh target.  The
     // k-th needing entry in (request, block) order pops free_ids[fc-1-k].
+    // Entries at block N_max and beyond (admission only) are released: their
+    // destination is -1.  Entries past a request's blocks are not entries.
     // Thread t owns the contiguous entries [t*per, (t+1)*per): its loads are
     // independent, and one block scan orders the pops.
-    const int E = a.R * a.N;
+    const int E = a.R * a.M;
     const int per = (E + kPlanThreads - 1) / kPlanThreads;
     const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
     auto src_of = [&](int e) {
-        const int r = e / a.N, p = e - r * a.N;
+        const int r = e / a.M, p = e - r * a.M;
         const int row = a.req_idx ? a.req_idx[r] : r;
         return a.tables[(size_t)row * a.stride + p];
+    };
+    // 0: not an entry, 1: destination block (p < N), 2: released (p >= N)
+    auto kind_of = [&](int e) {
+        if (!a.prefill)
+            return 1;
+        const int r = e / a.M, p = e - r * a.M;
+        const int row = a.req_idx ? a.req_idx[r] : r;
+        const int nblk = (a.lengths[row] + kBlk - 1) / kBlk;
+        return p >= nblk ? 0 : p < a.N ? 1 : 2;
     };
     int my_need = 0;
 #pragma unroll 8
     for (int e = e0; e < e1; ++e) {
+        const int kind = kind_of(e);
+        if (kind == 0)
+            continue;
         const int blk = src_of(e);
         if (blk < 0 || blk >= a.num_blocks) {
             atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
@@ -92,7 +108,7 @@ __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
         const int rc = a.refcount[blk];
         if (rc < 1)
             atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
-        my_need += rc > 1;
+        my_need += kind == 1 && rc > 1;
     }
     int pops;
     int k = block_excl_scan<kPlanThreads>(my_need, s_scan, pops);
@@ -108,9 +124,10 @@ __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
     }
 #pragma unroll 8
     for (int e = e0; e < e1; ++e) {
+        const int kind = kind_of(e);
         const int blk = src_of(e);
-        int dst = blk;
-        if (a.refcount[blk] > 1) {
+        int dst = kind == 2 ? -1 : blk;
+        if (kind == 1 && a.refcount[blk] > 1) {
             dst = a.free_ids[fc - 1 - k];
             ++k;
             if (dst < 0 || dst >= a.num_blocks || a.refcount[dst] != 0)
@@ -119,7 +136,7 @@ __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
         a.ws.dst_table[e] = dst;
     }
     __syncthreads();
-    if (s_err != 0 || pops == 0) {
+    if (s_err != 0 || (pops == 0 && !a.prefill)) {
         // nothing shared: no reference is released, nothing is pushed
         if (tid == 0) {
             a.ws.counters[0] = pops;
@@ -190,16 +207,18 @@ __global__ void __launch_bounds__(kPlanThreads) zp_finalize_kernel(const Finaliz
         s_fc = *a.free_count;
     __syncthreads();
     const int pops = a.ws.counters[0], pushes = a.ws.counters[1];
-    const int E = pops > 0 ? a.R * a.N : 0;  // nothing shared: tables unchanged
+    // nothing shared and nothing released: tables unchanged
+    const int E = pops > 0 || a.prefill ? a.R * a.M : 0;
     for (int e = tid; e < E; e += kPlanThreads) {
-        const int r = e / a.N, p = e - r * a.N;
+        const int r = e / a.M, p = e - r * a.M;
         const int row = a.req_idx ? a.req_idx[r] : r;
         int32_t *slot = a.tables + (size_t)row * a.stride + p;
         const int src = *slot, dst = a.ws.dst_table[e];
         if (dst != src) {
             if (a.ws.last[src] == e)
                 a.refcount[src] -= a.ws.occ[src];
-            a.refcount[dst] = 1;
+            if (dst >= 0)
+                a.refcount[dst] = 1;
             *slot = dst;
         }
     }

@@ -47,12 +47,15 @@ struct Workspace {
 };
 
 // ------------------------------------------------------------ launch args
+// The plan and finalize kernels serve both compressions: at N_max full
+// blocks (M = N, every request exactly N*b tokens) and at admission (prefill:
+// M = the table stride, N*b <= T <= M*b, blocks N .. of a request released).
 struct PlanArgs {
     const int32_t *tables;
     int32_t stride, num_rows;
     const int32_t *lengths;
     const int32_t *req_idx;
-    int32_t R, N, num_blocks;
+    int32_t R, N, M, prefill, num_blocks;
     const int32_t *refcount;
     const int32_t *free_ids;
     const int32_t *free_count;
@@ -65,7 +68,7 @@ struct FinalizeArgs {
     int32_t stride;
     int32_t *lengths;
     const int32_t *req_idx;
-    int32_t R, N;
+    int32_t R, N, M, prefill;
     int32_t *refcount;
     int32_t *free_ids;
     int32_t *free_count;
@@ -107,6 +110,29 @@ struct DecodeArgs {
     int32_t *sticky;
 };
 
+// Compression at admission (zp_prefill.cu); units u = (l*R + r)*Hkv + h.
+struct PrefillArgs {
+    const CUtensorMap *kmaps;
+    void *const *kpools;
+    void *const *vpools;
+    const int32_t *tables;
+    int32_t stride;
+    const int32_t *lengths;
+    const int32_t *req_idx;
+    const int32_t *dst_table;  // [R][stride] from the plan
+    const __nv_bfloat16 *window_q;
+    float2 *stats;             // [units][NC][kMaxRows] per-chunk (max, sum), base 2
+    float *red;                // [units][T_cap]
+    float *scores;             // [units][T_cap] (the caller's scores_out when given)
+    int32_t *kept;             // [units][(N-1)*b] (the caller's kept_out when given)
+    int32_t *call;
+    int32_t *sticky;
+    int32_t L, Hkv, Hq, R, N, w, rows, T_cap, NC;
+    float lambda;
+    float inv_rows;
+    float logit_scale;
+};
+
 struct AppendArgs {
     int32_t *tables;
     int32_t stride, num_rows;
@@ -135,6 +161,10 @@ struct AppendKvArgs {
 
 // Launchers (defined next to their kernels).
 cudaError_t launch_append_slots(const AppendArgs &a, cudaStream_t s);
+// Scoring, selection and compaction of a compression at admission.
+cudaError_t launch_prefill(const PrefillArgs &a, int d, int mt, int units, cudaStream_t s);
+constexpr int kPrefillChunk = 512;      // tokens per scoring CTA
+constexpr int kPrefillMaxTokens = 32768;  // scores of one unit fit in shared memory
 cudaError_t launch_append_kv(const AppendKvArgs &a, cudaStream_t s);
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s);

@@ -1,0 +1,553 @@
+// zp_prefill.cu -- compression at admission of requests longer than the budget.
+//
+// Zipage (gist.science, Dutch "Methodologie" §1): the kept entries move into
+// the first N_max-1 blocks, the N_max-th block is reserved for decoding, and
+// the excess blocks are released; §3: shared blocks compress into fresh target
+// blocks; §5 and Korean "방법론" E: the Lightning Redundancy Score compares the
+// keys of one block only.  The scores are those of zp_compress computed over
+// each request's own T >= N_max*b tokens (the window is its last w tokens); the
+// selection keeps (N_max-1)*b - w candidates, so T - (N_max-1)*b tokens go --
+// a number that varies per request and can be most of the request.
+//
+// Launches, between the shared plan and finalize kernels (zp_compress.cu):
+//   zp_prefill_pass_kernel<.., false>  grid (unit, chunk of 512 tokens), four
+//       warps each streaming their blocks through a private three-stage TMA
+//       ring: window logits and the Gram of each block on mma.sync, the
+//       chunk's softmax statistics of every window row, the redundancy of
+//       every key (over the filled slots of its block) -> workspace.
+//   zp_prefill_pass_kernel<.., true>   same grid: the statistics of all
+//       chunks of the unit merged, logits again, importance and score.
+//   zp_prefill_select_kernel  one CTA per unit: radix select (four 8-bit
+//       digit passes over the order-preserving image of the fp32 scores held
+//       in shared memory) of the K_keep-th largest score; ties at the
+//       threshold go to the lower index; the kept positions in ascending
+//       order by block scans, then the window.
+//   zp_prefill_compact_kernel  one CTA per unit: destination rows in
+//       ascending chunks of 64; a chunk's source rows are read before any of
+//       its writes (one barrier), and every later chunk reads sources at or
+//       after its own first destination (kept[j] >= j), which no earlier
+//       chunk wrote -- so compacting in place is safe.
+#include "zp_internal.cuh"
+
+namespace zp {
+
+constexpr int kPW = 4;                       // warps of a scoring CTA
+constexpr int kPThreads = kPW * 32;
+constexpr int kPStages = 3;                  // TMA stages per warp
+constexpr int kPChunk = kPrefillChunk;       // tokens per scoring CTA
+constexpr int kPBlocks = kPChunk / kBlk;
+constexpr int kSelThreads = 1024;
+constexpr int kCmpThreads = 256;
+constexpr int kCmpRows = 64;                 // destination rows per compaction chunk
+
+template <int D, int MT>
+struct PrefillSmem {
+    static constexpr int ROWS = MT * 16;
+    static constexpr int SLAB = kBlk * D * 2;
+    static constexpr int off_ring = 0;                              // [kPW][kPStages][SLAB]
+    static constexpr int off_q = off_ring + kPW * kPStages * SLAB;  // bf16 [ROWS][D], swizzled
+    static constexpr int off_rm = off_q + ROWS * D * 2;             // float [kPW][ROWS]
+    static constexpr int off_rs = off_rm + kPW * ROWS * 4;          // float [kPW][ROWS]
+    static constexpr int off_gm = off_rs + kPW * ROWS * 4;          // float [ROWS]
+    static constexpr int off_ginv = off_gm + ROWS * 4;              // float [ROWS]
+    static constexpr int off_inv = off_ginv + ROWS * 4;             // float [kPW][b]
+    static constexpr int off_bar = (off_inv + kPW * kBlk * 4 + 7) / 8 * 8;
+    static constexpr int BYTES = off_bar + kPW * kPStages * 8;
+    static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024 B
+};
+
+// Merges the softmax statistics (m, s) of two key sets (base 2); (-inf, 0) is
+// the empty set.
+__device__ __forceinline__ void stat_merge(float &m, float &s, float m2, float s2)
+{
+    if (m2 == -INFINITY)
+        return;
+    if (m == -INFINITY) {
+        m = m2;
+        s = s2;
+        return;
+    }
+    const float mn = fmaxf(m, m2);
+    s = s * exp2f(m - mn) + s2 * exp2f(m2 - mn);
+    m = mn;
+}
+
+template <int D, int MT, bool SCORE>
+__global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const PrefillArgs a)
+{
+    using S = PrefillSmem<D, MT>;
+    constexpr int ROWS = S::ROWS, SLAB = S::SLAB, HALVES = D / 64, CPR = D / 8;
+    if (*(volatile int32_t *)a.call != 0)
+        return;
+    const int u = blockIdx.x, chunk = blockIdx.y;
+    const int h = u % a.Hkv, r = (u / a.Hkv) % a.R, l = u / (a.Hkv * a.R);
+    const int row = a.req_idx ? a.req_idx[r] : r;
+    const int T = a.lengths[row];  // checked by the plan
+    const int C = T - a.w;
+    const int t0 = chunk * kPChunk;
+    if (t0 >= T)
+        return;
+    const int nblk = min(kPBlocks, (T - t0 + kBlk - 1) / kBlk);
+    const int G = a.Hq / a.Hkv;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sQ = sm + S::off_q;
+    float *sRM = reinterpret_cast<float *>(sm + S::off_rm);
+    float *sRS = reinterpret_cast<float *>(sm + S::off_rs);
+    float *sGm = reinterpret_cast<float *>(sm + S::off_gm);
+    float *sGinv = reinterpret_cast<float *>(sm + S::off_ginv);
+    float *sInv = reinterpret_cast<float *>(sm + S::off_inv);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::off_bar);
+    const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5, mi = lane >> 3;
+
+    // window queries -> shared memory (swizzled, rows past w*G zero)
+    {
+        const __nv_bfloat16 *qsrc =
+            a.window_q + ((((size_t)l * a.R + r) * a.Hq + (size_t)h * G) * a.w) * D;
+        const uint32_t qb = smem_u32(sQ);
+        for (int c = tid; c < ROWS * CPR; c += kPThreads) {
+            const int rr = c / CPR, ch = c - rr * CPR;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (rr < a.rows)
+                v = ld_global_nc_v4(qsrc + (size_t)rr * D + ch * 8);
+            st_shared_v4(qb + swz(rr, ch, ROWS), v);
+        }
+    }
+    if (tid < kPW * kPStages)
+        mbar_init(&bars[tid], 1);
+    if (tid == 0)
+        fence_mbar_init();
+    if (SCORE && tid < ROWS) {
+        // statistics of all keys of the unit: merge the chunks
+        const int nc = (T + kPChunk - 1) / kPChunk;
+        const float2 *st = a.stats + (size_t)u * a.NC * kMaxRows + tid;
+        float m = -INFINITY, s = 0.f;
+        for (int c = 0; c < nc; ++c) {
+            const float2 v = st[(size_t)c * kMaxRows];
+            stat_merge(m, s, v.x, v.y);
+        }
+        sGm[tid] = m;
+        sGinv[tid] = tid < a.rows && s > 0.f ? 1.0f / s : 0.f;
+    }
+    __syncthreads();
+
+    // this warp's blocks of the chunk: wi, wi + kPW, ...
+    const int my_n = wi < nblk ? (nblk - wi + kPW - 1) / kPW : 0;
+    uint8_t *ring = sm + S::off_ring + wi * kPStages * SLAB;
+    uint64_t *bar = bars + wi * kPStages;
+    const int32_t *trow = a.tables + (size_t)row * a.stride;
+    const CUtensorMap *kmap = a.kmaps + l;
+    auto issue = [&](int i) {
+        const int blk = trow[t0 / kBlk + wi + i * kPW];  // checked by the plan
+        const int s = i % kPStages;
+        mbar_arrive_expect_tx(&bar[s], SLAB);
+        const int y = (blk * a.Hkv + h) * kBlk;
+#pragma unroll
+        for (int hf = 0; hf < HALVES; ++hf)
+            tma_load_2d(ring + s * SLAB + hf * kBlk * 128, kmap, hf * 64, y, &bar[s]);
+    };
+    if (lane == 0)
+        for (int i = 0; i < my_n && i < kPStages; ++i)
+            issue(i);
+
+    int slot_of[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int rr = mt * 16 + (lane >> 2) + hh * 8;
+            slot_of[mt][hh] = rr < a.rows ? rr % a.w : -1;
+        }
+    float rm[MT][2], rsum[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            rm[mt][hh] = -INFINITY;
+            rsum[mt][hh] = 0.f;
+        }
+    const size_t ubase = (size_t)u * a.T_cap;
+    const uint32_t qb = smem_u32(sQ);
+    bool ok = true;
+
+    for (int i = 0; i < my_n; ++i) {
+        const int s = i % kPStages;
+        ok &= mbar_wait(&bar[s], (i / kPStages) & 1);
+        const int key0 = t0 + (wi + i * kPW) * kBlk;  // token of the block's slot 0
+        const uint32_t kb = smem_u32(ring + s * SLAB);
+        float acc[MT][2][4], gram[2][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    acc[mt][nt][e] = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                gram[nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            uint32_t kf[4];
+            ldsm_x4(kb + swz((mi >> 1) * 8 + (lane & 7), ks * 2 + (mi & 1), kBlk), kf);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                uint32_t qa[4];
+                ldsm_x4(qb + swz(mt * 16 + (mi & 1) * 8 + (lane & 7), ks * 2 + (mi >> 1), ROWS),
+                        qa);
+                mma_bf16(acc[mt][0], qa[0], qa[1], qa[2], qa[3], kf[0], kf[1]);
+                mma_bf16(acc[mt][1], qa[0], qa[1], qa[2], qa[3], kf[2], kf[3]);
+            }
+            if (!SCORE) {
+                mma_bf16(gram[0], kf[0], kf[2], kf[1], kf[3], kf[0], kf[1]);
+                mma_bf16(gram[1], kf[0], kf[2], kf[1], kf[3], kf[2], kf[3]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && i + kPStages < my_n) {
+            fence_proxy_async_smem();
+            issue(i + kPStages);
+        }
+        // base-2 logits; window row of slot i sees keys up to C + i, which
+        // also hides the unfilled slots of a partial last block
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float v = acc[mt][nt][e] * a.logit_scale;
+                    const int slot = slot_of[mt][e >> 1];
+                    const int tok = key0 + nt * 8 + (lane & 3) * 2 + (e & 1);
+                    if (slot >= 0 ? tok > C + slot : tok >= T)
+                        v = -INFINITY;
+                    acc[mt][nt][e] = v;
+                }
+
+        if (!SCORE) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const float bm = fmaxf(fmaxf(acc[mt][0][hh * 2], acc[mt][0][hh * 2 + 1]),
+                                           fmaxf(acc[mt][1][hh * 2], acc[mt][1][hh * 2 + 1]));
+                    const float m_new = fmaxf(rm[mt][hh], bm);
+                    if (m_new == -INFINITY)
+                        continue;
+                    float sum = rm[mt][hh] == -INFINITY
+                                    ? 0.f
+                                    : rsum[mt][hh] * exp2f(rm[mt][hh] - m_new);
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+                        sum += exp2f(acc[mt][nt][hh * 2] - m_new) +
+                               exp2f(acc[mt][nt][hh * 2 + 1] - m_new);
+                    rm[mt][hh] = m_new;
+                    rsum[mt][hh] = sum;
+                }
+            // redundancy over the f filled slots: G[j][k] is element e of
+            // n-tile nt with j = lane/4 + 8(e/2), k = 8 nt + 2 (lane%4) + e%2
+            const int f = min(kBlk, T - key0);
+            float *inv = sInv + wi * kBlk;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = (lane >> 2) + (e >> 1) * 8, k = nt * 8 + (lane & 3) * 2 + (e & 1);
+                    if (j == k)
+                        inv[j] = gram[nt][e];
+                }
+            __syncwarp();
+            if (lane < kBlk) {
+                const float dj = inv[lane];
+                inv[lane] = lane < f && dj > 0.f ? 1.0f / sqrtf(dj) : 0.f;
+            }
+            __syncwarp();
+            float rs[2] = {0.f, 0.f};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = (lane >> 2) + (e >> 1) * 8, k = nt * 8 + (lane & 3) * 2 + (e & 1);
+                    if (j != k && k < f)
+                        rs[e >> 1] += gram[nt][e] * inv[k];
+                }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float v = rs[hh];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                const int j = (lane >> 2) + hh * 8;
+                if ((lane & 3) == 0 && j < f)
+                    a.red[ubase + key0 + j] = f > 1 ? inv[j] * v / static_cast<float>(f - 1) : 0.f;
+            }
+            __syncwarp();
+        } else {
+            // importance = mean over the window rows of the softmax probability
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int ee = 0; ee < 2; ++ee) {
+                    float v = 0.f;
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int rr = mt * 16 + (lane >> 2) + hh * 8;
+                            v += exp2f(acc[mt][nt][hh * 2 + ee] - sGm[rr]) * sGinv[rr];
+                        }
+                    v += __shfl_xor_sync(0xffffffffu, v, 4);
+                    v += __shfl_xor_sync(0xffffffffu, v, 8);
+                    v += __shfl_xor_sync(0xffffffffu, v, 16);
+                    const int key = key0 + nt * 8 + lane * 2 + ee;
+                    if (lane < 4 && key < T)
+                        a.scores[ubase + key] =
+                            key < C ? v * a.inv_rows - a.lambda * a.red[ubase + key] : INFINITY;
+                }
+        }
+    }
+    if (!ok && lane == 0)
+        set_error(a.sticky, ZP_ERR_TIMEOUT);
+
+    if (!SCORE) {
+        // the chunk's statistics of every row: lanes, then warps
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float m = rm[mt][hh], s = rsum[mt][hh];
+#pragma unroll
+                for (int o = 1; o <= 2; o <<= 1) {
+                    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+                    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+                    stat_merge(m, s, m2, s2);
+                }
+                if ((lane & 3) == 0) {
+                    const int rr = mt * 16 + (lane >> 2) + hh * 8;
+                    sRM[wi * ROWS + rr] = m;
+                    sRS[wi * ROWS + rr] = s;
+                }
+            }
+        __syncthreads();
+        if (tid < ROWS) {
+            float m = -INFINITY, s = 0.f;
+#pragma unroll
+            for (int w2 = 0; w2 < kPW; ++w2)
+                stat_merge(m, s, sRM[w2 * ROWS + tid], sRS[w2 * ROWS + tid]);
+            a.stats[((size_t)u * a.NC + chunk) * kMaxRows + tid] = make_float2(m, s);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kSelThreads) zp_prefill_select_kernel(const PrefillArgs a)
+{
+    if (*(volatile int32_t *)a.call != 0)
+        return;
+    extern __shared__ uint32_t sKey[];  // [T_cap] order images of the scores
+    __shared__ int hist[256];
+    __shared__ int s_scan[kSelThreads / 32 + 1];
+    __shared__ uint32_t s_prefix;
+    __shared__ int s_need;
+    const int tid = threadIdx.x;
+    const int u = blockIdx.x;
+    const int r = (u / a.Hkv) % a.R;
+    const int row = a.req_idx ? a.req_idx[r] : r;
+    const int T = a.lengths[row];
+    const int C = T - a.w;
+    const int KT = (a.N - 1) * kBlk, keep = KT - a.w;  // keep < C since T >= N*b
+    const float *sc = a.scores + (size_t)u * a.T_cap;
+    for (int j = tid; j < C; j += kSelThreads)
+        sKey[j] = f32_order(sc[j]);
+    if (tid == 0) {
+        s_prefix = 0u;
+        s_need = keep;
+    }
+    __syncthreads();
+
+    // the keep-th largest order image, one 8-bit digit at a time from the top
+    uint32_t mask = 0u;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += kSelThreads)
+            hist[i] = 0;
+        __syncthreads();
+        const uint32_t prefix = s_prefix;
+        for (int j = tid; j < C; j += kSelThreads) {
+            const uint32_t k = sKey[j];
+            if ((k & mask) == prefix)
+                atomicAdd(&hist[(k >> shift) & 255u], 1);
+        }
+        __syncthreads();
+        if (tid < 32) {
+            // warp 0: the digit at which the count from the top reaches s_need
+            const int need = s_need;
+            int above = 0;  // keys with a larger digit, over the digits done
+            int digit = -1, before = 0;
+            for (int base = 255; base >= 0 && digit < 0; base -= 32) {
+                const int dg = base - tid;  // lane t takes digit base - t
+                const int c = hist[dg];
+                int incl = c;  // inclusive sum over lanes 0..t (larger digits first)
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (tid >= o)
+                        incl += y;
+                }
+                const unsigned hit = __ballot_sync(0xffffffffu, above + incl >= need);
+                if (hit) {
+                    const int t = __ffs(hit) - 1;
+                    const int excl = __shfl_sync(0xffffffffu, incl - c, t);
+                    digit = base - t;
+                    before = above + excl;
+                } else {
+                    above += __shfl_sync(0xffffffffu, incl, 31);
+                }
+            }
+            if (tid == 0) {
+                s_prefix = prefix | (static_cast<uint32_t>(digit) << shift);
+                s_need = need - before;
+            }
+        }
+        mask |= 255u << shift;
+        __syncthreads();
+    }
+    const uint32_t thr = s_prefix;
+    const int take_eq = s_need;  // keys equal to thr to keep: the lowest indices
+
+    // keep j iff key > thr, or key == thr among the first take_eq such indices
+    const int per = (C + kSelThreads - 1) / kSelThreads;
+    const int j0 = min(C, tid * per), j1 = min(C, j0 + per);
+    int my_eq = 0;
+    for (int j = j0; j < j1; ++j)
+        my_eq += sKey[j] == thr;
+    int total;
+    int eq_before = block_excl_scan<kSelThreads>(my_eq, s_scan, total);
+    int my_keep = 0;
+    {
+        int e = eq_before;
+        for (int j = j0; j < j1; ++j) {
+            const uint32_t k = sKey[j];
+            my_keep += k > thr || (k == thr && e++ < take_eq);
+        }
+    }
+    int pos = block_excl_scan<kSelThreads>(my_keep, s_scan, total);
+    int32_t *kept = a.kept + (size_t)u * KT;
+    {
+        int e = eq_before;
+        for (int j = j0; j < j1; ++j) {
+            const uint32_t k = sKey[j];
+            if (k > thr || (k == thr && e++ < take_eq)) {
+                if (pos < keep)  // holds by construction; guards the neighbour's slice
+                    kept[pos] = j;
+                ++pos;
+            }
+        }
+    }
+    for (int i = tid; i < a.w; i += kSelThreads)
+        kept[keep + i] = C + i;
+    if (tid == 0 && total != keep)
+        set_error(a.sticky, ZP_ERR_DEVICE_CHECK);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kCmpThreads) zp_prefill_compact_kernel(const PrefillArgs a)
+{
+    constexpr int VPR = D / 8;                                  // 16-byte vectors per row
+    constexpr int ITEMS = kCmpRows * VPR * 2 / kCmpThreads;     // K and V
+    if (*(volatile int32_t *)a.call != 0)
+        return;
+    const int u = blockIdx.x;
+    const int h = u % a.Hkv, r = (u / a.Hkv) % a.R, l = u / (a.Hkv * a.R);
+    const int row = a.req_idx ? a.req_idx[r] : r;
+    const int T = a.lengths[row];
+    const int KT = (a.N - 1) * kBlk;
+    const int32_t *kept = a.kept + (size_t)u * KT;
+    const int32_t *trow = a.tables + (size_t)row * a.stride;
+    const int32_t *drow = a.dst_table + (size_t)r * a.stride;
+    uint4 *pools[2] = {static_cast<uint4 *>(a.kpools[l]), static_cast<uint4 *>(a.vpools[l])};
+    for (int c0 = 0; c0 < KT; c0 += kCmpRows) {
+        const int n = min(kCmpRows, KT - c0);
+        uint4 buf[ITEMS];
+        size_t dst_off[ITEMS];
+        bool moved[ITEMS];
+#pragma unroll
+        for (int it = 0; it < ITEMS; ++it) {
+            const int v = threadIdx.x + it * kCmpThreads;
+            const int kv = v / (kCmpRows * VPR);
+            const int rem = v - kv * kCmpRows * VPR;
+            const int jj = rem / VPR, ch = rem - jj * VPR;
+            moved[it] = false;
+            if (jj < n) {
+                const int j = c0 + jj, src = kept[j];
+                if (src < j || src >= T) {  // kept[j] >= j holds for any valid selection
+                    if (ch == 0 && kv == 0)
+                        set_error(a.sticky, ZP_ERR_DEVICE_CHECK);
+                    continue;
+                }
+                const int sblk = trow[src / kBlk], dblk = drow[j / kBlk];
+                if (sblk != dblk || src % kBlk != j % kBlk) {
+                    moved[it] = true;
+                    buf[it] = ld_global_nc_v4(
+                        pools[kv] + (((size_t)sblk * a.Hkv + h) * kBlk + src % kBlk) * VPR + ch);
+                    dst_off[it] = (((size_t)dblk * a.Hkv + h) * kBlk + j % kBlk) * VPR + ch;
+                }
+            }
+        }
+        __syncthreads();  // every source row of the chunk read before any write
+#pragma unroll
+        for (int it = 0; it < ITEMS; ++it) {
+            const int v = threadIdx.x + it * kCmpThreads;
+            const int kv = v / (kCmpRows * VPR);
+            if (moved[it])
+                pools[kv][dst_off[it]] = buf[it];
+        }
+    }
+}
+
+template <int D, int MT>
+static cudaError_t launch_passes(const PrefillArgs &a, int units, cudaStream_t s)
+{
+    using S = PrefillSmem<D, MT>;
+    auto k1 = zp_prefill_pass_kernel<D, MT, false>;
+    auto k2 = zp_prefill_pass_kernel<D, MT, true>;
+    cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
+    if (e != cudaSuccess)
+        return e;
+    const dim3 grid(static_cast<unsigned>(units), static_cast<unsigned>(a.NC));
+    k1<<<grid, kPThreads, S::ALLOC, s>>>(a);
+    k2<<<grid, kPThreads, S::ALLOC, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_for_d(const PrefillArgs &a, int mt, int units, cudaStream_t s)
+{
+    cudaError_t e = mt == 1   ? launch_passes<D, 1>(a, units, s)
+                    : mt == 2 ? launch_passes<D, 2>(a, units, s)
+                              : launch_passes<D, 4>(a, units, s);
+    if (e != cudaSuccess)
+        return e;
+    const int sel_smem = a.T_cap * 4;
+    e = cudaFuncSetAttribute(zp_prefill_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             sel_smem);
+    if (e != cudaSuccess)
+        return e;
+    zp_prefill_select_kernel<<<static_cast<unsigned>(units), kSelThreads, sel_smem, s>>>(a);
+    zp_prefill_compact_kernel<D><<<static_cast<unsigned>(units), kCmpThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const PrefillArgs &a, int d, int mt, int units, cudaStream_t s)
+{
+    if (d == 64)
+        return launch_for_d<64>(a, mt, units, s);
+    if (d == 128)
+        return launch_for_d<128>(a, mt, units, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace zp

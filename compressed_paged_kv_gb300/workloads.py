@@ -349,6 +349,63 @@ def fork_cache(seed: int, R: int, n_max: int, L: int = 2, Hkv: int = 2, d: int =
                 v_pools=v_pools, num_blocks=num_blocks, b=b, n_max=n_max, L=L, Hkv=Hkv, d=d)
 
 
+def prefill_cache(seed: int, lens, n_max: int, L: int = 2, Hkv: int = 2, Hq: int = 8,
+                  d: int = 128, w: int = 8, group: int = 1, prefix_blocks: int = 0,
+                  spare: int = 64, b: int = 16, device="cpu") -> dict:
+    """Requests admitted with prompts longer than the budget.
+
+    Request r holds lens[r] tokens (any count, the last block possibly
+    partial) in a seeded permutation of physical blocks; consecutive groups of
+    `group` requests share their first `prefix_blocks` blocks (one prompt
+    prefix); table entries past a request's blocks are -1; the rest of the
+    pool plus `spare` blocks form the free stack.  K/V pools
+    [num_blocks][Hkv][b][d] and window queries [L][R][Hq][w][d] are N(0,1)
+    rounded to bf16 (slots past a request's length hold draws too).
+
+    Returns dict of torch tensors on `device` (tables, lengths, refcount,
+    free_ids, free_count, k_pools, v_pools, window_q) and the sizes.
+    """
+    R = len(lens)
+    nblk = [-(-int(T) // b) for T in lens]
+    stride = max(max(nblk), n_max)
+    g = _gen("cpu", derive_seed(seed, TENSOR_TABLE))
+    n_groups = -(-R // group)
+    pb = prefix_blocks if group > 1 else 0
+    used = sum(nblk) - (R - n_groups) * pb
+    num_blocks = used + spare
+    phys = torch.randperm(num_blocks, generator=g).to(torch.int32)
+    tables = torch.full((R, stride), -1, dtype=torch.int32)
+    nxt = 0
+    for gi in range(n_groups):
+        members = range(gi * group, min((gi + 1) * group, R))
+        shared = phys[nxt:nxt + pb]
+        nxt += pb
+        for r in members:
+            assert nblk[r] >= pb
+            tables[r, :pb] = shared
+            tables[r, pb:nblk[r]] = phys[nxt:nxt + nblk[r] - pb]
+            nxt += nblk[r] - pb
+    assert nxt == used
+    refcount = torch.zeros(num_blocks, dtype=torch.int32)
+    ids = tables[tables >= 0].long()
+    refcount.index_add_(0, ids, torch.ones_like(ids, dtype=torch.int32))
+    free_ids = torch.full((num_blocks,), -1, dtype=torch.int32)
+    free_ids[:num_blocks - used] = phys[used:]
+    shape = (num_blocks, Hkv, b, d)
+    k_pools = [_normal(shape, device, derive_seed(seed, TENSOR_K, l)).to(torch.bfloat16)
+               for l in range(L)]
+    v_pools = [_normal(shape, device, derive_seed(seed, TENSOR_V, l)).to(torch.bfloat16)
+               for l in range(L)]
+    window_q = torch.stack([_normal((R, Hq, w, d), device, derive_seed(seed, TENSOR_Q, l))
+                            for l in range(L)]).to(torch.bfloat16)
+    i32 = dict(dtype=torch.int32, device=device)
+    return dict(tables=tables.to(device), lengths=torch.tensor([int(T) for T in lens], **i32),
+                refcount=refcount.to(device), free_ids=free_ids.to(device),
+                free_count=torch.tensor([num_blocks - used], **i32), k_pools=k_pools,
+                v_pools=v_pools, window_q=window_q, num_blocks=num_blocks, stride=stride,
+                n_max=n_max, L=L, Hkv=Hkv, Hq=Hq, d=d, w=w, b=b)
+
+
 def bf16_bits(t: torch.Tensor):
     """Raw uint16 bit patterns of a bf16 tensor, as a host numpy array."""
     import numpy as np

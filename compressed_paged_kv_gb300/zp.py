@@ -5,6 +5,7 @@ every call raises.
 
 The functions keep the C names (``zp_cache_create``, ``zp_compress``,
 ``zp_paged_decode_attn``, ``zp_append_slots``, ``zp_append_kv``,
+``zp_compress_prefill``, ``zp_compress_prefill_workspace_size``,
 ``zp_cache_status``, ``zp_cache_destroy``, ``zp_status_string``) and take raw integers (device pointers, a cudaStream_t
 as an int).  ``Cache`` wraps them for torch tensors: it reads ``data_ptr()``
 and the current stream, and keeps the pool tensors alive.
@@ -81,6 +82,13 @@ def lib():
         L.zp_append_slots.restype = I32
         L.zp_append_kv.argtypes = [P, I32, P, P, P, I32, I32, P, P, I32, P]
         L.zp_append_kv.restype = I32
+        L.zp_compress_prefill_workspace_size.argtypes = [P, I32, I32,
+                                                         ctypes.POINTER(ctypes.c_size_t)]
+        L.zp_compress_prefill_workspace_size.restype = I32
+        L.zp_compress_prefill.argtypes = [P, P, I32, I32, P, P, I32, P, I32, I32, ctypes.c_float,
+                                          ctypes.POINTER(zp_block_pool), P, ctypes.c_size_t, P,
+                                          P, P]
+        L.zp_compress_prefill.restype = I32
         L.zp_cache_status.argtypes = [P, P, ctypes.POINTER(I32)]
         L.zp_cache_status.restype = I32
         L.zp_status_string.argtypes = [I32]
@@ -118,6 +126,24 @@ def zp_compress(handle, block_tables, bt_stride, num_rows, lengths, req_idx, R, 
                              P(req_idx or None), R, P(window_q), n_max, window, float(lam),
                              ctypes.byref(pool), P(stream or None), P(scores_out or None),
                              P(kept_out or None))
+
+
+def zp_compress_prefill_workspace_size(handle, R, bt_stride) -> int:
+    n = ctypes.c_size_t(0)
+    st = lib().zp_compress_prefill_workspace_size(P(handle), R, bt_stride, ctypes.byref(n))
+    if st != OK:
+        raise ZpError(st, "zp_compress_prefill_workspace_size")
+    return n.value
+
+
+def zp_compress_prefill(handle, block_tables, bt_stride, num_rows, lengths, req_idx, R, window_q,
+                        n_max, window, lam, pool: zp_block_pool, workspace, workspace_bytes,
+                        stream, scores_out=0, kept_out=0) -> int:
+    return lib().zp_compress_prefill(P(handle), P(block_tables), bt_stride, num_rows,
+                                     P(lengths), P(req_idx or None), R, P(window_q), n_max,
+                                     window, float(lam), ctypes.byref(pool), P(workspace or None),
+                                     workspace_bytes, P(stream or None), P(scores_out or None),
+                                     P(kept_out or None))
 
 
 def zp_paged_decode_attn(handle, layer, q, block_tables, bt_stride, num_rows, lengths, req_idx,
@@ -214,6 +240,26 @@ class Cache:
         if check and st != OK:
             raise ZpError(st, "zp_compress")
         return st
+
+    def compress_prefill(self, block_tables, lengths, window_q, n_max, window, lam, free_ids,
+                         free_count, refcount, workspace, req_idx=None, scores_out=None,
+                         kept_out=None, stream=None, check=True):
+        """``workspace``: a uint8 CUDA tensor of at least
+        ``prefill_workspace_bytes(R, block_tables.shape[1])`` bytes."""
+        pool = zp_block_pool(free_ids.data_ptr(), free_count.data_ptr(), refcount.data_ptr(),
+                             free_ids.numel())
+        R = window_q.shape[1]
+        st = zp_compress_prefill(self.handle, block_tables.data_ptr(), block_tables.shape[1],
+                                 block_tables.shape[0], lengths.data_ptr(), _ptr(req_idx), R,
+                                 window_q.data_ptr(), n_max, window, lam, pool,
+                                 workspace.data_ptr(), workspace.numel(), _stream(stream),
+                                 _ptr(scores_out), _ptr(kept_out))
+        if check and st != OK:
+            raise ZpError(st, "zp_compress_prefill")
+        return st
+
+    def prefill_workspace_bytes(self, R, bt_stride) -> int:
+        return zp_compress_prefill_workspace_size(self.handle, R, bt_stride)
 
     def decode(self, layer, q, block_tables, lengths, scale, out, req_idx=None, stream=None,
                check=True):

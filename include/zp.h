@@ -25,8 +25,8 @@
  *  - A handle serves at most one call of each entry point in flight at a
  *    time.  zp_compress may run concurrently with zp_paged_decode_attn and
  *    zp_append_kv on another stream when they touch disjoint requests.
- *    zp_compress and zp_append_slots both change the free stack and
- *    refcounts: order them (one stream, or events).  More concurrency needs
+ *    zp_compress, zp_compress_prefill and zp_append_slots change the free
+ *    stack and refcounts: order them (one stream, or events).  More concurrency needs
  *    more handles.
  *
  * KV pool layout (one K pool and one V pool per layer, caller-owned):
@@ -39,6 +39,7 @@
 #ifndef ZP_H
 #define ZP_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -149,6 +150,52 @@ zp_status zp_compress(zp_cache *cache, int32_t *block_tables, int32_t bt_stride,
                       const void *window_q, int32_t n_max, int32_t window, float lambda,
                       const zp_block_pool *pool, void *stream, float *scores_out,
                       int32_t *kept_out);
+
+/* Bytes of caller workspace zp_compress_prefill needs for R requests and a
+ * table stride of bt_stride blocks (the upper bound of every request's
+ * length).  Host only; no CUDA call. */
+zp_status zp_compress_prefill_workspace_size(const zp_cache *cache, int32_t R, int32_t bt_stride,
+                                             size_t *bytes);
+
+/* Compression at admission of requests longer than the budget (Dutch summary
+ * "Methodologie" §1: the kept entries move into the first n_max-1 blocks, the
+ * n_max-th block is reserved for decoding, and the excess blocks are
+ * released; §3: shared blocks compress into fresh target blocks).  Request i
+ * (row = req_idx[i], or i) holds T_i = lengths[row] tokens, n_max*16 <= T_i
+ * <= bt_stride*16, in blocks 0 .. ceil(T_i/16)-1 of its table row (the last
+ * possibly partial).  Per (request, layer, kv head), with C_i = T_i - window:
+ *   scores as in zp_compress over the T_i keys (the window is the last
+ *   `window` tokens; the redundancy of a key in a partial last block is its
+ *   mean cosine to the other filled slots of that block, 0 if alone);
+ *   keep the (n_max-1)*16 - window best candidates (ties to the lower index)
+ *   and the window, in original order, in blocks 0 .. n_max-2;
+ *   blocks 0 .. n_max-1: destinations by the rule of zp_compress (refcount 1
+ *   at call start: rewritten in place / kept as the reserved block; > 1: a
+ *   fresh target popped from the free stack, one reference dropped);
+ *   blocks n_max .. ceil(T_i/16)-1: one reference dropped each, pushed on the
+ *   free stack (after the pops, in request-then-block order) when that
+ *   empties it, table entry set to -1.
+ * Afterwards lengths are (n_max-1)*16.
+ *
+ *  block_tables, lengths, req_idx, pool  as in zp_compress (lengths as above)
+ *  window_q      device bf16 [L][R][Hq][window][d] (the last `window` tokens)
+ *  bt_stride     at most max_blocks_per_req of the handle, and bt_stride * 16
+ *                <= 32768 (ZP_ERR_UNSUPPORTED beyond)
+ *  workspace     device, 256-byte aligned, at least the bytes
+ *                zp_compress_prefill_workspace_size reports; caller-owned,
+ *                only used during the call's kernels
+ *  scores_out    NULL or device fp32 [L][R][Hkv][bt_stride*16]: candidate
+ *                scores, +inf at window positions, entries at T_i and beyond
+ *                not written
+ *  kept_out      NULL or device int32 [L][R][Hkv][(n_max-1)*16], ascending
+ * All-or-nothing like zp_compress.  Orders with zp_compress and
+ * zp_append_slots (all three change the free stack and refcounts). */
+zp_status zp_compress_prefill(zp_cache *cache, int32_t *block_tables, int32_t bt_stride,
+                              int32_t num_rows, int32_t *lengths, const int32_t *req_idx,
+                              int32_t R, const void *window_q, int32_t n_max, int32_t window,
+                              float lambda, const zp_block_pool *pool, void *workspace,
+                              size_t workspace_bytes, void *stream, float *scores_out,
+                              int32_t *kept_out);
 
 /* Paged decode attention over the block tables of one layer ("Paged KV cache
  * and continuous batching for LLMs", "How it works"): for request i and query
