@@ -163,7 +163,7 @@ struct AppendKvArgs {
 cudaError_t launch_append_slots(const AppendArgs &a, cudaStream_t s);
 // Scoring, selection and compaction of a compression at admission.
 cudaError_t launch_prefill(const PrefillArgs &a, int d, int mt, int units, cudaStream_t s);
-constexpr int kPrefillChunk = 512;      // tokens per scoring CTA
+constexpr int kPrefillChunk = 2048;     // tokens per scoring CTA
 constexpr int kPrefillMaxTokens = 32768;  // scores of one unit fit in shared memory
 cudaError_t launch_append_kv(const AppendKvArgs &a, cudaStream_t s);
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);

@@ -10,8 +10,8 @@
 // a number that varies per request and can be most of the request.
 //
 // Launches, between the shared plan and finalize kernels (zp_compress.cu):
-//   zp_prefill_pass_kernel<.., false>  grid (unit, chunk of 512 tokens), four
-//       warps each streaming their blocks through a private three-stage TMA
+//   zp_prefill_pass_kernel<.., false>  grid (unit, chunk of 2048 tokens), four
+//       warps each streaming their blocks through a private two-stage TMA
 //       ring: window logits and the Gram of each block on mma.sync, the
 //       chunk's softmax statistics of every window row, the redundancy of
 //       every key (over the filled slots of its block) -> workspace.
@@ -23,22 +23,23 @@
 //       threshold go to the lower index; the kept positions in ascending
 //       order by block scans, then the window.
 //   zp_prefill_compact_kernel  one CTA per unit: destination rows in
-//       ascending chunks of 64; a chunk's source rows are read before any of
+//       ascending chunks of 32; a chunk's source rows are read before any of
 //       its writes (one barrier), and every later chunk reads sources at or
 //       after its own first destination (kept[j] >= j), which no earlier
-//       chunk wrote -- so compacting in place is safe.
+//       chunk writes -- so compacting in place is safe, and the next chunk's
+//       rows can be loaded while this chunk's are stored.
 #include "zp_internal.cuh"
 
 namespace zp {
 
 constexpr int kPW = 4;                       // warps of a scoring CTA
 constexpr int kPThreads = kPW * 32;
-constexpr int kPStages = 3;                  // TMA stages per warp
+constexpr int kPStages = 2;                  // TMA stages per warp
 constexpr int kPChunk = kPrefillChunk;       // tokens per scoring CTA
 constexpr int kPBlocks = kPChunk / kBlk;
 constexpr int kSelThreads = 1024;
 constexpr int kCmpThreads = 256;
-constexpr int kCmpRows = 64;                 // destination rows per compaction chunk
+constexpr int kCmpRows = 32;                 // destination rows per compaction chunk
 
 template <int D, int MT>
 struct PrefillSmem {
@@ -213,7 +214,9 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
             issue(i + kPStages);
         }
         // base-2 logits; window row of slot i sees keys up to C + i, which
-        // also hides the unfilled slots of a partial last block
+        // also hides the unfilled slots of a partial last block (only blocks
+        // reaching past C hold such keys)
+        const bool masked_block = key0 + kBlk - 1 > C;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -221,10 +224,12 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float v = acc[mt][nt][e] * a.logit_scale;
-                    const int slot = slot_of[mt][e >> 1];
-                    const int tok = key0 + nt * 8 + (lane & 3) * 2 + (e & 1);
-                    if (slot >= 0 ? tok > C + slot : tok >= T)
-                        v = -INFINITY;
+                    if (masked_block) {
+                        const int slot = slot_of[mt][e >> 1];
+                        const int tok = key0 + nt * 8 + (lane & 3) * 2 + (e & 1);
+                        if (slot >= 0 ? tok > C + slot : tok >= T)
+                            v = -INFINITY;
+                    }
                     acc[mt][nt][e] = v;
                 }
 
@@ -467,42 +472,54 @@ __global__ void __launch_bounds__(kCmpThreads) zp_prefill_compact_kernel(const P
     const int32_t *trow = a.tables + (size_t)row * a.stride;
     const int32_t *drow = a.dst_table + (size_t)r * a.stride;
     uint4 *pools[2] = {static_cast<uint4 *>(a.kpools[l]), static_cast<uint4 *>(a.vpools[l])};
-    for (int c0 = 0; c0 < KT; c0 += kCmpRows) {
+
+    // item `it` of a chunk: vector ch of row c0 + jj of K (kv 0) or V (kv 1)
+    struct Chunk {
+        uint4 v[ITEMS];
+        uint32_t dst[ITEMS];  // vector index into the pool, or ~0u: nothing to move
+    };
+    auto load = [&](int c0, Chunk &ck) {
         const int n = min(kCmpRows, KT - c0);
-        uint4 buf[ITEMS];
-        size_t dst_off[ITEMS];
-        bool moved[ITEMS];
 #pragma unroll
         for (int it = 0; it < ITEMS; ++it) {
             const int v = threadIdx.x + it * kCmpThreads;
             const int kv = v / (kCmpRows * VPR);
             const int rem = v - kv * kCmpRows * VPR;
             const int jj = rem / VPR, ch = rem - jj * VPR;
-            moved[it] = false;
-            if (jj < n) {
-                const int j = c0 + jj, src = kept[j];
-                if (src < j || src >= T) {  // kept[j] >= j holds for any valid selection
-                    if (ch == 0 && kv == 0)
-                        set_error(a.sticky, ZP_ERR_DEVICE_CHECK);
-                    continue;
-                }
-                const int sblk = trow[src / kBlk], dblk = drow[j / kBlk];
-                if (sblk != dblk || src % kBlk != j % kBlk) {
-                    moved[it] = true;
-                    buf[it] = ld_global_nc_v4(
-                        pools[kv] + (((size_t)sblk * a.Hkv + h) * kBlk + src % kBlk) * VPR + ch);
-                    dst_off[it] = (((size_t)dblk * a.Hkv + h) * kBlk + j % kBlk) * VPR + ch;
-                }
+            ck.dst[it] = ~0u;
+            if (jj >= n)
+                continue;
+            const int j = c0 + jj, src = kept[j];
+            if (src < j || src >= T) {  // kept[j] >= j holds for any valid selection
+                if (ch == 0 && kv == 0)
+                    set_error(a.sticky, ZP_ERR_DEVICE_CHECK);
+                continue;
             }
+            const int sblk = trow[src / kBlk], dblk = drow[j / kBlk];
+            if (sblk == dblk && src % kBlk == j % kBlk)
+                continue;  // already in place
+            ck.v[it] = ld_global_nc_v4(pools[kv] +
+                                       (((size_t)sblk * a.Hkv + h) * kBlk + src % kBlk) * VPR + ch);
+            ck.dst[it] = static_cast<uint32_t>((((size_t)dblk * a.Hkv + h) * kBlk + j % kBlk) * VPR +
+                                               ch);
         }
-        __syncthreads();  // every source row of the chunk read before any write
+    };
+    auto store = [&](const Chunk &ck) {
 #pragma unroll
         for (int it = 0; it < ITEMS; ++it) {
-            const int v = threadIdx.x + it * kCmpThreads;
-            const int kv = v / (kCmpRows * VPR);
-            if (moved[it])
-                pools[kv][dst_off[it]] = buf[it];
+            const int kv = (threadIdx.x + it * kCmpThreads) / (kCmpRows * VPR);
+            if (ck.dst[it] != ~0u)
+                pools[kv][ck.dst[it]] = ck.v[it];
         }
+    };
+    Chunk cur, nxt;
+    load(0, cur);
+    for (int c0 = 0; c0 < KT; c0 += kCmpRows) {
+        __syncthreads();  // every source row of this chunk read before any of its writes
+        if (c0 + kCmpRows < KT)
+            load(c0 + kCmpRows, nxt);  // sources past this chunk: none written by it
+        store(cur);
+        cur = nxt;
     }
 }
 
