@@ -78,7 +78,6 @@ def kernel_source_digest():
     from compressed_paged_kv_gb300 import _build
     h = hashlib.sha256()
     paths = [os.path.join(_build.CSRC, n) for n in COMPRESS_KERNEL_SOURCES]
-    paths.append(os.path.join(os.path.dirname(os.path.abspath(__file__)), "include", "zp.h"))
     for path in paths:
         with open(path, "rb") as f:
             h.update(os.path.basename(path).encode())
