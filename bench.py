@@ -48,6 +48,8 @@ def parse_args():
     p.add_argument("--workload", default="qwen3_1l")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--prefill-layers", type=int, default=None,
+                   help="layers of the prefill8k workload (default: the model's 36)")
     return p.parse_args()
 
 
@@ -352,7 +354,9 @@ def run_prefill(args, world, rank, local):
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    P = PREFILL
+    P = dict(PREFILL)
+    if args.prefill_layers:
+        P["L"] = args.prefill_layers
     g = torch.Generator()
     g.manual_seed(P["seed"] + rank)
     lens = torch.randint(P["len_lo"], P["len_hi"] + 1, (P["R"],), generator=g).tolist()
