@@ -66,6 +66,8 @@ def _declare(lib):
     lib.zpo_importance.restype = None
     lib.zpo_redundancy.argtypes = [P, I, I, I, P]
     lib.zpo_redundancy.restype = None
+    lib.zpo_redundancy_global.argtypes = [P, I, I, P]
+    lib.zpo_redundancy_global.restype = None
     lib.zpo_unit_scores.argtypes = [P, P, I, I, I, I, I, D, P, P, P]
     lib.zpo_unit_scores.restype = None
     lib.zpo_select.argtypes = [P, I, I, I, P]
@@ -148,6 +150,14 @@ class Oracle:
         T, d = K.shape
         red = np.zeros(T, dtype=np.float64)
         self.lib.zpo_redundancy(_p(K), T, d, b, _p(red))
+        return red
+
+    def redundancy_global(self, K):
+        """Mean cosine of each key to every other key of the unit (O(T^2 d))."""
+        K = _c(K, np.uint16)
+        T, d = K.shape
+        red = np.zeros(T, dtype=np.float64)
+        self.lib.zpo_redundancy_global(_p(K), T, d, _p(red))
         return red
 
     def unit_scores(self, K, Q, b, w, G, lam):

@@ -178,6 +178,29 @@ void zpo_redundancy(const uint16_t *K, int T, int d, int b, double *red)
     free(norm);
 }
 
+/* Redundancy over ALL keys of a unit: the O(N^2*b^2) score that the
+ * Lightning Redundancy Score replaces [ZP-nl Methodologie §5; ZP-ko 방법론 E],
+ * read with this library's definition (mean cosine similarity to the other
+ * keys), the comparison set being every other key of the unit instead of
+ * its block: red[j] = (1/(T-1)) * sum_{k != j} cos(K_j, K_k), a zero-norm
+ * key having cosine 0 with every key.  Written pair by pair, O(T^2 d). */
+void zpo_redundancy_global(const uint16_t *K, int T, int d, double *red)
+{
+    double *norm = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    for (int j = 0; j < T; ++j)
+        norm[j] = sqrt(dot_bf16(K + (size_t)j * d, K + (size_t)j * d, d));
+    for (int j = 0; j < T; ++j) {
+        double sum = 0.0;
+        for (int k = 0; k < T; ++k) {
+            if (k == j || norm[j] == 0.0 || norm[k] == 0.0)
+                continue;
+            sum += dot_bf16(K + (size_t)j * d, K + (size_t)k * d, d) / (norm[j] * norm[k]);
+        }
+        red[j] = T > 1 ? sum / (double)(T - 1) : 0.0;
+    }
+    free(norm);
+}
+
 /* score[j] = imp[j] - lambda * red[j] for the C candidates. */
 void zpo_unit_scores(const uint16_t *K, const uint16_t *Q, int T, int d, int b, int w, int G,
                      double lambda, double *imp, double *red, double *score)

@@ -203,6 +203,39 @@ def pin_redundancy_block_locality(orc):
 
 # -------------------------------------------------------------------- score
 
+def pin_redundancy_global_one_block_is_lrs(orc):
+    """With a single block (T = b) the global redundancy is the Lightning
+    Redundancy Score; partial blocks too (T < b)."""
+    g = rng(160)
+    for T in (16, 9):
+        K = bf16(g.standard_normal((T, 8)))
+        close(orc.redundancy_global(K), orc.redundancy(K, 16), 1e-12, "one block")
+
+
+def pin_redundancy_global_closed_forms(orc):
+    """Identical keys: 1; mutually orthogonal keys: 0; m copies of u and m of
+    -u: (m - 1 - m)/(2m - 1) = -1/(2m - 1); a zero key: 0 for it, and it
+    counts as a cosine of 0 for the others."""
+    u = np.ones(4)
+    close(orc.redundancy_global(bf16(np.tile(u, (7, 1)))), np.ones(7), 1e-12, "identical")
+    close(orc.redundancy_global(bf16(np.eye(6))), np.zeros(6), 1e-12, "orthogonal")
+    m = 3
+    K = bf16(np.vstack([np.tile(u, (m, 1)), np.tile(-u, (m, 1))]))
+    close(orc.redundancy_global(K), np.full(2 * m, -1.0 / (2 * m - 1)), 1e-12, "+-u")
+    K = bf16(np.vstack([np.tile(u, (3, 1)), np.zeros((1, 4))]))
+    close(orc.redundancy_global(K), [2 / 3, 2 / 3, 2 / 3, 0.0], 1e-12, "zero key")
+
+
+def pin_redundancy_global_torch(orc):
+    """Against torch fp64: the mean of each row of the cosine-similarity
+    matrix without its diagonal."""
+    K = bf16(rng(161).standard_normal((70, 16)))
+    Kd = torch.tensor(widen(K))
+    cos = torch.nn.functional.cosine_similarity(Kd[:, None, :], Kd[None, :, :], dim=-1)
+    cos.fill_diagonal_(0.0)
+    close(orc.redundancy_global(K), (cos.sum(dim=1) / 69).numpy(), 1e-12, "torch")
+
+
 def pin_score_lambda_zero_is_importance(orc):
     T, d, b, w, G = 64, 16, 8, 4, 2
     K = bf16(rng(50).standard_normal((T, d)))

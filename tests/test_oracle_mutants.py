@@ -83,6 +83,11 @@ MUTANTS = [
     ("append: new row in the next slot",
      "size_t to = (((size_t)blk * Hkv + h) * b + p % b) * d;",
      "size_t to = (((size_t)blk * Hkv + h) * b + (p + 1) % b) * d;"),
+    ("global redundancy over T", "red[j] = T > 1 ? sum / (double)(T - 1) : 0.0;",
+     "red[j] = T > 1 ? sum / (double)T : 0.0;"),
+    ("global redundancy includes self",
+     "if (k == j || norm[j] == 0.0 || norm[k] == 0.0)\n                continue;",
+     "if (norm[j] == 0.0 || norm[k] == 0.0)\n                continue;"),
     ("length check dropped", "if (lengths[row] != N * b)\n            return ZPO_ERR_INVALID_ARG;",
      ""),
 ]
