@@ -594,9 +594,26 @@ def run_gpu(args, world, rank, local):
     e2e_ms = e2e_ms_total / E
     status2 = cache.status()
 
+    # ablation: the redundancy of every key against all keys of its unit (the
+    # score the block-local one replaces), timed alone on the same units
+    restore()
+    red_all = torch.empty((wl.L, Rc, wl.Hkv, st.block_tables.shape[1] * wl.b), device=dev)
+    abl = []
+    for i in range(6):
+        flush.zero_()
+        e0.record()
+        cache.global_redundancy(st.block_tables, st.lengths, red_all, req_idx=req_idx, R=Rc)
+        e1.record()
+        e1.synchronize()
+        if i >= 2:
+            abl.append(e0.elapsed_time(e1))
+    abl_ms = sum(abl) / len(abl)
+    assert cache.status() == zp.OK
+    del red_all
+
     # max over ranks
-    step_ms, comp_avg, dec_avg, e2e_ms, t_wall = reduce_max(
-        [step_ms, comp_avg, dec_avg, e2e_ms, t_wall], world, dev)
+    step_ms, comp_avg, dec_avg, e2e_ms, t_wall, abl_ms = reduce_max(
+        [step_ms, comp_avg, dec_avg, e2e_ms, t_wall, abl_ms], world, dev)
 
     if rank != 0:
         if world > 1:
@@ -658,6 +675,10 @@ def run_gpu(args, world, rank, local):
                 "ms_per_step": e2e_ms},
         "gpu_launches": K * (3 + wl.L * (1 if cache_splits_one(wl, Rc, cache) else 2)),
         "wall_s_timed_loop": t_wall,
+        "ablation_all_keys_redundancy": {
+            "ms": abl_ms, "gbs": 2 * units * T * row / (abl_ms * 1e-3) / 1e9,
+            "what": "zp_global_redundancy on the same units (two passes over K), outside the "
+                    "timed step"},
         "device_status": [status, status2],
     }
     res["clocks"] = clk.summary()

@@ -5,7 +5,7 @@ every call raises.
 
 The functions keep the C names (``zp_cache_create``, ``zp_compress``,
 ``zp_paged_decode_attn``, ``zp_append_slots``, ``zp_append_kv``,
-``zp_compress_prefill``, ``zp_compress_prefill_workspace_size``,
+``zp_compress_prefill``, ``zp_compress_prefill_workspace_size``, ``zp_global_redundancy``,
 ``zp_cache_status``, ``zp_cache_destroy``, ``zp_status_string``) and take raw integers (device pointers, a cudaStream_t
 as an int).  ``Cache`` wraps them for torch tensors: it reads ``data_ptr()``
 and the current stream, and keeps the pool tensors alive.
@@ -89,6 +89,8 @@ def lib():
                                           ctypes.POINTER(zp_block_pool), P, ctypes.c_size_t, P,
                                           P, P]
         L.zp_compress_prefill.restype = I32
+        L.zp_global_redundancy.argtypes = [P, P, I32, I32, P, P, I32, P, P]
+        L.zp_global_redundancy.restype = I32
         L.zp_cache_status.argtypes = [P, P, ctypes.POINTER(I32)]
         L.zp_cache_status.restype = I32
         L.zp_status_string.argtypes = [I32]
@@ -176,6 +178,13 @@ def zp_append_kv(handle, layer, k_new, v_new, block_tables, bt_stride, num_rows,
                  req_idx, R, stream) -> int:
     return lib().zp_append_kv(P(handle), layer, P(k_new), P(v_new), P(block_tables), bt_stride,
                               num_rows, P(lengths), P(req_idx or None), R, P(stream or None))
+
+
+def zp_global_redundancy(handle, block_tables, bt_stride, num_rows, lengths, req_idx, R, red_out,
+                         stream) -> int:
+    return lib().zp_global_redundancy(P(handle), P(block_tables), bt_stride, num_rows,
+                                      P(lengths), P(req_idx or None), R, P(red_out),
+                                      P(stream or None))
 
 
 def zp_cache_status(handle, stream) -> tuple[int, int]:
@@ -292,6 +301,17 @@ class Cache:
                           lengths.data_ptr(), _ptr(req_idx), k_new.shape[0], _stream(stream))
         if check and st != OK:
             raise ZpError(st, "zp_append_kv")
+        return st
+
+    def global_redundancy(self, block_tables, lengths, red_out, req_idx=None, R=None,
+                          stream=None, check=True):
+        if R is None:
+            R = req_idx.numel() if req_idx is not None else block_tables.shape[0]
+        st = zp_global_redundancy(self.handle, block_tables.data_ptr(), block_tables.shape[1],
+                                  block_tables.shape[0], lengths.data_ptr(), _ptr(req_idx), R,
+                                  red_out.data_ptr(), _stream(stream))
+        if check and st != OK:
+            raise ZpError(st, "zp_global_redundancy")
         return st
 
     def status(self, stream=None) -> int:

@@ -305,6 +305,25 @@ zp_status zp_append_kv(zp_cache *cache, int32_t layer, const void *k_new, const 
                        const int32_t *block_tables, int32_t bt_stride, int32_t num_rows,
                        const int32_t *lengths, const int32_t *req_idx, int32_t R, void *stream);
 
+/* Redundancy of every key against ALL keys of its (request, layer, kv
+ * head): the O(N^2 b^2) score that the Lightning Redundancy Score replaces
+ * (Dutch summary "Methodologie" §5, Korean "방법론" E), computed for
+ * comparison; the compression calls never use it.  With this library's
+ * definition, red[t] = mean over the other keys k of the unit of
+ * cos(K_t, K_k) (a zero key has cosine 0 with every key), over the
+ * T_i = lengths[row] cached tokens of request i (row = req_idx[i], or i).
+ * Computed as (K_t/|K_t| . S - 1) / (T_i - 1) with S the sum of the unit's
+ * normalised nonzero keys: two passes over the keys, O(T d).
+ *
+ *  block_tables, lengths, req_idx  as in zp_paged_decode_attn (read only)
+ *  red_out       device fp32 [L][R][Hkv][bt_stride*16]; entries at T_i and
+ *                beyond are not written
+ * A row, length or block id out of range is recorded as ZP_ERR_DEVICE_CHECK
+ * (ZP_ERR_INVALID_ARG for a row) in the sticky status. */
+zp_status zp_global_redundancy(zp_cache *cache, const int32_t *block_tables, int32_t bt_stride,
+                               int32_t num_rows, const int32_t *lengths, const int32_t *req_idx,
+                               int32_t R, float *red_out, void *stream);
+
 /* Synchronises `stream`, returns the handle's sticky device status in
  * *out_status (ZP_OK or the first device-detected error since the last
  * read) and clears it.  Returns ZP_ERR_CUDA if the stream reports an error. */

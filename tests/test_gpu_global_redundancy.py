@@ -1,0 +1,62 @@
+"""GPU parity of the all-keys redundancy ablation (zp_global_redundancy)
+against the oracle's pair-by-pair definition: per unit, |r_gpu - r_orc| <=
+1e-4 * max(|r_orc|, mean |r_orc|) (fp32 sums of normalised keys against fp64
+pairwise cosines)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from compressed_paged_kv_gb300 import workloads as W
+from compressed_paged_kv_gb300 import zp
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+RTOL = 1e-4
+
+
+def gather(pool, table_row, T, h):
+    n = -(-T // 16)
+    x = pool[table_row[:n].long(), h]
+    return W.bf16_bits(x.reshape(n * 16, -1)[:T])
+
+
+@pytest.mark.parametrize("lens,d", [([2048, 1000, 17, 16, 1, 300], 128), ([700, 64, 5], 64)])
+def test_global_redundancy_matches_pairwise(orc, lens, d):
+    c = W.prefill_cache(500 + d, lens, 8, L=2, Hkv=2, Hq=4, d=d, w=4, device=DEV)
+    # a few zero keys: cosine 0 with everything, redundancy 0
+    c["k_pools"][0][c["tables"][1, 0], 0, 3] = 0
+    c["k_pools"][1][c["tables"][0, 2], 1, 0] = 0
+    cache = zp.Cache(c["k_pools"], c["v_pools"], c["Hq"], max_requests=len(lens),
+                     max_blocks_per_req=c["stride"])
+    red = torch.full((2, len(lens), 2, c["stride"] * 16), float("nan"), device=DEV)
+    cache.global_redundancy(c["tables"], c["lengths"], red)
+    assert cache.status() == zp.OK
+    got = red.cpu().numpy()
+    worst = 0.0
+    for l in range(2):
+        for r, T in enumerate(lens):
+            for h in range(2):
+                K = gather(c["k_pools"][l], c["tables"][r], T, h)
+                want = orc.redundancy_global(K)
+                g = got[l, r, h, :T].astype(np.float64)
+                scale = max(float(np.mean(np.abs(want))), 1e-30)
+                err = np.abs(g - want) / np.maximum(np.abs(want), scale)
+                worst = max(worst, float(err.max()))
+                assert np.all(np.isnan(got[l, r, h, T:])), "written past the length"
+                if T <= 16:  # one block: the block-local score
+                    assert np.allclose(want, orc.redundancy(K, 16), atol=1e-12)
+    print(f"[parity] global redundancy: max rel err {worst:.2e}")
+    assert worst <= RTOL
+
+
+def test_global_redundancy_bad_length_is_flagged():
+    c = W.prefill_cache(510, [100], 8, L=1, Hkv=2, Hq=2, d=64, w=1, device=DEV)
+    c["lengths"][0] = c["stride"] * 16 + 1
+    cache = zp.Cache(c["k_pools"], c["v_pools"], 2, max_requests=1, max_blocks_per_req=c["stride"])
+    red = torch.zeros(1, 1, 2, c["stride"] * 16, device=DEV)
+    cache.global_redundancy(c["tables"], c["lengths"], red)
+    assert cache.status() == zp.ERR_DEVICE_CHECK
+    assert torch.count_nonzero(red) == 0
