@@ -88,6 +88,10 @@ def _declare(lib):
     lib.zpo_compress_prefill.argtypes = [I, I, I, I, I, I, P, P, P, P, P, I, P, P, I, I, P, I, I,
                                          D, P, P, P, P, P, I]
     lib.zpo_compress_prefill.restype = I
+    lib.zpo_alloc_rows.argtypes = [P, I, I, P, P, I, P, I, I, P, P, P, I]
+    lib.zpo_alloc_rows.restype = I
+    lib.zpo_release_rows.argtypes = [P, I, I, P, P, I, I, P, P, P, I]
+    lib.zpo_release_rows.restype = I
     lib.zpo_append_slots.argtypes = [I, I, I, I, I, P, P, P, I, I, P, P, I, I, P, P, P, I, P, P]
     lib.zpo_append_slots.restype = I
     lib.zpo_append_kv.argtypes = [I, I, I, I, P, P, P, I, I, P, P, I, P, P]
@@ -371,3 +375,43 @@ class Oracle:
                                     stride, num_rows, _p(lengths), _p(req_idx), R, _p(k_new),
                                     _p(v_new))
         return st, kpool, vpool
+
+    # -- whole-request allocation and release ---------------------------------
+    def _ints(self, tables, lengths, free_ids, refcount, req_idx):
+        tables = _c(tables, np.int32).copy()
+        lengths = _c(lengths, np.int32).copy()
+        free_ids = _c(free_ids, np.int32).copy()
+        refcount = _c(refcount, np.int32).copy()
+        if req_idx is not None:
+            req_idx = _c(req_idx, np.int32)
+        return tables, lengths, free_ids, refcount, req_idx
+
+    def alloc_rows(self, tables, lengths, free_ids, free_count, refcount, counts, b,
+                   req_idx=None):
+        """Blocks for the first counts[i] tokens of empty rows; returns dict
+        (status, tables, lengths, free_ids, free_count, refcount) of copies."""
+        tables, lengths, free_ids, refcount, req_idx = self._ints(tables, lengths, free_ids,
+                                                                  refcount, req_idx)
+        counts = _c(counts, np.int32)
+        num_rows, stride = tables.shape
+        fc = ctypes.c_int32(int(free_count))
+        st = self.lib.zpo_alloc_rows(_p(tables), stride, num_rows, _p(lengths), _p(req_idx),
+                                     counts.shape[0], _p(counts), b, refcount.shape[0],
+                                     _p(refcount), _p(free_ids), ctypes.byref(fc),
+                                     free_ids.shape[0])
+        return dict(status=st, tables=tables, lengths=lengths, free_ids=free_ids,
+                    free_count=fc.value, refcount=refcount)
+
+    def release_rows(self, tables, lengths, free_ids, free_count, refcount, req_idx=None, R=None):
+        """Every block of the listed rows back to the pool; dict as alloc_rows."""
+        tables, lengths, free_ids, refcount, req_idx = self._ints(tables, lengths, free_ids,
+                                                                  refcount, req_idx)
+        num_rows, stride = tables.shape
+        if R is None:
+            R = req_idx.shape[0] if req_idx is not None else num_rows
+        fc = ctypes.c_int32(int(free_count))
+        st = self.lib.zpo_release_rows(_p(tables), stride, num_rows, _p(lengths), _p(req_idx), R,
+                                       refcount.shape[0], _p(refcount), _p(free_ids),
+                                       ctypes.byref(fc), free_ids.shape[0])
+        return dict(status=st, tables=tables, lengths=lengths, free_ids=free_ids,
+                    free_count=fc.value, refcount=refcount)

@@ -32,6 +32,9 @@
  *   prefill    [ZP-nl Methodologie §1, §3]: the same scoring, selection and
  *              compaction for a request admitted with more than N*b tokens;
  *              its excess blocks are released.
+ *   alloc /    [PKV]: blocks for a request's first tokens (taken from the free
+ *   release    stack) and, when it finishes or is preempted, every block of
+ *              its table back (one reference each, pushed when it reaches 0).
  *   append     [PKV; ZP-nl Methodologie §1]: the slot of each decoding request's
  *              next token (a new block only when the last one is full,
  *              copy-on-write of a shared block), the new token's K/V written
@@ -853,5 +856,125 @@ int zpo_append_kv(int Hkv, int d, int b, int num_blocks, uint16_t *kpool, uint16
             memcpy(vpool + to, v_new + from, sizeof(uint16_t) * (size_t)d);
         }
     }
+    return ZPO_OK;
+}
+
+/* ------------------------------------------------------ alloc / release */
+
+/* Blocks for the first tokens of empty requests [PKV, "How it works": blocks
+ * are taken from the pool only as the tokens need them].  Request i (row =
+ * req_idx[i], or i) gets counts[i] tokens: entries 0 .. ceil(counts[i]/b)-1
+ * of its row become blocks popped from the top of the free stack, in
+ * (request, block) order, each with refcount 1; lengths[row] = counts[i].
+ * Checked first (all or nothing): rows in range and distinct, lengths[row]
+ * == 0, 0 <= counts[i] <= stride*b, the entries to fill < 0 -> INVALID_ARG;
+ * enough free blocks -> OUT_OF_BLOCKS; popped ids in range with refcount 0,
+ * free_count within [0, capacity] -> DEVICE_CHECK. */
+int zpo_alloc_rows(int32_t *tables, int stride, int num_rows, int32_t *lengths,
+                   const int32_t *req_idx, int R, const int32_t *counts, int b, int num_blocks,
+                   int32_t *refcount, int32_t *free_ids, int32_t *free_count, int capacity)
+{
+    int fc = *free_count;
+    if (R < 0 || b < 1 || stride < 1)
+        return ZPO_ERR_INVALID_ARG;
+    if (fc < 0 || fc > capacity)
+        return ZPO_ERR_DEVICE_CHECK;
+    int need = 0;
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        if (row < 0 || row >= num_rows)
+            return ZPO_ERR_INVALID_ARG;
+        for (int r2 = 0; r2 < r; ++r2)
+            if ((req_idx ? req_idx[r2] : r2) == row)
+                return ZPO_ERR_INVALID_ARG;
+        if (lengths[row] != 0 || counts[r] < 0 || counts[r] > stride * b)
+            return ZPO_ERR_INVALID_ARG;
+        int nb = (counts[r] + b - 1) / b;
+        for (int p = 0; p < nb; ++p)
+            if (tables[(size_t)row * stride + p] >= 0)
+                return ZPO_ERR_INVALID_ARG;
+        need += nb;
+    }
+    if (need > fc)
+        return ZPO_ERR_OUT_OF_BLOCKS;
+    for (int k = 0; k < need; ++k) {
+        int32_t t = free_ids[fc - 1 - k];
+        if (t < 0 || t >= num_blocks || refcount[t] != 0)
+            return ZPO_ERR_DEVICE_CHECK;
+    }
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        int nb = (counts[r] + b - 1) / b;
+        for (int p = 0; p < nb; ++p) {
+            int32_t t = free_ids[--fc];
+            refcount[t] = 1;
+            tables[(size_t)row * stride + p] = t;
+        }
+        lengths[row] = counts[r];
+    }
+    *free_count = fc;
+    return ZPO_OK;
+}
+
+/* Every block of finished or preempted requests back to the pool [PKV,
+ * "How it works": a block's reference counter counts the tables that point
+ * at it; finished requests leave the batch].  Request after request, entry
+ * after entry, each entry >= 0 of the row loses one reference of its block,
+ * which is pushed onto the free stack when that empties it; the entry becomes
+ * -1 and lengths[row] becomes 0.  Checked first (all or nothing): rows in
+ * range and distinct, entries < num_blocks, every block referenced by the
+ * released rows at most refcount times -> INVALID_ARG; free_count within
+ * [0, capacity] and room for the pushes -> DEVICE_CHECK. */
+int zpo_release_rows(int32_t *tables, int stride, int num_rows, int32_t *lengths,
+                     const int32_t *req_idx, int R, int num_blocks, int32_t *refcount,
+                     int32_t *free_ids, int32_t *free_count, int capacity)
+{
+    int fc = *free_count;
+    if (R < 0 || stride < 1)
+        return ZPO_ERR_INVALID_ARG;
+    if (fc < 0 || fc > capacity)
+        return ZPO_ERR_DEVICE_CHECK;
+    int32_t *rc = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_blocks > 0 ? num_blocks : 1));
+    memcpy(rc, refcount, sizeof(int32_t) * (size_t)num_blocks);
+    int pushes = 0, st = ZPO_OK;
+    for (int r = 0; r < R && st == ZPO_OK; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        if (row < 0 || row >= num_rows) {
+            st = ZPO_ERR_INVALID_ARG;
+            break;
+        }
+        for (int r2 = 0; r2 < r; ++r2)
+            if ((req_idx ? req_idx[r2] : r2) == row)
+                st = ZPO_ERR_INVALID_ARG;
+        for (int p = 0; p < stride && st == ZPO_OK; ++p) {
+            int32_t blk = tables[(size_t)row * stride + p];
+            if (blk < 0)
+                continue;
+            if (blk >= num_blocks || rc[blk] < 1) {
+                st = ZPO_ERR_INVALID_ARG;
+                break;
+            }
+            if (--rc[blk] == 0)
+                ++pushes;
+        }
+    }
+    free(rc);
+    if (st != ZPO_OK)
+        return st;
+    if (fc + pushes > capacity)
+        return ZPO_ERR_DEVICE_CHECK;
+    for (int r = 0; r < R; ++r) {
+        int row = req_idx ? req_idx[r] : r;
+        for (int p = 0; p < stride; ++p) {
+            int32_t *entry = tables + (size_t)row * stride + p;
+            if (*entry < 0)
+                continue;
+            if (--refcount[*entry] == 0)
+                free_ids[fc++] = *entry;
+            *entry = -1;
+        }
+        lengths[row] = 0;
+    }
+    *free_count = fc;
     return ZPO_OK;
 }

@@ -939,6 +939,102 @@ def pin_append_errors(orc):
     assert run(tables=t, rc=[2, 2, 0, 0, 0, 0], lengths=[5, 5], fc=0) == -3
 
 
+def pin_alloc_release_handworked(orc):
+    """b = 4, free stack [5, 4, 3, 2, 1, 0] (top 0).  Rows 0 and 1 get 5 and 3
+    tokens: row 0 pops 0 then 1, row 1 pops 2; lengths 5 and 3, three blocks
+    left.  Releasing rows 1 then 0 pushes 2, then 0 and 1: the stack reads
+    [5, 4, 3, 2, 0, 1] and every refcount is 0 again."""
+    tables = np.full((3, 4), -1, dtype=np.int32)
+    free = np.array([5, 4, 3, 2, 1, 0], dtype=np.int32)
+    rc = np.zeros(6, dtype=np.int32)
+    a = orc.alloc_rows(tables, np.zeros(3, np.int32), free, 6, rc, [5, 3], 4,
+                       req_idx=np.array([0, 1], np.int32))
+    assert a["status"] == 0
+    assert a["tables"][:2].tolist() == [[0, 1, -1, -1], [2, -1, -1, -1]]
+    assert a["lengths"].tolist() == [5, 3, 0] and a["free_count"] == 3
+    assert a["refcount"].tolist() == [1, 1, 1, 0, 0, 0]
+    r = orc.release_rows(a["tables"], a["lengths"], a["free_ids"], a["free_count"],
+                         a["refcount"], req_idx=np.array([1, 0], np.int32))
+    assert r["status"] == 0
+    assert r["free_ids"].tolist() == [5, 4, 3, 2, 0, 1] and r["free_count"] == 6
+    assert np.all(r["tables"] == -1) and np.all(r["lengths"] == 0)
+    assert np.all(r["refcount"] == 0)
+
+
+def pin_release_shared_and_lifecycle(orc):
+    """Releasing forked requests drops one reference per holder and frees a
+    block at its last holder, in request-then-entry order; a whole life cycle
+    (alloc, append, compress, release of everything) returns every block to
+    the pool with refcount 0."""
+    c = _fork_cache(170, R=9, b=4, nmax=5)
+    req = np.array([4, 0, 7, 2], dtype=np.int32)
+    r = orc.release_rows(c["tables"], c["lengths"], c["free"], c["nfree"], c["rc"], req_idx=req)
+    assert r["status"] == 0
+    rc = c["rc"].copy()
+    pushed = []
+    for row in req:
+        for x in c["tables"][row]:
+            if x >= 0:
+                rc[x] -= 1
+                if rc[x] == 0:
+                    pushed.append(int(x))
+    assert np.array_equal(r["refcount"], rc)
+    assert r["free_ids"][c["nfree"]:r["free_count"]].tolist() == pushed
+    assert np.all(r["tables"][req] == -1) and np.all(r["lengths"][req] == 0)
+    others = np.setdiff1d(np.arange(9), req)
+    assert np.array_equal(r["tables"][others], c["tables"][others])
+
+    # life cycle on an empty pool
+    b, N, L, Hkv, d = 4, 3, 1, 2, 4
+    nb = 40
+    kp = [bf16(rng(171).standard_normal((nb, Hkv, b, d)))]
+    vp = [bf16(rng(172).standard_normal((nb, Hkv, b, d)))]
+    tables = np.full((4, N), -1, dtype=np.int32)
+    st = orc.alloc_rows(tables, np.zeros(4, np.int32), np.arange(nb, dtype=np.int32), nb,
+                        np.zeros(nb, np.int32), [9, 11, 4, 0], b)
+    assert st["status"] == 0
+    cur = dict(kpools=kp, vpools=vp, tables=st["tables"], lengths=st["lengths"],
+               free_ids=st["free_ids"], free_count=st["free_count"], refcount=st["refcount"])
+    a = orc.append_slots(cur["kpools"], cur["vpools"], cur["tables"], cur["lengths"],
+                         cur["free_ids"], cur["free_count"], cur["refcount"], N)
+    assert a["status"] == 0 and a["triggers"].tolist() == [1]   # 11 -> 12 = N*b
+    wq = bf16(rng(173).standard_normal((L, 1, Hkv, 2, d)))
+    cmp_ = orc.compress(a["kpools"], a["vpools"], a["tables"], a["lengths"], wq, N, 2, 0.5,
+                        a["free_ids"], a["free_count"], a["refcount"], Hq=Hkv,
+                        req_idx=a["triggers"])
+    assert cmp_["status"] == 0
+    a = orc.append_slots(cmp_["kpools"], cmp_["vpools"], cmp_["tables"], cmp_["lengths"],
+                         cmp_["free_ids"], cmp_["free_count"], cmp_["refcount"], N)
+    assert a["status"] == 0 and a["lengths"].tolist() == [11, 9, 6, 2]
+    rel = orc.release_rows(a["tables"], a["lengths"], a["free_ids"], a["free_count"],
+                           a["refcount"])
+    assert rel["status"] == 0
+    assert rel["free_count"] == nb and np.all(rel["refcount"] == 0)
+    assert sorted(rel["free_ids"].tolist()) == list(range(nb))
+
+
+def pin_alloc_release_errors(orc):
+    """All or nothing: allocating into a row that holds tokens or blocks, too
+    few free blocks, a repeated row, or releasing a block more often than it
+    is referenced changes nothing."""
+    tables = np.full((2, 3), -1, dtype=np.int32)
+    free = np.arange(4, dtype=np.int32)
+    rc = np.zeros(4, np.int32)
+    assert orc.alloc_rows(tables, np.array([1, 0], np.int32), free, 4, rc, [4, 4], 4)["status"] == -1
+    t2 = tables.copy()
+    t2[1, 0] = 3
+    assert orc.alloc_rows(t2, np.zeros(2, np.int32), free, 4, rc, [4, 4], 4)["status"] == -1
+    assert orc.alloc_rows(tables, np.zeros(2, np.int32), free, 4, rc, [9, 8], 4)["status"] == -3
+    assert orc.alloc_rows(tables, np.zeros(2, np.int32), free, 4, rc, [4, 4], 4,
+                          req_idx=np.array([0, 0], np.int32))["status"] == -1
+    held = np.array([[0, 1, -1], [0, -1, -1]], dtype=np.int32)
+    rc2 = np.array([1, 1, 0, 0], np.int32)   # block 0 is in two rows but counted once
+    r = orc.release_rows(held, np.array([5, 2], np.int32), np.array([2, 3, -1, -1], np.int32), 2,
+                         rc2)
+    assert r["status"] == -1
+    assert np.array_equal(r["tables"], held) and r["free_count"] == 2
+
+
 def pin_append_kv_then_decode(orc):
     """After the slots are reserved and each layer's new K/V row written, the
     new row sits at position p of the row's table, nothing else moved, and

@@ -88,6 +88,12 @@ MUTANTS = [
     ("global redundancy includes self",
      "if (k == j || norm[j] == 0.0 || norm[k] == 0.0)\n                continue;",
      "if (norm[j] == 0.0 || norm[k] == 0.0)\n                continue;"),
+    ("alloc pops from the bottom", "int32_t t = free_ids[--fc];",
+     "int32_t t = free_ids[*free_count - fc--];"),
+    ("release pushes every reference", "if (--refcount[*entry] == 0)\n                free_ids[fc++] = *entry;",
+     "--refcount[*entry];\n                free_ids[fc++] = *entry;"),
+    ("release keeps the entries", "            *entry = -1;\n        }\n        lengths[row] = 0;",
+     "        }\n        lengths[row] = 0;"),
     ("length check dropped", "if (lengths[row] != N * b)\n            return ZPO_ERR_INVALID_ARG;",
      ""),
 ]
