@@ -9,7 +9,7 @@
 #include <new>
 #include <vector>
 
-#include "zp_global_red.cuh"
+#include "zp_aux.cuh"
 #include "zp_internal.cuh"
 
 using zp::Workspace;
@@ -590,6 +590,59 @@ zp_status zp_append_kv(zp_cache *c, int32_t layer, const void *k_new, const void
     a.sticky = c->ws.sticky;
     return zp::launch_append_kv(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ZP_OK
                                                                                       : ZP_ERR_CUDA;
+}
+
+static zp_status rows_checks(const zp_cache *c, const int32_t *block_tables, int32_t bt_stride,
+                             int32_t num_rows, const int32_t *lengths, int32_t R,
+                             const zp_block_pool *pool)
+{
+    if (!c || !block_tables || !lengths || !pool || !pool->free_ids || !pool->free_count ||
+        !pool->refcount || pool->capacity < 1)
+        return ZP_ERR_INVALID_ARG;
+    if (R < 0 || num_rows < 1 || num_rows > c->max_requests || R > num_rows || bt_stride < 1)
+        return ZP_ERR_INVALID_ARG;
+    if (static_cast<long long>(bt_stride) * c->b >= (1ll << 31) ||
+        static_cast<long long>(R) * bt_stride >= (1ll << 31))
+        return ZP_ERR_UNSUPPORTED;
+    return ZP_OK;
+}
+
+zp_status zp_alloc_rows(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int32_t num_rows,
+                        int32_t *lengths, const int32_t *req_idx, int32_t R,
+                        const int32_t *counts, const zp_block_pool *pool, void *stream)
+{
+    zp_status st = rows_checks(c, block_tables, bt_stride, num_rows, lengths, R, pool);
+    if (st != ZP_OK)
+        return st;
+    if (!counts)
+        return ZP_ERR_INVALID_ARG;
+    if (R == 0)
+        return ZP_OK;
+    if (!on_device(c))
+        return ZP_ERR_INVALID_ARG;
+    return zp::launch_alloc_rows(c->ws, block_tables, bt_stride, num_rows, lengths, req_idx, R,
+                                 counts, c->num_blocks, pool,
+                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ZP_OK
+               : ZP_ERR_CUDA;
+}
+
+zp_status zp_release_rows(zp_cache *c, int32_t *block_tables, int32_t bt_stride,
+                          int32_t num_rows, int32_t *lengths, const int32_t *req_idx, int32_t R,
+                          const zp_block_pool *pool, void *stream)
+{
+    zp_status st = rows_checks(c, block_tables, bt_stride, num_rows, lengths, R, pool);
+    if (st != ZP_OK)
+        return st;
+    if (R == 0)
+        return ZP_OK;
+    if (!on_device(c))
+        return ZP_ERR_INVALID_ARG;
+    return zp::launch_release_rows(c->ws, block_tables, bt_stride, num_rows, lengths, req_idx, R,
+                                   c->num_blocks, pool,
+                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ZP_OK
+               : ZP_ERR_CUDA;
 }
 
 zp_status zp_global_redundancy(zp_cache *c, const int32_t *block_tables, int32_t bt_stride,

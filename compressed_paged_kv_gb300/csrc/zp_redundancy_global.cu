@@ -10,7 +10,7 @@
 // two passes over the unit's T keys, O(T d) each: S, then every key's dot
 // with S.  A row of d bf16 is d/8 lanes of 16-byte loads; the norms are
 // reduced across those lanes with shuffles.
-#include "zp_global_red.cuh"
+#include "zp_aux.cuh"
 
 namespace zp {
 

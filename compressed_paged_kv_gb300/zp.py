@@ -6,6 +6,7 @@ every call raises.
 The functions keep the C names (``zp_cache_create``, ``zp_compress``,
 ``zp_paged_decode_attn``, ``zp_append_slots``, ``zp_append_kv``,
 ``zp_compress_prefill``, ``zp_compress_prefill_workspace_size``, ``zp_global_redundancy``,
+``zp_alloc_rows``, ``zp_release_rows``,
 ``zp_cache_status``, ``zp_cache_destroy``, ``zp_status_string``) and take raw integers (device pointers, a cudaStream_t
 as an int).  ``Cache`` wraps them for torch tensors: it reads ``data_ptr()``
 and the current stream, and keeps the pool tensors alive.
@@ -89,6 +90,10 @@ def lib():
                                           ctypes.POINTER(zp_block_pool), P, ctypes.c_size_t, P,
                                           P, P]
         L.zp_compress_prefill.restype = I32
+        L.zp_alloc_rows.argtypes = [P, P, I32, I32, P, P, I32, P, ctypes.POINTER(zp_block_pool), P]
+        L.zp_alloc_rows.restype = I32
+        L.zp_release_rows.argtypes = [P, P, I32, I32, P, P, I32, ctypes.POINTER(zp_block_pool), P]
+        L.zp_release_rows.restype = I32
         L.zp_global_redundancy.argtypes = [P, P, I32, I32, P, P, I32, P, P]
         L.zp_global_redundancy.restype = I32
         L.zp_cache_status.argtypes = [P, P, ctypes.POINTER(I32)]
@@ -178,6 +183,19 @@ def zp_append_kv(handle, layer, k_new, v_new, block_tables, bt_stride, num_rows,
                  req_idx, R, stream) -> int:
     return lib().zp_append_kv(P(handle), layer, P(k_new), P(v_new), P(block_tables), bt_stride,
                               num_rows, P(lengths), P(req_idx or None), R, P(stream or None))
+
+
+def zp_alloc_rows(handle, block_tables, bt_stride, num_rows, lengths, req_idx, R, counts,
+                  pool: zp_block_pool, stream) -> int:
+    return lib().zp_alloc_rows(P(handle), P(block_tables), bt_stride, num_rows, P(lengths),
+                               P(req_idx or None), R, P(counts), ctypes.byref(pool),
+                               P(stream or None))
+
+
+def zp_release_rows(handle, block_tables, bt_stride, num_rows, lengths, req_idx, R,
+                    pool: zp_block_pool, stream) -> int:
+    return lib().zp_release_rows(P(handle), P(block_tables), bt_stride, num_rows, P(lengths),
+                                 P(req_idx or None), R, ctypes.byref(pool), P(stream or None))
 
 
 def zp_global_redundancy(handle, block_tables, bt_stride, num_rows, lengths, req_idx, R, red_out,
@@ -301,6 +319,30 @@ class Cache:
                           lengths.data_ptr(), _ptr(req_idx), k_new.shape[0], _stream(stream))
         if check and st != OK:
             raise ZpError(st, "zp_append_kv")
+        return st
+
+    def alloc_rows(self, block_tables, lengths, counts, free_ids, free_count, refcount,
+                   req_idx=None, stream=None, check=True):
+        pool = zp_block_pool(free_ids.data_ptr(), free_count.data_ptr(), refcount.data_ptr(),
+                             free_ids.numel())
+        st = zp_alloc_rows(self.handle, block_tables.data_ptr(), block_tables.shape[1],
+                           block_tables.shape[0], lengths.data_ptr(), _ptr(req_idx),
+                           counts.numel(), counts.data_ptr(), pool, _stream(stream))
+        if check and st != OK:
+            raise ZpError(st, "zp_alloc_rows")
+        return st
+
+    def release_rows(self, block_tables, lengths, free_ids, free_count, refcount, req_idx=None,
+                     R=None, stream=None, check=True):
+        pool = zp_block_pool(free_ids.data_ptr(), free_count.data_ptr(), refcount.data_ptr(),
+                             free_ids.numel())
+        if R is None:
+            R = req_idx.numel() if req_idx is not None else block_tables.shape[0]
+        st = zp_release_rows(self.handle, block_tables.data_ptr(), block_tables.shape[1],
+                             block_tables.shape[0], lengths.data_ptr(), _ptr(req_idx), R, pool,
+                             _stream(stream))
+        if check and st != OK:
+            raise ZpError(st, "zp_release_rows")
         return st
 
     def global_redundancy(self, block_tables, lengths, red_out, req_idx=None, R=None,

@@ -25,8 +25,9 @@
  *  - A handle serves at most one call of each entry point in flight at a
  *    time.  zp_compress may run concurrently with zp_paged_decode_attn and
  *    zp_append_kv on another stream when they touch disjoint requests.
- *    zp_compress, zp_compress_prefill and zp_append_slots change the free
- *    stack and refcounts: order them (one stream, or events).  More concurrency needs
+ *    zp_compress, zp_compress_prefill, zp_append_slots, zp_alloc_rows and
+ *    zp_release_rows change the free stack and refcounts: order them (one
+ *    stream, or events).  More concurrency needs
  *    more handles.
  *
  * KV pool layout (one K pool and one V pool per layer, caller-owned):
@@ -288,6 +289,38 @@ zp_status zp_append_slots(zp_cache *cache, int32_t *block_tables, int32_t bt_str
                           int32_t num_rows, int32_t *lengths, const int32_t *req_idx, int32_t R,
                           int32_t n_max, const zp_block_pool *pool, void *stream,
                           int32_t *trigger_rows, int32_t *trigger_count);
+
+/* Blocks for the first tokens of requests entering the batch ("Paged KV
+ * cache and continuous batching for LLMs", "How it works": blocks are taken
+ * from the pool only as the tokens need them).  Request i (row = req_idx[i],
+ * or i) must be empty (lengths[row] == 0, entries < 0); it gets counts[i]
+ * tokens: entries 0 .. ceil(counts[i]/16)-1 become blocks popped from the top
+ * of the free stack in (request, block) order, refcount 1, and lengths[row] =
+ * counts[i].  The tokens' keys and values are the caller's to write.
+ *
+ *  counts        device int32 [R], 0 <= counts[i] <= bt_stride * 16
+ * All-or-nothing: a bad or repeated row, a row that is not empty, a count out
+ * of range -> ZP_ERR_INVALID_ARG; too few free blocks -> ZP_ERR_OUT_OF_BLOCKS;
+ * a popped id out of range or with a nonzero refcount -> ZP_ERR_DEVICE_CHECK
+ * (all in the sticky status).  Orders with every other call that changes the
+ * pool. */
+zp_status zp_alloc_rows(zp_cache *cache, int32_t *block_tables, int32_t bt_stride,
+                        int32_t num_rows, int32_t *lengths, const int32_t *req_idx, int32_t R,
+                        const int32_t *counts, const zp_block_pool *pool, void *stream);
+
+/* Every block of finished or preempted requests back to the pool ("How
+ * it works": a block's reference counter counts the tables that point at
+ * it).  Request after request, entry after entry, each entry >= 0 of the row
+ * (including a reserved, still empty block) drops one reference of its block,
+ * which is pushed on the free stack when that empties it; the entry becomes
+ * -1 and lengths[row] becomes 0.  Shared blocks survive while other rows hold
+ * them.  All-or-nothing: a bad or repeated row, an entry >= num_blocks, a
+ * block held by more released entries than its refcount ->
+ * ZP_ERR_INVALID_ARG; no room on the free stack -> ZP_ERR_DEVICE_CHECK.
+ * Orders with every other call that changes the pool. */
+zp_status zp_release_rows(zp_cache *cache, int32_t *block_tables, int32_t bt_stride,
+                          int32_t num_rows, int32_t *lengths, const int32_t *req_idx, int32_t R,
+                          const zp_block_pool *pool, void *stream);
 
 /* Writes one layer's new-token keys and values into the slots zp_append_slots
  * reserved ("Paged KV cache and continuous batching for LLMs", "How it
