@@ -454,6 +454,70 @@ def run_prefill(args, world, rank, local):
     return res
 
 
+# Hybrid vs strict scheduling of long reasoning requests through the library.
+SCHED = dict(name="sched", R=192, L=4, Hkv=8, Hq=32, d=128, N=128, w=8, num_blocks=6144,
+             query_slots=32, prompt=(128, 512), out_median=3000, out_sigma=0.6, out_max=8192,
+             seed=77)
+
+
+def run_sched(args, world, rank, local):
+    """The step-level simulator (compressed_paged_kv_gb300.scheduler) under
+    both policies on the same requests, every step running the kernels:
+    admission allocation (and compression at admission after a preemption),
+    slot reservation, new K/V and decode attention per layer, compression at
+    N_max, release."""
+    import torch
+
+    from compressed_paged_kv_gb300 import _build
+    from compressed_paged_kv_gb300 import scheduler as S
+
+    _build.build()
+    torch.cuda.set_device(local)
+    P = SCHED
+    res = {}
+    for policy in ("hybrid", "strict"):
+        reqs = S.synthetic_requests(P["R"], P["seed"] + rank, prompt=P["prompt"],
+                                    out_median=P["out_median"], out_sigma=P["out_sigma"],
+                                    out_max=P["out_max"])
+        cfg = S.SimConfig(num_blocks=P["num_blocks"], max_rows=P["R"], n_max=P["N"], w=P["w"],
+                          query_slots=P["query_slots"], strict=policy == "strict",
+                          seed=P["seed"])
+        stride = -(-(P["prompt"][1] + P["out_max"]) // 16)
+        be = S.GpuBackend(cfg, L=P["L"], Hkv=P["Hkv"], Hq=P["Hq"], d=P["d"],
+                          device=f"cuda:{local}", max_row_blocks=stride)
+        sch = S.Scheduler(cfg, be, reqs)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        out = sch.run()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        assert be.status() == 0 and be.free_count() == cfg.num_blocks
+        out["wall_s"] = wall
+        out["tokens_per_s"] = out["tokens"] / wall
+        res[policy] = out
+        del sch, be
+        torch.cuda.empty_cache()
+    if rank != 0:
+        return None
+    h, s = res["hybrid"], res["strict"]
+    return {
+        "metric": "generated tokens/s of a simulated serving run (real kernels every step)",
+        "value": world * h["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+        "steps": h["steps"], "warmup": 0, "ms_per_step": 1e3 * h["wall_s"] / h["steps"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded request lengths; random K/V/queries, no model)",
+        "config": {"workload": f"{P['name']}: {P['R']} requests, prompts {P['prompt']}, outputs "
+                               f"log-normal median {P['out_median']} (max {P['out_max']}); "
+                               f"L={P['L']}, 8/32 heads, d 128, N_max={P['N']}, "
+                               f"{P['num_blocks']} blocks, {P['query_slots']} query slots",
+                   "global_batch": world * P["R"], "seq_len": P["N"] * 16,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "hybrid": h, "strict": s,
+        "hybrid_over_strict_steps": s["steps"] / h["steps"],
+        "hybrid_over_strict_concurrency": h["mean_decoding"] / s["mean_decoding"],
+    }
+
+
 def run_gpu(args, world, rank, local):
     import torch
     import torch.distributed as dist
@@ -778,6 +842,8 @@ def main():
         res = run_mixed(args, world, rank, local)
     elif args.workload == PREFILL["name"]:
         res = run_prefill(args, world, rank, local)
+    elif args.workload == SCHED["name"]:
+        res = run_sched(args, world, rank, local)
     else:
         res = run_gpu(args, world, rank, local)
     if res is not None:
