@@ -295,6 +295,7 @@ zp_status zp_compress(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int
     ca.scores_out = scores_out;
     ca.kept_out = kept_out;
     ca.call = c->ws.call;
+    ca.cstat = c->ws.counters + 2;
     ca.sticky = c->ws.sticky;
     ca.L = c->L;
     ca.Hkv = c->Hkv;
@@ -304,6 +305,8 @@ zp_status zp_compress(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int
     ca.w = window;
     ca.rows = rows;
     ca.cs = cs;
+    ca.num_rows = num_rows;
+    ca.num_blocks = c->num_blocks;
     ca.lambda = lambda;
     ca.inv_rows = 1.0f / static_cast<float>(rows);
     ca.logit_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c->d)));

@@ -34,11 +34,15 @@ namespace zp {
 
 __global__ void __launch_bounds__(kPlanThreads) zp_plan_kernel(const PlanArgs a)
 {
+    // the fused kernel may start now: it reads nothing of this plan before
+    // its own griddepcontrol.wait
+    pdl_launch_dependents();
     __shared__ int s_err;
     __shared__ int s_fc, s_gen;
     __shared__ int s_scan[kPlanThreads / 32 + 1];
     const int tid = threadIdx.x;
     if (tid == 0) {
+        a.ws.counters[2] = 0;  // the compaction's status, set by it only on a failed wait
         const int g = a.ws.gens[0];
         s_gen = g >= 0x7ffffff0 ? 1 : g + 1;
         a.ws.gens[0] = s_gen;
@@ -197,7 +201,10 @@ __global__ void __launch_bounds__(kPlanThreads) zp_finalize_kernel(const Finaliz
 {
     __shared__ int s_fc;
     const int tid = threadIdx.x;
-    const int st = *(volatile int32_t *)a.ws.call;
+    pdl_wait();  // every write of the kernels before it is visible
+    int st = *(volatile int32_t *)a.ws.call;
+    if (st == 0)
+        st = *(volatile int32_t *)(a.ws.counters + 2);
     if (st != 0) {
         if (tid == 0)
             set_error(a.ws.sticky, st);
@@ -244,8 +251,17 @@ cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s)
 
 cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s)
 {
-    zp_finalize_kernel<<<1, kPlanThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    // launched early (programmatic serialisation); it waits at its start
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(kPlanThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, zp_finalize_kernel, a);
 }
 
 int compress_cluster_size(int T)

@@ -236,11 +236,14 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
     const int l = (unit / a.Hkv) % a.L;
     const int r = unit / (a.Hkv * a.L);
 
-    // A failed plan makes the whole grid exit here, uniformly per cluster.
-    if (*reinterpret_cast<volatile int32_t *>(a.call) != 0)
-        return;
-
+    // This kernel may start while the plan kernel still runs (programmatic
+    // dependent launch).  Until its griddepcontrol.wait it reads no plan
+    // output and writes no global memory; reads taken from the caller's
+    // tables are bounds-checked (TMA loads are by the tensor map), and a bad
+    // row or block, which the plan reports, only stops this unit.
     const int row = a.req_idx ? a.req_idx[r] : r;
+    if (row < 0 || row >= a.num_rows)
+        return;  // uniform per cluster: its CTAs share the unit
     const int32_t *src_row = a.tables + (size_t)row * a.stride;
     const int32_t *dst_row = a.dst_table + (size_t)r * a.N;
     const int T = a.N * kBlk, C = T - a.w;
@@ -259,10 +262,6 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
     // moves at most one block down)
     for (int q = tid; q < nblk; q += kSThreads)
         sSblk[q] = src_row[blk0 + q];
-    for (int q = tid; q <= nblk; q += kSThreads) {
-        const int lb = blk0 - 1 + q;
-        sDblk[q] = (lb >= 0 && lb < a.N - 1) ? dst_row[lb] : -1;
-    }
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
@@ -287,10 +286,14 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
             bool ok = true;
             if (cs > 1) {
                 const int blk = sSblk[nblk - 1];
-                const size_t off = ((size_t)blk * a.Hkv + h) * kBlk * D;
-                mbar_arrive_expect_tx(tailb, 2 * SLAB);
-                bulk_g2s_hint(sTail, kpool_in + off, SLAB, tailb, once);
-                bulk_g2s_hint(sTail + SLAB, vpool_in + off, SLAB, tailb, once);
+                if (blk >= 0 && blk < a.num_blocks) {
+                    const size_t off = ((size_t)blk * a.Hkv + h) * kBlk * D;
+                    mbar_arrive_expect_tx(tailb, 2 * SLAB);
+                    bulk_g2s_hint(sTail, kpool_in + off, SLAB, tailb, once);
+                    bulk_g2s_hint(sTail + SLAB, vpool_in + off, SLAB, tailb, once);
+                } else {
+                    mbar_arrive_expect_tx(tailb, 0);  // a bad id: the plan fails the call
+                }
             }
             const CUtensorMap *kmap = a.kmaps + l;
             int idx = 0;
@@ -315,7 +318,12 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                     }
                 }
             }
-            for (int g = 0; g < n_move; ++g, ++idx) {
+            // pass 3 reads the blocks with plain bulk copies: only after the
+            // plan has checked every id (and not at all if it failed)
+            pdl_wait();
+            const int n_move_live =
+                *reinterpret_cast<volatile int32_t *>(a.call) == 0 ? n_move : 0;
+            for (int g = 0; g < n_move_live; ++g, ++idx) {
                 const int s = idx % NS;
                 if (idx >= NS)
                     ok &= mbar_wait(&empty[s], ((idx / NS) - 1) & 1);
@@ -336,7 +344,7 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                 }
             }
             if (!ok) {
-                set_error(a.call, ZP_ERR_TIMEOUT);
+                set_error(a.cstat, ZP_ERR_TIMEOUT);
                 set_error(a.sticky, ZP_ERR_TIMEOUT);
             }
         }
@@ -556,6 +564,16 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
         }
         named_sync(NCT);
 
+        // the plan's verdict and destinations (the plan kernel may have run
+        // alongside everything above)
+        pdl_wait();
+        const bool live = *reinterpret_cast<volatile int32_t *>(a.call) == 0;
+        for (int q = tid; q <= nblk; q += NCT) {
+            const int lb = blk0 - 1 + q;
+            sDblk[q] = (live && lb >= 0 && lb < a.N - 1) ? dst_row[lb] : -1;
+        }
+        named_sync(NCT);
+
         // ---- pass 2: importance and score of every key
         const size_t uo = ((size_t)l * a.R + r) * a.Hkv + h;
         for (int g = 0; g < n_score; ++g, ++idx) {
@@ -588,148 +606,155 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                         const int key = key0 + nt * 8 + lane * 2 + ee;
                         const float sc = v * a.inv_rows - a.lambda * sRed[key];
                         sScore[key] = sc;
-                        if (a.scores_out)
+                        if (a.scores_out && live)
                             a.scores_out[uo * (size_t)T + t0 + key] =
                                 (t0 + key < C) ? sc : INFINITY;
                     }
                 }
         }
         named_sync(NCT);
-
-        // ---- select the b evicted tokens
-        {
-            const int KW = TC / kSW;  // keys of this warp
-            uint64_t key[kSKeysPerLane];
-#pragma unroll
-            for (int s2 = 0; s2 < kSKeysPerLane; ++s2) {
-                const int kk = lane + 32 * s2;
-                key[s2] = ~0ull;
-                if (kk < KW) {
-                    const int k = wi * KW + kk, tok = t0 + k;
-                    const uint32_t hi = tok < C ? f32_order(sScore[k]) : 0xffffffffu;
-                    key[s2] = (static_cast<uint64_t>(hi) << 32) |
-                              (0xffffffffu - static_cast<uint32_t>(tok));
-                }
-            }
-            uint32_t chosen[kSKeysPerLane];
-            warp_select_smallest<kSKeysPerLane>(key, kBlk, chosen);
-            warp_compact_keys<kSKeysPerLane>(key, chosen, sCand + wi * kBlk);
-        }
-        named_sync(NCT);
-        for (int t = tid; t < kSW * kBlk; t += NCT) {  // the CTA's b smallest, sorted
-            const uint64_t k0 = sCand[t];
-            int rank = 0;
-#pragma unroll 8
-            for (int s2 = 0; s2 < kSW * kBlk; ++s2)
-                rank += sCand[s2] < k0;
-            if (rank < kBlk)
-                sPub[rank] = k0;
-        }
-        named_sync(NCT);
-        if (cs > 1) {
-            if (tid == 0) {
-                // this CTA's last block is staged: peers may now write into it
+        if (!live) {
+            // a failed plan: nothing is written; wait for the staged tail
+            // block before leaving (no copy may target freed shared memory)
+            if (cs > 1 && tid == 0)
                 bad |= !mbar_wait(tailb, 0);
-                for (int c = 0; c < cs; ++c)
-                    mbar_arrive_remote(dsmem_addr(xb2, c));
+        } else {
+            // ---- select the b evicted tokens
+            {
+                const int KW = TC / kSW;  // keys of this warp
+                uint64_t key[kSKeysPerLane];
+    #pragma unroll
+                for (int s2 = 0; s2 < kSKeysPerLane; ++s2) {
+                    const int kk = lane + 32 * s2;
+                    key[s2] = ~0ull;
+                    if (kk < KW) {
+                        const int k = wi * KW + kk, tok = t0 + k;
+                        const uint32_t hi = tok < C ? f32_order(sScore[k]) : 0xffffffffu;
+                        key[s2] = (static_cast<uint64_t>(hi) << 32) |
+                                  (0xffffffffu - static_cast<uint32_t>(tok));
+                    }
+                }
+                uint32_t chosen[kSKeysPerLane];
+                warp_select_smallest<kSKeysPerLane>(key, kBlk, chosen);
+                warp_compact_keys<kSKeysPerLane>(key, chosen, sCand + wi * kBlk);
             }
-            bad |= !mbar_wait_cluster(xb2, 0);
-            for (int e = tid; e < cs * kBlk; e += NCT)
-                sAll[e] = ld_dsmem_u64(dsmem_addr(sPub + (e & (kBlk - 1)), e / kBlk));
             named_sync(NCT);
-            if (cs <= 4) {
-                // rank of each candidate: its place in its own sorted list plus
-                // a binary search in each other list
-                for (int e = tid; e < cs * kBlk; e += NCT) {
-                    const uint64_t k0 = sAll[e];
-                    const int c0 = e / kBlk;
-                    int rank = e % kBlk;
+            for (int t = tid; t < kSW * kBlk; t += NCT) {  // the CTA's b smallest, sorted
+                const uint64_t k0 = sCand[t];
+                int rank = 0;
+    #pragma unroll 8
+                for (int s2 = 0; s2 < kSW * kBlk; ++s2)
+                    rank += sCand[s2] < k0;
+                if (rank < kBlk)
+                    sPub[rank] = k0;
+            }
+            named_sync(NCT);
+            if (cs > 1) {
+                if (tid == 0) {
+                    // this CTA's last block is staged: peers may now write into it
+                    bad |= !mbar_wait(tailb, 0);
                     for (int c = 0; c < cs; ++c)
-                        if (c != c0)
-                            rank += count_below16(sAll + c * kBlk, k0);
-                    if (rank < kBlk)
-                        sEv[rank] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k0));
+                        mbar_arrive_remote(dsmem_addr(xb2, c));
                 }
-            } else if (wi == 0) {  // b steps of a k-way merge of the sorted lists
-                int ptr = 0;
-                for (int step = 0; step < kBlk; ++step) {
-                    const uint64_t head =
-                        (lane < cs && ptr < kBlk) ? sAll[lane * kBlk + ptr] : ~0ull;
-                    const uint32_t hi = static_cast<uint32_t>(head >> 32);
-                    const uint32_t lo = static_cast<uint32_t>(head);
-                    const uint32_t mhi = __reduce_min_sync(0xffffffffu, hi);
-                    const uint32_t mlo =
-                        __reduce_min_sync(0xffffffffu, hi == mhi ? lo : 0xffffffffu);
-                    if (lane < cs && hi == mhi && lo == mlo)
-                        ++ptr;
-                    if (lane == 0)
-                        sEv[step] = static_cast<int>(0xffffffffu - mlo);
+                bad |= !mbar_wait_cluster(xb2, 0);
+                for (int e = tid; e < cs * kBlk; e += NCT)
+                    sAll[e] = ld_dsmem_u64(dsmem_addr(sPub + (e & (kBlk - 1)), e / kBlk));
+                named_sync(NCT);
+                if (cs <= 4) {
+                    // rank of each candidate: its place in its own sorted list plus
+                    // a binary search in each other list
+                    for (int e = tid; e < cs * kBlk; e += NCT) {
+                        const uint64_t k0 = sAll[e];
+                        const int c0 = e / kBlk;
+                        int rank = e % kBlk;
+                        for (int c = 0; c < cs; ++c)
+                            if (c != c0)
+                                rank += count_below16(sAll + c * kBlk, k0);
+                        if (rank < kBlk)
+                            sEv[rank] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k0));
+                    }
+                } else if (wi == 0) {  // b steps of a k-way merge of the sorted lists
+                    int ptr = 0;
+                    for (int step = 0; step < kBlk; ++step) {
+                        const uint64_t head =
+                            (lane < cs && ptr < kBlk) ? sAll[lane * kBlk + ptr] : ~0ull;
+                        const uint32_t hi = static_cast<uint32_t>(head >> 32);
+                        const uint32_t lo = static_cast<uint32_t>(head);
+                        const uint32_t mhi = __reduce_min_sync(0xffffffffu, hi);
+                        const uint32_t mlo =
+                            __reduce_min_sync(0xffffffffu, hi == mhi ? lo : 0xffffffffu);
+                        if (lane < cs && hi == mhi && lo == mlo)
+                            ++ptr;
+                        if (lane == 0)
+                            sEv[step] = static_cast<int>(0xffffffffu - mlo);
+                    }
                 }
+            } else if (tid < kBlk) {
+                sEv[tid] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(sPub[tid]));
             }
-        } else if (tid < kBlk) {
-            sEv[tid] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(sPub[tid]));
-        }
-        named_sync(NCT);
+            named_sync(NCT);
 
-        // ---- pass 3: compaction, a half block per warp
-        __nv_bfloat16 *kpool = static_cast<__nv_bfloat16 *>(a.kpools[l]);
-        __nv_bfloat16 *vpool = static_cast<__nv_bfloat16 *>(a.vpools[l]);
-        const uint64_t once = policy_evict_first();
-        for (int g = 0; g < n_move; ++g, ++idx) {
-            if ((g & 1) != grp)
-                continue;
-            const int s = idx % NS;
-            bad |= !mbar_wait(&full[s], (idx / NS) & 1);
-            const int bi = gw >> 1;              // block of the stage
-            const int q = g * kSMoveBlocks + bi;  // block of the chunk
-            const int r8 = (gw & 1) * 8 + lane;   // row of the block (lanes 0..7)
-            const bool tail = cs > 1 && q == nblk - 1;
-            int dp = 0, dblk = -1;
-            bool moved = false;
-            if (lane < 8) {
-                const int tok = t0 + q * kBlk + r8;
-                int before = 0;
-                bool ev = false;
-#pragma unroll
-                for (int i = 0; i < kBlk; ++i) {
-                    const int e = sEv[i];
-                    before += e < tok;
-                    ev |= e == tok;
+            // ---- pass 3: compaction, a half block per warp
+            pdl_launch_dependents();  // the finalize kernel may be scheduled
+            __nv_bfloat16 *kpool = static_cast<__nv_bfloat16 *>(a.kpools[l]);
+            __nv_bfloat16 *vpool = static_cast<__nv_bfloat16 *>(a.vpools[l]);
+            const uint64_t once = policy_evict_first();
+            for (int g = 0; g < n_move; ++g, ++idx) {
+                if ((g & 1) != grp)
+                    continue;
+                const int s = idx % NS;
+                bad |= !mbar_wait(&full[s], (idx / NS) & 1);
+                const int bi = gw >> 1;              // block of the stage
+                const int q = g * kSMoveBlocks + bi;  // block of the chunk
+                const int r8 = (gw & 1) * 8 + lane;   // row of the block (lanes 0..7)
+                const bool tail = cs > 1 && q == nblk - 1;
+                int dp = 0, dblk = -1;
+                bool moved = false;
+                if (lane < 8) {
+                    const int tok = t0 + q * kBlk + r8;
+                    int before = 0;
+                    bool ev = false;
+    #pragma unroll
+                    for (int i = 0; i < kBlk; ++i) {
+                        const int e = sEv[i];
+                        before += e < tok;
+                        ev |= e == tok;
+                    }
+                    if (!ev) {
+                        dp = tok - before;
+                        dblk = sDblk[(dp >> 4) - blk0 + 1];
+                        moved = dp != tok || dblk != sSblk[q];
+                        if (a.kept_out)
+                            a.kept_out[uo * (size_t)(T - kBlk) + dp] = tok;
+                    }
                 }
-                if (!ev) {
-                    dp = tok - before;
-                    dblk = sDblk[(dp >> 4) - blk0 + 1];
-                    moved = dp != tok || dblk != sSblk[q];
-                    if (a.kept_out)
-                        a.kept_out[uo * (size_t)(T - kBlk) + dp] = tok;
+                const int dp_prev = __shfl_up_sync(0xffffffffu, dp, 1);
+                const int dblk_prev = __shfl_up_sync(0xffffffffu, dblk, 1);
+                const bool moved_prev = __shfl_up_sync(0xffffffffu, moved ? 1 : 0, 1) != 0;
+                const bool cont = moved && lane > 0 && moved_prev && dblk_prev == dblk &&
+                                  dp_prev + 1 == dp;
+                const uint32_t cont_mask = __ballot_sync(0xffffffffu, cont);
+                if (moved && !cont && !bad) {
+                    const uint32_t rest = ~(cont_mask >> (lane + 1));
+                    const int len = __ffs(rest);  // 1 + continuing lanes after this one
+                    const size_t goff = ((size_t)dblk * a.Hkv + h) * kBlk + (dp & (kBlk - 1));
+                    const uint8_t *ksrc = tail ? sTail + r8 * ROW_BYTES
+                                               : sRing + s * STAGE + bi * SLAB + r8 * ROW_BYTES;
+                    const uint8_t *vsrc = tail ? sTail + SLAB + r8 * ROW_BYTES
+                                               : sRing + s * STAGE + (kSMoveBlocks + bi) * SLAB +
+                                                     r8 * ROW_BYTES;
+                    bulk_s2g_hint(kpool + goff * D, ksrc, len * ROW_BYTES, once);
+                    bulk_s2g_hint(vpool + goff * D, vsrc, len * ROW_BYTES, once);
                 }
+                bulk_commit();
+                bulk_wait_read0();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&empty[s]);
             }
-            const int dp_prev = __shfl_up_sync(0xffffffffu, dp, 1);
-            const int dblk_prev = __shfl_up_sync(0xffffffffu, dblk, 1);
-            const bool moved_prev = __shfl_up_sync(0xffffffffu, moved ? 1 : 0, 1) != 0;
-            const bool cont = moved && lane > 0 && moved_prev && dblk_prev == dblk &&
-                              dp_prev + 1 == dp;
-            const uint32_t cont_mask = __ballot_sync(0xffffffffu, cont);
-            if (moved && !cont && !bad) {
-                const uint32_t rest = ~(cont_mask >> (lane + 1));
-                const int len = __ffs(rest);  // 1 + continuing lanes after this one
-                const size_t goff = ((size_t)dblk * a.Hkv + h) * kBlk + (dp & (kBlk - 1));
-                const uint8_t *ksrc = tail ? sTail + r8 * ROW_BYTES
-                                           : sRing + s * STAGE + bi * SLAB + r8 * ROW_BYTES;
-                const uint8_t *vsrc = tail ? sTail + SLAB + r8 * ROW_BYTES
-                                           : sRing + s * STAGE + (kSMoveBlocks + bi) * SLAB +
-                                                 r8 * ROW_BYTES;
-                bulk_s2g_hint(kpool + goff * D, ksrc, len * ROW_BYTES, once);
-                bulk_s2g_hint(vpool + goff * D, vsrc, len * ROW_BYTES, once);
-            }
-            bulk_commit();
-            bulk_wait_read0();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&empty[s]);
         }
         if (bad && tid == 0) {
-            set_error(a.call, ZP_ERR_TIMEOUT);
+            set_error(a.cstat, ZP_ERR_TIMEOUT);
             set_error(a.sticky, ZP_ERR_TIMEOUT);
         }
     }
@@ -767,13 +792,16 @@ cudaError_t launch_stream_t(const CompressArgs &a, int units, cudaStream_t s)
     cfg.blockDim = dim3(kSThreads, 1, 1);
     cfg.dynamicSmemBytes = Sm::ALLOC;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(a.cs);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // may start while the plan kernel runs; it waits before using the plan
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

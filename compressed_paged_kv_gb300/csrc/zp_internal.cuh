@@ -31,7 +31,7 @@ struct Workspace {
     void **vpools;       // [L]
     int32_t *dst_table;  // [max_requests * max_blocks] plan: destination blocks
     int32_t *push_list;  // [max_requests * max_blocks] plan: blocks to free, in order
-    int32_t *counters;   // [4]  plan: pops, pushes
+    int32_t *counters;   // [4]  plan: pops, pushes; [2] the compaction's own status
     int32_t *occ;        // [num_blocks] plan: holders of a replaced block in this call
     int32_t *last;       // [num_blocks] plan: last (request, block) entry of such a block
     int32_t *rowmark;    // [max_requests] generation stamps (duplicate-row check)
@@ -86,9 +86,11 @@ struct CompressArgs {
     const __nv_bfloat16 *window_q;
     float *scores_out;
     int32_t *kept_out;
-    int32_t *call;
+    int32_t *call;   // the plan's verdict: only the plan writes it
+    int32_t *cstat;  // the compaction's own status (a bounded wait that gave up)
     int32_t *sticky;
     int32_t L, Hkv, Hq, R, N, w, rows, cs;
+    int32_t num_rows, num_blocks;  // bounds for reads made before the plan's verdict
     float lambda;
     float inv_rows;       // 1 / (w * G)
     float logit_scale;    // log2(e) / sqrt(d): logits are kept in base 2
@@ -186,6 +188,21 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
 __device__ __forceinline__ void set_error(int32_t *word, int32_t code)
 {
     atomicCAS(word, 0, code);
+}
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before its predecessor on the stream finishes;
+// griddepcontrol.wait blocks until the predecessor grid has completed and its
+// memory operations are visible (a no-op when launched without it), and
+// launch_dependents lets the successor start once every CTA issued it.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // block scan ----------------------------------------------------------------
