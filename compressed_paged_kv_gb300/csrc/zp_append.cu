@@ -210,6 +210,8 @@ __global__ void __launch_bounds__(kApplyThreads) zp_append_apply_kernel(const Ap
 
 __global__ void __launch_bounds__(kKvThreads) zp_append_kv_kernel(const AppendKvArgs a)
 {
+    pdl_wait();  // launched early: the reservation's writes are visible from here
+    pdl_launch_dependents();
     const int warp = (blockIdx.x * kKvThreads + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= a.R * a.Hkv)
@@ -247,8 +249,16 @@ cudaError_t launch_append_kv(const AppendKvArgs &a, cudaStream_t s)
 {
     const long long threads = static_cast<long long>(a.R) * a.Hkv * 32;
     const unsigned grid = static_cast<unsigned>((threads + kKvThreads - 1) / kKvThreads);
-    zp_append_kv_kernel<<<grid, kKvThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kKvThreads, 1, 1);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, zp_append_kv_kernel, a);
 }
 
 }  // namespace zp

@@ -41,6 +41,7 @@ struct DecodeSmem {
 template <int D>
 __global__ void __launch_bounds__(kDecThreads, 2) zp_decode_kernel(const DecodeArgs a)
 {
+    pdl_wait();  // launched early: everything of the kernels before it is visible from here
     using S = DecodeSmem<D>;
     constexpr int CPR = D / 8;
     constexpr int HALVES = D / 64;
@@ -200,6 +201,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) zp_decode_kernel(const DecodeA
     }
     if (!ok && lane == 0)
         set_error(a.sticky, ZP_ERR_TIMEOUT);
+    pdl_launch_dependents();  // the combine kernel may be scheduled
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 1);
@@ -257,6 +259,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) zp_decode_kernel(const DecodeA
 template <int D>
 __global__ void __launch_bounds__(D) zp_decode_combine(const DecodeArgs a)
 {
+    pdl_wait();
     const int rh = blockIdx.x;  // r * Hq + hq
     const int c = threadIdx.x;
     const float *base = a.part + (size_t)rh * a.splits * (D + 2);
@@ -280,14 +283,25 @@ static cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t s)
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::ALLOC);
     if (err != cudaSuccess)
         return err;
-    dim3 grid(static_cast<unsigned>(a.splits), static_cast<unsigned>(a.Hkv),
-              static_cast<unsigned>(a.R));
-    zp_decode_kernel<D><<<grid, kDecThreads, Sm::ALLOC, s>>>(a);
-    err = cudaGetLastError();
+    // both launched early (programmatic serialisation); each waits at its start
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.splits), static_cast<unsigned>(a.Hkv),
+                       static_cast<unsigned>(a.R));
+    cfg.blockDim = dim3(kDecThreads, 1, 1);
+    cfg.dynamicSmemBytes = Sm::ALLOC;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, zp_decode_kernel<D>, a);
     if (err != cudaSuccess || a.splits == 1)
         return err;
-    zp_decode_combine<D><<<static_cast<unsigned>(a.R * a.Hq), D, 0, s>>>(a);
-    return cudaGetLastError();
+    cfg.gridDim = dim3(static_cast<unsigned>(a.R * a.Hq), 1, 1);
+    cfg.blockDim = dim3(D, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, zp_decode_combine<D>, a);
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t s)
