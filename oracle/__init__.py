@@ -92,6 +92,8 @@ def _declare(lib):
     lib.zpo_alloc_rows.restype = I
     lib.zpo_release_rows.argtypes = [P, I, I, P, P, I, I, P, P, P, I]
     lib.zpo_release_rows.restype = I
+    lib.zpo_fork_rows.argtypes = [P, I, I, P, P, P, I, I, P]
+    lib.zpo_fork_rows.restype = I
     lib.zpo_append_slots.argtypes = [I, I, I, I, I, P, P, P, I, I, P, P, I, I, P, P, P, I, P, P]
     lib.zpo_append_slots.restype = I
     lib.zpo_append_kv.argtypes = [I, I, I, I, P, P, P, I, I, P, P, I, P, P]
@@ -415,3 +417,16 @@ class Oracle:
                                        ctypes.byref(fc), free_ids.shape[0])
         return dict(status=st, tables=tables, lengths=lengths, free_ids=free_ids,
                     free_count=fc.value, refcount=refcount)
+
+    def fork_rows(self, tables, lengths, refcount, src, dst):
+        """Rows dst[i] become copies of rows src[i] sharing their blocks;
+        dict(status, tables, lengths, refcount) of copies."""
+        tables = _c(tables, np.int32).copy()
+        lengths = _c(lengths, np.int32).copy()
+        refcount = _c(refcount, np.int32).copy()
+        src = _c(src, np.int32)
+        dst = _c(dst, np.int32)
+        num_rows, stride = tables.shape
+        st = self.lib.zpo_fork_rows(_p(tables), stride, num_rows, _p(lengths), _p(src), _p(dst),
+                                    src.shape[0], refcount.shape[0], _p(refcount))
+        return dict(status=st, tables=tables, lengths=lengths, refcount=refcount)

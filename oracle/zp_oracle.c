@@ -35,6 +35,8 @@
  *   alloc /    [PKV]: blocks for a request's first tokens (taken from the free
  *   release    stack) and, when it finishes or is preempted, every block of
  *              its table back (one reference each, pushed when it reaches 0).
+ *   fork       [PKV]: a new request sharing every block of another one (parallel
+ *              sampling stores the shared prompt once; refcounts count holders).
  *   append     [PKV; ZP-nl Methodologie §1]: the slot of each decoding request's
  *              next token (a new block only when the last one is full,
  *              copy-on-write of a shared block), the new token's K/V written
@@ -976,5 +978,49 @@ int zpo_release_rows(int32_t *tables, int stride, int num_rows, int32_t *lengths
         lengths[row] = 0;
     }
     *free_count = fc;
+    return ZPO_OK;
+}
+
+/* Forks requests [PKV, "How it works": parallel samples share the prompt's
+ * blocks, each block's reference counter counts the tables pointing at it]:
+ * pair i makes row dst[i] (empty: length 0, every entry < 0) a copy of row
+ * src[i] -- the same table entries (a reserved empty block included) and the
+ * same length -- and every block entry gains one reference.  Checked first
+ * (all or nothing): rows in range, destinations distinct and none of them a
+ * source of the same call, destinations empty, source entries < num_blocks
+ * with refcount >= 1 -> INVALID_ARG. */
+int zpo_fork_rows(int32_t *tables, int stride, int num_rows, int32_t *lengths,
+                  const int32_t *src, const int32_t *dst, int n, int num_blocks,
+                  int32_t *refcount)
+{
+    if (n < 0 || stride < 1)
+        return ZPO_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        int s = src[i], d = dst[i];
+        if (s < 0 || s >= num_rows || d < 0 || d >= num_rows || s == d)
+            return ZPO_ERR_INVALID_ARG;
+        for (int k = 0; k < n; ++k)
+            if ((k != i && dst[k] == d) || src[k] == d)
+                return ZPO_ERR_INVALID_ARG;
+        if (lengths[d] != 0)
+            return ZPO_ERR_INVALID_ARG;
+        for (int p = 0; p < stride; ++p) {
+            if (tables[(size_t)d * stride + p] >= 0)
+                return ZPO_ERR_INVALID_ARG;
+            int32_t blk = tables[(size_t)s * stride + p];
+            if (blk >= num_blocks || (blk >= 0 && refcount[blk] < 1))
+                return ZPO_ERR_INVALID_ARG;
+        }
+    }
+    for (int i = 0; i < n; ++i) {
+        int s = src[i], d = dst[i];
+        for (int p = 0; p < stride; ++p) {
+            int32_t blk = tables[(size_t)s * stride + p];
+            tables[(size_t)d * stride + p] = blk;
+            if (blk >= 0)
+                refcount[blk] += 1;
+        }
+        lengths[d] = lengths[s];
+    }
     return ZPO_OK;
 }

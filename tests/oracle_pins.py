@@ -1013,6 +1013,35 @@ def pin_release_shared_and_lifecycle(orc):
     assert sorted(rel["free_ids"].tolist()) == list(range(nb))
 
 
+def pin_fork_then_append_then_release(orc):
+    """Forking a request of 6 tokens (b 4) into two samples shares both blocks
+    (refcount 3); each sample's next token copies the partial tail on write
+    (the last writer keeps it); releasing the three rows returns every block."""
+    b = 4
+    kp = [bf16(rng(180).standard_normal((8, 1, b, 2)))]
+    vp = [bf16(rng(181).standard_normal((8, 1, b, 2)))]
+    tables = np.full((3, 3), -1, np.int32)
+    a = orc.alloc_rows(tables, np.zeros(3, np.int32), np.arange(8, dtype=np.int32), 8,
+                       np.zeros(8, np.int32), [6], b, req_idx=np.array([0], np.int32))
+    assert a["tables"][0].tolist() == [7, 6, -1]
+    f = orc.fork_rows(a["tables"], a["lengths"], a["refcount"], [0, 0], [1, 2])
+    assert f["status"] == 0
+    assert f["tables"].tolist() == [[7, 6, -1]] * 3 and f["lengths"].tolist() == [6, 6, 6]
+    assert f["refcount"][[7, 6]].tolist() == [3, 3]
+    s = orc.append_slots(kp, vp, f["tables"], f["lengths"], a["free_ids"], a["free_count"],
+                         f["refcount"], 3)
+    assert s["status"] == 0
+    # rows 0 and 1 copy block 6 (to 5, then 4); row 2, the last writer, keeps it
+    assert s["tables"][:, 1].tolist() == [5, 4, 6]
+    assert s["refcount"][[7, 6, 5, 4]].tolist() == [3, 1, 1, 1]
+    assert np.array_equal(s["kpools"][0][5, :, :2], kp[0][6, :, :2])
+    r = orc.release_rows(s["tables"], s["lengths"], s["free_ids"], s["free_count"], s["refcount"])
+    assert r["status"] == 0 and r["free_count"] == 8 and np.all(r["refcount"] == 0)
+    # errors: a destination that holds tokens, or a row forked from itself
+    assert orc.fork_rows(f["tables"], f["lengths"], f["refcount"], [0], [1])["status"] == -1
+    assert orc.fork_rows(a["tables"], a["lengths"], a["refcount"], [1], [1])["status"] == -1
+
+
 def pin_alloc_release_errors(orc):
     """All or nothing: allocating into a row that holds tokens or blocks, too
     few free blocks, a repeated row, or releasing a block more often than it

@@ -94,6 +94,7 @@ MUTANTS = [
      "--refcount[*entry];\n                free_ids[fc++] = *entry;"),
     ("release keeps the entries", "            *entry = -1;\n        }\n        lengths[row] = 0;",
      "        }\n        lengths[row] = 0;"),
+    ("fork without a reference", "            if (blk >= 0)\n                refcount[blk] += 1;", ""),
     ("length check dropped", "if (lengths[row] != N * b)\n            return ZPO_ERR_INVALID_ARG;",
      ""),
 ]
