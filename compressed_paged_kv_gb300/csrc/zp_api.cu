@@ -648,6 +648,27 @@ zp_status zp_release_rows(zp_cache *c, int32_t *block_tables, int32_t bt_stride,
                : ZP_ERR_CUDA;
 }
 
+zp_status zp_fork_rows(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int32_t num_rows,
+                       int32_t *lengths, const int32_t *src_rows, const int32_t *dst_rows,
+                       int32_t n, int32_t *refcount, void *stream)
+{
+    if (!c || !block_tables || !lengths || !refcount || (n > 0 && (!src_rows || !dst_rows)))
+        return ZP_ERR_INVALID_ARG;
+    if (n < 0 || num_rows < 1 || num_rows > c->max_requests || n > num_rows || bt_stride < 1)
+        return ZP_ERR_INVALID_ARG;
+    if (static_cast<long long>(n) * bt_stride >= (1ll << 31))
+        return ZP_ERR_UNSUPPORTED;
+    if (n == 0)
+        return ZP_OK;
+    if (!on_device(c))
+        return ZP_ERR_INVALID_ARG;
+    return zp::launch_fork_rows(c->ws, block_tables, bt_stride, num_rows, lengths, src_rows,
+                                dst_rows, n, c->num_blocks, refcount,
+                                static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ZP_OK
+               : ZP_ERR_CUDA;
+}
+
 zp_status zp_global_redundancy(zp_cache *c, const int32_t *block_tables, int32_t bt_stride,
                                int32_t num_rows, const int32_t *lengths, const int32_t *req_idx,
                                int32_t R, float *red_out, void *stream)

@@ -1,6 +1,6 @@
 // zp_aux.cuh -- launch arguments and launchers of the kernels off the
 // compression path: the all-keys redundancy ablation (zp_redundancy_global.cu)
-// and whole-request block allocation / release (zp_blocks.cu).  Internal: not
+// and whole-request block allocation / release / fork (zp_blocks.cu).  Internal: not
 // part of the C ABI.
 #pragma once
 
@@ -26,6 +26,10 @@ cudaError_t launch_alloc_rows(const Workspace &ws, int32_t *block_tables, int32_
                               int32_t num_rows, int32_t *lengths, const int32_t *req_idx,
                               int32_t R, const int32_t *counts, int32_t num_blocks,
                               const zp_block_pool *pool, cudaStream_t s);
+cudaError_t launch_fork_rows(const Workspace &ws, int32_t *block_tables, int32_t bt_stride,
+                             int32_t num_rows, int32_t *lengths, const int32_t *src,
+                             const int32_t *dst, int32_t n, int32_t num_blocks, int32_t *refcount,
+                             cudaStream_t s);
 cudaError_t launch_release_rows(const Workspace &ws, int32_t *block_tables, int32_t bt_stride,
                                 int32_t num_rows, int32_t *lengths, const int32_t *req_idx,
                                 int32_t R, int32_t num_blocks, const zp_block_pool *pool,

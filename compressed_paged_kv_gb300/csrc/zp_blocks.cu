@@ -1,9 +1,10 @@
-// zp_blocks.cu -- whole-request block allocation and release.
+// zp_blocks.cu -- whole-request block allocation, release and fork.
 //
 // "Paged KV cache and continuous batching for LLMs" ("How it works"): blocks
 // are taken from the pool only as a request's tokens need them, a block's
-// reference counter counts the tables that point at it, and finished (or
-// preempted) requests leave the batch and give their blocks back.
+// reference counter counts the tables that point at it, finished (or
+// preempted) requests leave the batch and give their blocks back, and
+// parallel samples of one prompt share its blocks.
 //
 // Each call is one launch of one CTA: every check first, then -- only if all
 // pass -- every write, so a failed call changes nothing.  Pops and pushes keep
@@ -204,6 +205,58 @@ __global__ void __launch_bounds__(kPlanThreads) zp_release_rows_kernel(const Row
         *a.free_count = fc + pushes;
 }
 
+// Rows dst[i] become copies of rows src[i]: same entries, same length, one
+// more reference per block entry (atomics: several forks may share a block).
+__global__ void __launch_bounds__(kPlanThreads) zp_fork_rows_kernel(const RowsArgs a,
+                                                                    const int32_t *src,
+                                                                    const int32_t *dst, int n)
+{
+    __shared__ int s_err, s_gen;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        s_gen = row_stamp_gen(a);
+        s_err = 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += kPlanThreads) {
+        const int s = src[i], d = dst[i];
+        if (s < 0 || s >= a.num_rows || d < 0 || d >= a.num_rows || s == d) {
+            atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
+            continue;
+        }
+        if (atomicExch(&a.ws.ap_rowmark[d], s_gen) == s_gen || a.lengths[d] != 0)
+            atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
+    }
+    __syncthreads();
+    // every (pair, entry): destinations empty, sources valid and referenced;
+    // no destination is also a source of this call
+    for (int e = tid; e < n * a.stride && s_err == 0; e += kPlanThreads) {
+        const int i = e / a.stride, p = e - i * a.stride;
+        const int s = src[i], d = dst[i];
+        if (p == 0 && a.ws.ap_rowmark[s] == s_gen)
+            atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
+        const int blk = a.tables[(size_t)s * a.stride + p];
+        if (a.tables[(size_t)d * a.stride + p] >= 0 || blk >= a.num_blocks ||
+            (blk >= 0 && a.refcount[blk] < 1))
+            atomicCAS(&s_err, 0, ZP_ERR_INVALID_ARG);
+    }
+    __syncthreads();
+    if (s_err != 0) {
+        if (tid == 0)
+            set_error(a.ws.sticky, s_err);
+        return;
+    }
+    for (int e = tid; e < n * a.stride; e += kPlanThreads) {
+        const int i = e / a.stride, p = e - i * a.stride;
+        const int blk = a.tables[(size_t)src[i] * a.stride + p];
+        a.tables[(size_t)dst[i] * a.stride + p] = blk;
+        if (blk >= 0)
+            atomicAdd(&a.refcount[blk], 1);
+    }
+    for (int i = tid; i < n; i += kPlanThreads)
+        a.lengths[dst[i]] = a.lengths[src[i]];
+}
+
 }  // namespace zp
 
 namespace {
@@ -241,6 +294,20 @@ cudaError_t launch_alloc_rows(const Workspace &ws, int32_t *block_tables, int32_
     zp_alloc_rows_kernel<<<1, kPlanThreads, 0, s>>>(
         rows_args(ws, block_tables, bt_stride, num_rows, lengths, req_idx, R, counts, num_blocks,
                   pool));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fork_rows(const Workspace &ws, int32_t *block_tables, int32_t bt_stride,
+                             int32_t num_rows, int32_t *lengths, const int32_t *src,
+                             const int32_t *dst, int32_t n, int32_t num_blocks, int32_t *refcount,
+                             cudaStream_t s)
+{
+    zp_block_pool pool{};
+    pool.refcount = refcount;
+    zp_fork_rows_kernel<<<1, kPlanThreads, 0, s>>>(
+        rows_args(ws, block_tables, bt_stride, num_rows, lengths, nullptr, 0, nullptr, num_blocks,
+                  &pool),
+        src, dst, n);
     return cudaGetLastError();
 }
 

@@ -6,7 +6,7 @@ every call raises.
 The functions keep the C names (``zp_cache_create``, ``zp_compress``,
 ``zp_paged_decode_attn``, ``zp_append_slots``, ``zp_append_kv``,
 ``zp_compress_prefill``, ``zp_compress_prefill_workspace_size``, ``zp_global_redundancy``,
-``zp_alloc_rows``, ``zp_release_rows``,
+``zp_alloc_rows``, ``zp_release_rows``, ``zp_fork_rows``,
 ``zp_cache_status``, ``zp_cache_destroy``, ``zp_status_string``) and take raw integers (device pointers, a cudaStream_t
 as an int).  ``Cache`` wraps them for torch tensors: it reads ``data_ptr()``
 and the current stream, and keeps the pool tensors alive.
@@ -94,6 +94,8 @@ def lib():
         L.zp_alloc_rows.restype = I32
         L.zp_release_rows.argtypes = [P, P, I32, I32, P, P, I32, ctypes.POINTER(zp_block_pool), P]
         L.zp_release_rows.restype = I32
+        L.zp_fork_rows.argtypes = [P, P, I32, I32, P, P, P, I32, P, P]
+        L.zp_fork_rows.restype = I32
         L.zp_global_redundancy.argtypes = [P, P, I32, I32, P, P, I32, P, P]
         L.zp_global_redundancy.restype = I32
         L.zp_cache_status.argtypes = [P, P, ctypes.POINTER(I32)]
@@ -196,6 +198,12 @@ def zp_release_rows(handle, block_tables, bt_stride, num_rows, lengths, req_idx,
                     pool: zp_block_pool, stream) -> int:
     return lib().zp_release_rows(P(handle), P(block_tables), bt_stride, num_rows, P(lengths),
                                  P(req_idx or None), R, ctypes.byref(pool), P(stream or None))
+
+
+def zp_fork_rows(handle, block_tables, bt_stride, num_rows, lengths, src_rows, dst_rows, n,
+                 refcount, stream) -> int:
+    return lib().zp_fork_rows(P(handle), P(block_tables), bt_stride, num_rows, P(lengths),
+                              P(src_rows), P(dst_rows), n, P(refcount), P(stream or None))
 
 
 def zp_global_redundancy(handle, block_tables, bt_stride, num_rows, lengths, req_idx, R, red_out,
@@ -343,6 +351,16 @@ class Cache:
                              _stream(stream))
         if check and st != OK:
             raise ZpError(st, "zp_release_rows")
+        return st
+
+    def fork_rows(self, block_tables, lengths, refcount, src_rows, dst_rows, stream=None,
+                  check=True):
+        st = zp_fork_rows(self.handle, block_tables.data_ptr(), block_tables.shape[1],
+                          block_tables.shape[0], lengths.data_ptr(), src_rows.data_ptr(),
+                          dst_rows.data_ptr(), src_rows.numel(), refcount.data_ptr(),
+                          _stream(stream))
+        if check and st != OK:
+            raise ZpError(st, "zp_fork_rows")
         return st
 
     def global_redundancy(self, block_tables, lengths, red_out, req_idx=None, R=None,

@@ -25,9 +25,9 @@
  *  - A handle serves at most one call of each entry point in flight at a
  *    time.  zp_compress may run concurrently with zp_paged_decode_attn and
  *    zp_append_kv on another stream when they touch disjoint requests.
- *    zp_compress, zp_compress_prefill, zp_append_slots, zp_alloc_rows and
- *    zp_release_rows change the free stack and refcounts: order them (one
- *    stream, or events).  More concurrency needs
+ *    zp_compress, zp_compress_prefill, zp_append_slots, zp_alloc_rows,
+ *    zp_release_rows and zp_fork_rows change the free stack or refcounts:
+ *    order them (one stream, or events).  More concurrency needs
  *    more handles.
  *
  * KV pool layout (one K pool and one V pool per layer, caller-owned):
@@ -321,6 +321,24 @@ zp_status zp_alloc_rows(zp_cache *cache, int32_t *block_tables, int32_t bt_strid
 zp_status zp_release_rows(zp_cache *cache, int32_t *block_tables, int32_t bt_stride,
                           int32_t num_rows, int32_t *lengths, const int32_t *req_idx, int32_t R,
                           const zp_block_pool *pool, void *stream);
+
+/* Forks requests ("How it works": parallel samples of one prompt share its
+ * blocks, whose reference counters count the tables pointing at them): row
+ * dst_rows[i], which must be empty (length 0, every entry < 0), becomes a copy
+ * of row src_rows[i] -- the same entries (a reserved empty block included) and
+ * the same length -- and every block entry gains one reference.  The next
+ * write of either row into a shared partial block copies it first
+ * (zp_append_slots).
+ *
+ *  src_rows, dst_rows  device int32 [n]; destinations distinct, none of them
+ *                      a source in the same call
+ *  refcount            device int32 [num_blocks], updated
+ * All-or-nothing: a bad or repeated row, a destination that is not empty, a
+ * source entry out of range or unreferenced -> ZP_ERR_INVALID_ARG in the
+ * sticky status.  Orders with every other call that changes the pool. */
+zp_status zp_fork_rows(zp_cache *cache, int32_t *block_tables, int32_t bt_stride,
+                       int32_t num_rows, int32_t *lengths, const int32_t *src_rows,
+                       const int32_t *dst_rows, int32_t n, int32_t *refcount, void *stream);
 
 /* Writes one layer's new-token keys and values into the slots zp_append_slots
  * reserved ("Paged KV cache and continuous batching for LLMs", "How it
