@@ -7,7 +7,7 @@
 // §1, §3, §5, Korean "방법론" A, C, E).
 //
 // One unit = (request, layer, kv head) = T = N_max * b cached tokens.  A
-// cluster of `cs` CTAs owns the unit (cs = 1 up to 1024 tokens); CTA c owns
+// cluster of `cs` CTAs owns the unit (cs = 1 up to 2048 tokens); CTA c owns
 // the chunk of TC = T / cs tokens starting at c * TC.  Each CTA is 8
 // consumer warps (two groups of four taking alternate stages) and one
 // producer warp.  The producer streams the chunk through a ring of NS
@@ -32,6 +32,14 @@
 // complemented index, a per-CTA rank merge into a sorted list, and a merge
 // of the cluster's sorted lists (ranks by binary search for up to four
 // lists, else b steps of a k-way merge).
+//
+// Launch: the kernel may start while the one-CTA plan kernel still runs
+// (programmatic dependent launch).  Passes 1 and 2 need nothing from the
+// plan; griddepcontrol.wait comes before pass 2's first global write
+// (consumers) and before pass 3's bulk reads (producer), and the plan's
+// verdict word, written by nobody else, decides uniformly whether the CTA
+// selects and compacts.  Until then only bounds-safe reads happen: TMA loads
+// (bounded by the tensor map) and bounds-checked table rows and block ids.
 //
 // In-place safety: exactly b tokens are evicted, so destination j reads
 // source kept[j] with j <= kept[j] <= j + b.  Pass 3 handles the chunk's
