@@ -16,7 +16,9 @@
  *  - bf16 tensors are passed as void* and hold IEEE bfloat16 values.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Every call only enqueues work on `stream`: nothing
- *    synchronises except zp_cache_status.
+ *    synchronises except zp_cache_status, and nothing allocates after
+ *    zp_cache_create, so every call but zp_cache_status can be captured into
+ *    a CUDA graph and replayed.
  *  - Argument errors that the host can see are returned synchronously,
  *    before anything is enqueued.  Errors that only the device can see (a
  *    length or block id read from device memory, an empty free stack) are
