@@ -104,12 +104,17 @@ def test_mixed_sampled(orc):
 
 SHAPES = [
     # (name, changes) on top of the single-layer Qwen3-8B workload
-    ("T512_cluster4", dict(N=32, R=3)),
-    ("T1024_cluster8", dict(N=64, R=2)),
-    ("T4096_wide", dict(N=256, R=2)),
+    # up to 2048 tokens one CTA owns a unit; beyond, a cluster of T / 2048 CTAs
+    # (rank merge of the candidates up to 4 CTAs, k-way merge above)
+    ("T512_one_cta", dict(N=32, R=3)),
+    ("T1024_one_cta", dict(N=64, R=2)),
+    ("T4096_cluster2", dict(N=256, R=2)),
+    ("T6144_cluster3", dict(N=384, R=1)),
     ("T8192_cluster4", dict(N=512, R=1)),
     ("T10240_cluster5_kway", dict(N=640, R=1)),
-    ("T384_single_cta", dict(N=24, R=2)),
+    ("T16384_cluster8_kway", dict(N=1024, R=1, Hkv=2, Hq=8)),
+    ("T32768_cluster16_kway", dict(N=2048, R=1, Hkv=2, Hq=8)),
+    ("T384_one_cta", dict(N=24, R=2)),
     ("d64_rows64", dict(d=64, N=32, w=16, R=2)),
     ("w1_G1", dict(Hq=8, w=1, N=16, R=3)),
     ("G8_rows64", dict(Hkv=2, Hq=16, N=16, w=8, R=2)),
