@@ -205,6 +205,9 @@ __device__ __forceinline__ uint32_t blk_swz(int row, int ch)
 template <int D, int MT, int NS>
 __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const CompressArgs a)
 {
+    // a stage is always consumed by the same group of warps (idx and g have the
+    // same parity in every pass), which the parity waits on its barriers need
+    static_assert(NS % 2 == 0, "the two consumer groups take alternate stages");
     using S = StreamSmem<D, MT, NS>;
     constexpr int ROWS = S::ROWS, SLAB = S::SLAB, STAGE = S::STAGE;
     constexpr int HALVES = D / 64;
@@ -472,11 +475,11 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                     if (m_new == -INFINITY)
                         continue;
                     float sum = rm[mt][hh] == -INFINITY ? 0.f
-                                                         : rsum[mt][hh] * exp2f(rm[mt][hh] - m_new);
+                                                         : rsum[mt][hh] * ex2_approx(rm[mt][hh] - m_new);
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
-                        sum += exp2f(acc[mt][nt][hh * 2] - m_new) +
-                               exp2f(acc[mt][nt][hh * 2 + 1] - m_new);
+                        sum += ex2_approx(acc[mt][nt][hh * 2] - m_new) +
+                               ex2_approx(acc[mt][nt][hh * 2 + 1] - m_new);
                     rm[mt][hh] = m_new;
                     rsum[mt][hh] = sum;
                 }
@@ -584,6 +587,15 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
 
         // ---- pass 2: importance and score of every key
         const size_t uo = ((size_t)l * a.R + r) * a.Hkv + h;
+        float gm[MT][2], ginv[MT][2];  // statistics of this lane's rows
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int rr = mt * 16 + (lane >> 2) + hh * 8;
+                gm[mt][hh] = sGm[rr];
+                ginv[mt][hh] = sGinv[rr];
+            }
         for (int g = 0; g < n_score; ++g, ++idx) {
             if ((g & 1) != grp)
                 continue;
@@ -603,10 +615,8 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int rr = mt * 16 + (lane >> 2) + hh * 8;
-                            v += exp2f(acc[mt][nt][hh * 2 + ee] - sGm[rr]) * sGinv[rr];
-                        }
+                        for (int hh = 0; hh < 2; ++hh)
+                            v += ex2_approx(acc[mt][nt][hh * 2 + ee] - gm[mt][hh]) * ginv[mt][hh];
                     v += __shfl_xor_sync(0xffffffffu, v, 4);
                     v += __shfl_xor_sync(0xffffffffu, v, 8);
                     v += __shfl_xor_sync(0xffffffffu, v, 16);

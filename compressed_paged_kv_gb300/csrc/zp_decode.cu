@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) zp_decode_kernel(const DecodeA
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
             const float m_new = fmaxf(m_run[hh], mx);
-            const float corr = exp2f(m_run[hh] - m_new);
+            const float corr = ex2_approx(m_run[hh] - m_new);
             m_run[hh] = m_new;
             l_run[hh] *= corr;
 #pragma unroll
@@ -177,8 +177,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) zp_decode_kernel(const DecodeA
             }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                sacc[nt][hh * 2] = exp2f(sacc[nt][hh * 2] - m_new);
-                sacc[nt][hh * 2 + 1] = exp2f(sacc[nt][hh * 2 + 1] - m_new);
+                sacc[nt][hh * 2] = ex2_approx(sacc[nt][hh * 2] - m_new);
+                sacc[nt][hh * 2 + 1] = ex2_approx(sacc[nt][hh * 2 + 1] - m_new);
                 l_run[hh] += sacc[nt][hh * 2] + sacc[nt][hh * 2 + 1];
             }
         }

@@ -542,6 +542,16 @@ __device__ __forceinline__ void st_global_v4(void *p, uint4 v)
                  : "memory");
 }
 
+// 2^x by the PTX instruction ex2.approx.ftz.f32 (relative error about 2^-22,
+// subnormal arguments and results flushed to zero, 2^-inf = +0): the
+// exponentials of the online softmax, whose sums tolerate both.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // fp32 -> u32 map that preserves order (-0.0 sorts just below +0.0).
 __device__ __forceinline__ uint32_t f32_order(float f)
 {

@@ -245,11 +245,11 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
                         continue;
                     float sum = rm[mt][hh] == -INFINITY
                                     ? 0.f
-                                    : rsum[mt][hh] * exp2f(rm[mt][hh] - m_new);
+                                    : rsum[mt][hh] * ex2_approx(rm[mt][hh] - m_new);
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
-                        sum += exp2f(acc[mt][nt][hh * 2] - m_new) +
-                               exp2f(acc[mt][nt][hh * 2 + 1] - m_new);
+                        sum += ex2_approx(acc[mt][nt][hh * 2] - m_new) +
+                               ex2_approx(acc[mt][nt][hh * 2 + 1] - m_new);
                     rm[mt][hh] = m_new;
                     rsum[mt][hh] = sum;
                 }
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
                             const int rr = mt * 16 + (lane >> 2) + hh * 8;
-                            v += exp2f(acc[mt][nt][hh * 2 + ee] - sGm[rr]) * sGinv[rr];
+                            v += ex2_approx(acc[mt][nt][hh * 2 + ee] - sGm[rr]) * sGinv[rr];
                         }
                     v += __shfl_xor_sync(0xffffffffu, v, 4);
                     v += __shfl_xor_sync(0xffffffffu, v, 8);

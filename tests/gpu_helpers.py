@@ -51,7 +51,9 @@ def make_cache(st: W.CacheState):
 class CompressRun:
     """One GPU compression of a cache state, with debug outputs."""
 
-    def __init__(self, st: W.CacheState, cache=None, debug=True):
+    def __init__(self, st: W.CacheState, cache=None, debug=True, with_scores=True):
+        """debug: ask for the kept indices; with_scores: also for the scores
+        (without them a one-CTA unit takes the pruned selection)."""
         wl = st.wl
         self.st = st
         self.cache = cache or make_cache(st)
@@ -60,7 +62,7 @@ class CompressRun:
         self.Rc = Rc
         dev = st.block_tables.device
         self.scores = (torch.full((wl.L, Rc, wl.Hkv, wl.T), float("nan"), device=dev)
-                       if debug else None)
+                       if debug and with_scores else None)
         self.kept = (torch.full((wl.L, Rc, wl.Hkv, (wl.N - 1) * wl.b), -1, dtype=torch.int32,
                                 device=dev) if debug else None)
 
@@ -108,17 +110,20 @@ class UnitReport:
 
 
 def check_unit(orc, wl, Ksrc, Vsrc, Q, s_gpu, kept_gpu, Kout, Vout):
-    """Ksrc/Vsrc: [T, d] uint16 source rows; Q: [G*w, d]; s_gpu [T] fp32;
-    kept_gpu [(N-1)b]; Kout/Vout [(N-1)b, d] uint16 compacted rows.
-    Returns (kept set identical to the oracle's, worst relative score error)."""
+    """Ksrc/Vsrc: [T, d] uint16 source rows; Q: [G*w, d]; s_gpu [T] fp32 (None:
+    not asked for); kept_gpu [(N-1)b]; Kout/Vout [(N-1)b, d] uint16 compacted
+    rows.  Returns (kept set identical to the oracle's, worst relative score
+    error)."""
     C, b = wl.C, wl.b
     imp, red, s = orc.unit_scores(Ksrc, Q, b, wl.w, wl.G, wl.lam)
     D = float(np.mean(np.abs(imp) + wl.lam * np.abs(red[:C])))
-    sg = s_gpu.astype(np.float64)
-    assert np.all(np.isposinf(sg[C:])), "window positions must hold +inf"
-    rel = np.abs(sg[:C] - s) / np.maximum(np.abs(s), D)
-    worst = float(rel.max())
-    assert worst <= SCORE_RTOL, f"score error {worst:.3e} > {SCORE_RTOL}"
+    worst = 0.0
+    if s_gpu is not None:
+        sg = s_gpu.astype(np.float64)
+        assert np.all(np.isposinf(sg[C:])), "window positions must hold +inf"
+        rel = np.abs(sg[:C] - s) / np.maximum(np.abs(s), D)
+        worst = float(rel.max())
+        assert worst <= SCORE_RTOL, f"score error {worst:.3e} > {SCORE_RTOL}"
     kept_o = orc.select(s, wl.w, wl.n_keep)
     kg = kept_gpu.astype(np.int64)
     assert kg.shape == kept_o.shape
@@ -137,10 +142,12 @@ def check_unit(orc, wl, Ksrc, Vsrc, Q, s_gpu, kept_gpu, Kout, Vout):
     return exact, worst
 
 
-def check_compress(orc, st: W.CacheState, sample_rows=None, sample_layers=None, threads=None):
+def check_compress(orc, st: W.CacheState, sample_rows=None, sample_layers=None, threads=None,
+                   with_scores=True):
     """Runs one GPU compression of `st` and checks it against the oracle on the
     units of `sample_rows` (compress-batch indices) x `sample_layers` x all kv
-    heads (all units when None).  Returns the UnitReport."""
+    heads (all units when None); with_scores=False runs it without the score
+    output (the pruned selection of one-CTA units).  Returns the UnitReport."""
     wl = st.wl
     Rc = st.window_q.shape[1]
     rows_c = np.arange(Rc) if sample_rows is None else np.asarray(sample_rows)
@@ -158,7 +165,7 @@ def check_compress(orc, st: W.CacheState, sample_rows=None, sample_layers=None, 
     shared_before = [(st.k_pools[l][shared].clone(), st.v_pools[l][shared].clone())
                      for l in layers]
 
-    run = CompressRun(st)
+    run = CompressRun(st, with_scores=with_scores)
     rc, dev = run.run()
     assert rc == zp.OK and dev == zp.OK, (rc, dev)
 
@@ -171,7 +178,7 @@ def check_compress(orc, st: W.CacheState, sample_rows=None, sample_layers=None, 
         assert torch.equal(st.v_pools[l][shared], shared_before[i][1]), "shared V block written"
 
     new_tab = st.block_tables[:, :wl.N - 1]
-    scores = run.scores.cpu().numpy()
+    scores = run.scores.cpu().numpy() if with_scores else None
     kept = run.kept.cpu().numpy()
     rep = UnitReport()
     jobs = []
@@ -182,7 +189,8 @@ def check_compress(orc, st: W.CacheState, sample_rows=None, sample_layers=None, 
         for j, rcmp in enumerate(rows_c):
             for h in range(wl.Hkv):
                 Q = wq[i, j, h * wl.G:(h + 1) * wl.G].reshape(-1, wl.d)
-                jobs.append((Ks[j, h], Vs[j, h], Q, scores[l, rcmp, h], kept[l, rcmp, h],
+                jobs.append((Ks[j, h], Vs[j, h], Q,
+                             None if scores is None else scores[l, rcmp, h], kept[l, rcmp, h],
                              Kn[j, h], Vn[j, h]))
     nthreads = threads or min(32, os.cpu_count() or 1)
     with concurrent.futures.ThreadPoolExecutor(nthreads) as ex:
