@@ -140,6 +140,7 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
     const size_t o_sticky = A.take(4);
     const size_t o_call = A.take(4);
     const size_t o_gens = A.take(8);
+    const size_t o_smw = A.take(4 * 3 * zp::kSmSlots);
     const size_t o_kmaps = A.take(sizeof(CUtensorMap) * D.num_layers, 128);
     const size_t o_vmaps = A.take(sizeof(CUtensorMap) * D.num_layers, 128);
     const size_t o_kp = A.take(sizeof(void *) * D.num_layers);
@@ -169,6 +170,7 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
     ws.sticky = reinterpret_cast<int32_t *>(b + o_sticky);
     ws.call = reinterpret_cast<int32_t *>(b + o_call);
     ws.gens = reinterpret_cast<int32_t *>(b + o_gens);
+    ws.smwave = reinterpret_cast<uint32_t *>(b + o_smw);
     ws.kmaps = reinterpret_cast<CUtensorMap *>(b + o_kmaps);
     ws.vmaps = reinterpret_cast<CUtensorMap *>(b + o_vmaps);
     ws.kpools = reinterpret_cast<void **>(b + o_kp);
@@ -297,6 +299,7 @@ zp_status zp_compress(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int
     ca.call = c->ws.call;
     ca.cstat = c->ws.counters + 2;
     ca.sticky = c->ws.sticky;
+    ca.smwave = c->ws.smwave;
     ca.L = c->L;
     ca.Hkv = c->Hkv;
     ca.Hq = c->Hq;

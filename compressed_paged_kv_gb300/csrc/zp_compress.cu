@@ -202,6 +202,8 @@ __global__ void __launch_bounds__(kPlanThreads) zp_finalize_kernel(const Finaliz
     __shared__ int s_fc;
     const int tid = threadIdx.x;
     pdl_wait();  // every write of the kernels before it is visible
+    for (int i = tid; i < 3 * kSmSlots; i += kPlanThreads)
+        a.ws.smwave[i] = 0u;  // the compression kernel's per-SM pairing, for the next call
     int st = *(volatile int32_t *)a.ws.call;
     if (st == 0)
         st = *(volatile int32_t *)(a.ws.counters + 2);

@@ -27,16 +27,18 @@
 // Between the passes the cluster exchanges the per-CTA softmax statistics
 // and the per-CTA candidates over distributed shared memory, signalled with
 // remote mbarrier arrivals (the producer never waits on them).  The b evicted
-// tokens: a warp radix select (MSB first, one bit per step by ballot) over
-// 64-bit keys = order-preserving image of the fp32 score bits above the
-// complemented index, a per-CTA rank merge into a sorted list, and a merge
-// of the cluster's sorted lists (ranks by binary search for up to four
-// lists, else b steps of a k-way merge).
+// tokens: over 64-bit keys = order-preserving image of the fp32 score bits
+// above the complemented index, a threshold (the largest of the warps' two
+// smallest keys) leaves a few dozen candidates that are ranked by brute force
+// (a warp radix select per warp when more than 256 remain), and a merge of
+// the cluster's sorted lists (ranks by binary search for up to four lists,
+// else b steps of a k-way merge).
 //
 // Launch: the kernel may start while the one-CTA plan kernel still runs
 // (programmatic dependent launch).  Passes 1 and 2 need nothing from the
-// plan; griddepcontrol.wait comes before pass 2's first global write
-// (consumers) and before pass 3's bulk reads (producer), and the plan's
+// plan; griddepcontrol.wait comes right after pass 1 (consumers: the plan's
+// destinations load during the statistics merge, before any global write)
+// and before pass 3's bulk reads (producer), and the plan's
 // verdict word, written by nobody else, decides uniformly whether the CTA
 // selects and compacts.  Until then only bounds-safe reads happen: TMA loads
 // (bounded by the tensor map) and bounds-checked table rows and block ids.
@@ -189,7 +191,9 @@ struct StreamSmem {
     static constexpr int off_ev = off_all + kMaxCluster * kBlk * 8;  // int [b]
     static constexpr int off_sblk = off_ev + kBlk * 4;          // int [kSMaxTC / b] source blocks
     static constexpr int off_dblk = off_sblk + kSMaxTC / kBlk * 4;  // int [.. + 1] destinations
-    static constexpr int off_bar = (off_dblk + (kSMaxTC / kBlk + 1) * 4 + 7) / 8 * 8;
+    static constexpr int off_nsel = off_dblk + (kSMaxTC / kBlk + 1) * 4;  // int: candidates
+    static constexpr int off_role = off_nsel + 4;  // int: first-wave pairing role, SM id
+    static constexpr int off_bar = (off_role + 4 + 7) / 8 * 8;
     static constexpr int NBAR = 2 * NS + 3;  // full[NS], empty[NS], tail, exchange 1, exchange 2
     static constexpr int BYTES = off_bar + NBAR * 8;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024 B
@@ -235,6 +239,8 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
     int *sEv = reinterpret_cast<int *>(sm + S::off_ev);
     int *sSblk = reinterpret_cast<int *>(sm + S::off_sblk);  // chunk block q -> source block
     int *sDblk = reinterpret_cast<int *>(sm + S::off_dblk);  // dst block of chunk block q-1+i
+    int *sNsel = reinterpret_cast<int *>(sm + S::off_nsel);
+    int *sRole = reinterpret_cast<int *>(sm + S::off_role);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::off_bar);
     uint64_t *full = bars, *empty = bars + NS;
     uint64_t *tailb = bars + 2 * NS, *xb1 = tailb + 1, *xb2 = tailb + 2;
@@ -274,6 +280,26 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
     for (int q = tid; q < nblk; q += kSThreads)
         sSblk[q] = src_row[blk0 + q];
     if (tid == 0) {
+        // First-wave pairing (one-CTA units).  At the start of a call every
+        // resident CTA would run the same phase at the same time, HBM idling
+        // while all of them score from L2.  The second CTA of this call on an
+        // SM therefore waits (at most 100 us) until the first has consumed
+        // pass 1, and the two run out of phase from then on.  Later
+        // CTAs, and CTAs whose partner has already finished, do not wait.
+        int role = 0;
+        const uint32_t smid = sm_id();
+        if (cs == 1 && a.smwave && smid < static_cast<uint32_t>(kSmSlots)) {
+            if (atomicCAS(a.smwave + smid, 0u, 1u) == 0u) {
+                role = 1;
+            } else if (atomicCAS(a.smwave + kSmSlots + smid, 0u, 1u) == 0u) {
+                role = 2;
+                const volatile uint32_t *flag = a.smwave + 2 * kSmSlots + smid;
+                const uint64_t t_start = globaltimer_ns();
+                while (*flag == 0u && globaltimer_ns() - t_start < 100000ull)
+                    __nanosleep(256);
+            }
+        }
+        *sRole = role | static_cast<int>(smid << 2);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kSGroupWarps);
@@ -521,6 +547,24 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
             }
             __syncwarp();
         }
+        if (tid == 0 && (*sRole & 3) == 1) {
+            // pass 1 consumed: the SM's second CTA of this call may start
+            __threadfence();
+            *reinterpret_cast<volatile uint32_t *>(a.smwave + 2 * kSmSlots + (*sRole >> 2)) = 1u;
+        }
+
+        // the plan's verdict and destinations (the plan kernel may have run
+        // alongside pass 1); the loads overlap the statistics merge
+        pdl_wait();
+        const bool live = *reinterpret_cast<volatile int32_t *>(a.call) == 0;
+        constexpr int kDblkPerThread = (kSMaxTC / kBlk + 1 + NCT - 1) / NCT;
+        int dblk_ld[kDblkPerThread];
+#pragma unroll
+        for (int i = 0; i < kDblkPerThread; ++i) {
+            const int q = tid + i * NCT, lb = blk0 - 1 + q;
+            dblk_ld[i] = (q <= nblk && live && lb >= 0 && lb < a.N - 1) ? dst_row[lb] : -1;
+        }
+
         // per-warp statistics: combine the four lanes of each row
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
@@ -540,24 +584,28 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                 }
             }
         named_sync(NCT);
+        // ... of the CTA; with a cluster, of all its CTAs
         if (tid < ROWS) {
             float m = -INFINITY, sum = 0.f;
 #pragma unroll
             for (int w2 = 0; w2 < kSW; ++w2)
                 lse_merge(m, sum, sRM[w2 * ROWS + tid], sRS[w2 * ROWS + tid]);
-            sStat[tid] = make_float2(m, sum);
+            if (cs > 1) {
+                sStat[tid] = make_float2(m, sum);
+            } else {
+                sGm[tid] = m;
+                sGinv[tid] = tid < a.rows && sum > 0.f ? 1.0f / sum : 0.f;
+            }
         }
-        named_sync(NCT);
         if (cs > 1) {
+            named_sync(NCT);
             cluster_wait();  // (the arrive right after set-up)
             if (tid == 0)
                 for (int c = 0; c < cs; ++c)
                     mbar_arrive_remote(dsmem_addr(xb1, c));
             bad |= !mbar_wait_cluster(xb1, 0);
-        }
-        if (tid < ROWS) {
-            float m = -INFINITY, sum = 0.f;
-            if (cs > 1) {
+            if (tid < ROWS) {
+                float m = -INFINITY, sum = 0.f;
                 float2 v[kMaxCluster];
 #pragma unroll
                 for (int c = 0; c < kMaxCluster; ++c)
@@ -566,23 +614,14 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
 #pragma unroll
                 for (int c = 0; c < kMaxCluster; ++c)
                     lse_merge(m, sum, v[c].x, v[c].y);
-            } else {
-                m = sStat[tid].x;
-                sum = sStat[tid].y;
+                sGm[tid] = m;
+                sGinv[tid] = tid < a.rows && sum > 0.f ? 1.0f / sum : 0.f;
             }
-            sGm[tid] = m;
-            sGinv[tid] = tid < a.rows && sum > 0.f ? 1.0f / sum : 0.f;
         }
-        named_sync(NCT);
-
-        // the plan's verdict and destinations (the plan kernel may have run
-        // alongside everything above)
-        pdl_wait();
-        const bool live = *reinterpret_cast<volatile int32_t *>(a.call) == 0;
-        for (int q = tid; q <= nblk; q += NCT) {
-            const int lb = blk0 - 1 + q;
-            sDblk[q] = (live && lb >= 0 && lb < a.N - 1) ? dst_row[lb] : -1;
-        }
+#pragma unroll
+        for (int i = 0; i < kDblkPerThread; ++i)
+            if (tid + i * NCT <= nblk)
+                sDblk[tid + i * NCT] = dblk_ld[i];
         named_sync(NCT);
 
         // ---- pass 2: importance and score of every key
@@ -637,11 +676,20 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
             if (cs > 1 && tid == 0)
                 bad |= !mbar_wait(tailb, 0);
         } else {
-            // ---- select the b evicted tokens
+            // ---- select the b evicted tokens: the CTA's b smallest keys (order
+            // image of the score above the complemented token index), sorted,
+            // into sPub.  The largest of the warps' two smallest keys has at
+            // least 2 kSW = b keys at or below it, so the b smallest are among
+            // the keys at or below it (usually a few dozen), which are ranked by
+            // brute force; above kCand of them each warp radix-selects its b
+            // smallest and those are ranked.
             {
+                static_assert(2 * kSW == kBlk, "two keys per warp make the threshold");
+                constexpr int kCand = kMaxCluster * kBlk;  // candidate list in sAll
                 const int KW = TC / kSW;  // keys of this warp
                 uint64_t key[kSKeysPerLane];
-    #pragma unroll
+                uint64_t m1 = ~0ull, m2 = ~0ull;
+#pragma unroll
                 for (int s2 = 0; s2 < kSKeysPerLane; ++s2) {
                     const int kk = lane + 32 * s2;
                     key[s2] = ~0ull;
@@ -651,20 +699,72 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                         key[s2] = (static_cast<uint64_t>(hi) << 32) |
                                   (0xffffffffu - static_cast<uint32_t>(tok));
                     }
+                    if (key[s2] < m1) {
+                        m2 = m1;
+                        m1 = key[s2];
+                    } else if (key[s2] < m2) {
+                        m2 = key[s2];
+                    }
                 }
-                uint32_t chosen[kSKeysPerLane];
-                warp_select_smallest<kSKeysPerLane>(key, kBlk, chosen);
-                warp_compact_keys<kSKeysPerLane>(key, chosen, sCand + wi * kBlk);
-            }
-            named_sync(NCT);
-            for (int t = tid; t < kSW * kBlk; t += NCT) {  // the CTA's b smallest, sorted
-                const uint64_t k0 = sCand[t];
-                int rank = 0;
-    #pragma unroll 8
-                for (int s2 = 0; s2 < kSW * kBlk; ++s2)
-                    rank += sCand[s2] < k0;
-                if (rank < kBlk)
-                    sPub[rank] = k0;
+                uint64_t g1 = m1;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const uint64_t x = __shfl_xor_sync(0xffffffffu, g1, o);
+                    g1 = x < g1 ? x : g1;
+                }
+                uint64_t g2 = m1 == g1 ? m2 : m1;  // keys are distinct
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const uint64_t x = __shfl_xor_sync(0xffffffffu, g2, o);
+                    g2 = x < g2 ? x : g2;
+                }
+                if (lane == 0)
+                    sCand[wi] = g2;
+                if (tid == 0)
+                    *sNsel = 0;
+                named_sync(NCT);
+                uint64_t theta = 0ull;
+#pragma unroll
+                for (int w2 = 0; w2 < kSW; ++w2)
+                    theta = sCand[w2] > theta ? sCand[w2] : theta;
+#pragma unroll
+                for (int s2 = 0; s2 < kSKeysPerLane; ++s2) {
+                    const bool take = key[s2] <= theta;
+                    const uint32_t bal = __ballot_sync(0xffffffffu, take);
+                    int base = 0;
+                    if (lane == 0 && bal)
+                        base = atomicAdd(sNsel, __popc(bal));
+                    base = __shfl_sync(0xffffffffu, base, 0);
+                    const int pos = base + __popc(bal & ((1u << lane) - 1u));
+                    if (take && pos < kCand)
+                        sAll[pos] = key[s2];
+                }
+                named_sync(NCT);
+                const int n = *sNsel;
+                if (n <= kCand) {
+                    for (int t = tid; t < n; t += NCT) {
+                        const uint64_t k0 = sAll[t];
+                        int rank = 0;
+                        for (int s2 = 0; s2 < n; ++s2)
+                            rank += sAll[s2] < k0;
+                        if (rank < kBlk)
+                            sPub[rank] = k0;
+                    }
+                } else {
+                    uint32_t chosen[kSKeysPerLane];
+                    warp_select_smallest<kSKeysPerLane>(key, kBlk, chosen);
+                    warp_compact_keys<kSKeysPerLane>(key, chosen, sCand + wi * kBlk);
+                    named_sync(NCT);
+                    for (int t = tid; t < kSW * kBlk; t += NCT) {
+                        const uint64_t k0 = sCand[t];
+                        int rank = 0;
+#pragma unroll 8
+                        for (int s2 = 0; s2 < kSW * kBlk; ++s2)
+                            rank += sCand[s2] < k0;
+                        if (rank < kBlk)
+                            sPub[rank] = k0;
+                    }
+                }
             }
             named_sync(NCT);
             if (cs > 1) {

@@ -16,6 +16,7 @@ constexpr int kMaxRows = 64;        // window rows per unit: w * (Hq / Hkv)
 constexpr int kMaxCluster = 16;     // CTAs per unit in the compression kernel
 constexpr uint32_t kWaitSpins = 1u << 22;  // bound on every mbarrier wait
 constexpr int kPlanThreads = 1024;  // the one-CTA bookkeeping kernels
+constexpr int kSmSlots = 256;       // SM ids tracked by the compression kernel's pairing
 
 // ----------------------------------------------------------------- workspace
 // Device memory the handle owns (allocated once in zp_cache_create).
@@ -25,6 +26,9 @@ struct Workspace {
     int32_t *gens;       // [2]  generation counters of the duplicate-row stamps
                          //      (compression, reservation), advanced on the device so
                          //      that a captured CUDA graph stamps afresh on every replay
+    uint32_t *smwave;    // [3 * kSmSlots] per SM id, within one compression call: first
+                         //      and second CTA claims, the first CTA's pass-1 flag;
+                         //      zeroed by the finalize kernel
     CUtensorMap *kmaps;  // [L]  K pool maps, 128B swizzle, box {64, 16}
     CUtensorMap *vmaps;  // [L]  V pool maps, same
     void **kpools;       // [L]  device copies of the pool pointers
@@ -89,6 +93,7 @@ struct CompressArgs {
     int32_t *call;   // the plan's verdict: only the plan writes it
     int32_t *cstat;  // the compaction's own status (a bounded wait that gave up)
     int32_t *sticky;
+    uint32_t *smwave;  // Workspace::smwave (null: no pairing)
     int32_t L, Hkv, Hq, R, N, w, rows, cs;
     int32_t num_rows, num_blocks;  // bounds for reads made before the plan's verdict
     float lambda;
@@ -550,6 +555,20 @@ __device__ __forceinline__ float ex2_approx(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t sm_id()
+{
+    uint32_t v;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+    return v;
 }
 
 // fp32 -> u32 map that preserves order (-0.0 sorts just below +0.0).
