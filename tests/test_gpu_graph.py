@@ -104,11 +104,14 @@ def test_decode_step_graph_replays_match_eager():
     assert triggered == due
 
 
-def test_compress_graph_replays_match_eager():
+@pytest.mark.parametrize("many", [False, True], ids=["few_units", "more_units_than_sms"])
+def test_compress_graph_replays_match_eager(many):
     """One captured compression replayed on restored inputs: every replay
     gives the eager result (this also checks that the duplicate-row stamps
-    advance on the device, not in the captured launch arguments)."""
-    wl = W.scaled(W.WORKLOADS["qwen3_1l"], name="graph", N=16, R=12, group=3, prefix_blocks=2,
+    advance on the device, not in the captured launch arguments, and that the
+    per-SM pairing words are reset between replays)."""
+    R = torch.cuda.get_device_properties(0).multi_processor_count // 8 + 3 if many else 12
+    wl = W.scaled(W.WORKLOADS["qwen3_1l"], name="graph", N=16, R=R, group=3, prefix_blocks=2,
                   spare_blocks=128)
     st0 = W.build_cache(wl, DEV)
     base = [t.clone() for t in st0.k_pools + st0.v_pools +

@@ -134,6 +134,36 @@ def test_shapes(orc, name, changes):
     H.check_decode(orc, st, wl.L - 1)
 
 
+def _num_sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("kind", ["tail_few", "tail_many", "T256", "d64_T512"])
+@pytest.mark.parametrize("with_scores", [True, False])
+def test_more_units_than_sms(orc, kind, with_scores):
+    """More one-CTA units than SMs, not a multiple of them (several waves,
+    the first-wave pairing on every SM, a ragged last wave): every unit is
+    checked against the oracle."""
+    S = _num_sms()
+    Hkv = 8
+    if kind == "tail_few":
+        R, changes = S // Hkv + 1, {}
+    elif kind == "tail_many":
+        R, changes = (2 * S - 8) // Hkv, {}
+    elif kind == "T256":
+        R, changes = S // Hkv + 3, dict(N=16)
+    else:
+        R, changes = S // Hkv + 2, dict(N=32, d=64)
+    wl = W.scaled(W.WORKLOADS["qwen3_1l"], name=f"units_{kind}", R=R, Hkv=Hkv, **changes)
+    units = wl.units()
+    assert units >= S and units % S != 0
+    st = W.build_cache(wl, DEV, with_decode_q=False)
+    rep = H.check_compress(orc, st, with_scores=with_scores)
+    assert rep.units == units
+    del st
+    _free()
+
+
 def _small_state(**changes):
     wl = W.scaled(W.WORKLOADS["qwen3_1l"], name="edge", **{**dict(N=8, R=3, spare_blocks=16),
                                                            **changes})
