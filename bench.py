@@ -60,6 +60,17 @@ def dist_setup():
     return world, rank, local
 
 
+def bf16_peak():
+    """Dense bf16 tensor peak (TFLOP/s) for a kernel timed alone."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -672,12 +683,25 @@ def run_gpu(args, world, rank, local):
         if i >= 2:
             abl.append(e0.elapsed_time(e1))
     abl_ms = sum(abl) / len(abl)
+    # ... and the same score from the dense T x T Gram of every unit on the
+    # tensor cores (the cost of the original method)
+    gram = []
+    for i in range(6):
+        flush.zero_()
+        e0.record()
+        cache.global_redundancy(st.block_tables, st.lengths, red_all, req_idx=req_idx, R=Rc,
+                                gram=True)
+        e1.record()
+        e1.synchronize()
+        if i >= 2:
+            gram.append(e0.elapsed_time(e1))
+    gram_ms = sum(gram) / len(gram)
     assert cache.status() == zp.OK
     del red_all
 
     # max over ranks
-    step_ms, comp_avg, dec_avg, e2e_ms, t_wall, abl_ms = reduce_max(
-        [step_ms, comp_avg, dec_avg, e2e_ms, t_wall, abl_ms], world, dev)
+    step_ms, comp_avg, dec_avg, e2e_ms, t_wall, abl_ms, gram_ms = reduce_max(
+        [step_ms, comp_avg, dec_avg, e2e_ms, t_wall, abl_ms, gram_ms], world, dev)
 
     if rank != 0:
         if world > 1:
@@ -743,6 +767,12 @@ def run_gpu(args, world, rank, local):
             "ms": abl_ms, "gbs": 2 * units * T * row / (abl_ms * 1e-3) / 1e9,
             "what": "zp_global_redundancy on the same units (two passes over K), outside the "
                     "timed step"},
+        "ablation_dense_gram": {
+            "ms": gram_ms, "tflops": 2.0 * units * T * T * wl.d / (gram_ms * 1e-3) / 1e12,
+            "peak_tflops": bf16_peak()[0], "peak_source": bf16_peak()[1],
+            "frac": 2.0 * units * T * T * wl.d / (gram_ms * 1e-3) / 1e12 / bf16_peak()[0],
+            "what": "zp_global_redundancy_gram: the same score from each unit's dense T x T Gram "
+                    "(tcgen05, 2 T^2 d FLOP per unit), outside the timed step"},
         "device_status": [status, status2],
     }
     res["clocks"] = clk.summary()

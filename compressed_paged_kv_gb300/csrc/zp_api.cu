@@ -708,6 +708,46 @@ zp_status zp_global_redundancy(zp_cache *c, const int32_t *block_tables, int32_t
                : ZP_ERR_CUDA;
 }
 
+zp_status zp_global_redundancy_gram(zp_cache *c, const int32_t *block_tables,
+                                    int32_t bt_stride, int32_t num_rows, const int32_t *lengths,
+                                    const int32_t *req_idx, int32_t R, float *red_out,
+                                    void *stream)
+{
+    if (!c || !block_tables || !lengths || !red_out || !aligned(red_out, 4))
+        return ZP_ERR_INVALID_ARG;
+    if (R < 0 || R > c->max_requests || num_rows < 1 || bt_stride < 1)
+        return ZP_ERR_INVALID_ARG;
+    if (static_cast<long long>(bt_stride) * c->b >= (1ll << 31))
+        return ZP_ERR_UNSUPPORTED;
+    const long long units = static_cast<long long>(R) * c->L * c->Hkv;
+    const int T_cap = bt_stride * c->b;
+    const int row_tiles = zp::gram_row_tiles(T_cap);
+    if (units * row_tiles >= (1ll << 31))
+        return ZP_ERR_UNSUPPORTED;
+    if (R == 0)
+        return ZP_OK;
+    if (!on_device(c))
+        return ZP_ERR_INVALID_ARG;
+    zp::GramRedArgs a{};
+    a.kmaps = c->ws.kmaps;
+    a.tables = block_tables;
+    a.stride = bt_stride;
+    a.num_rows = num_rows;
+    a.lengths = lengths;
+    a.req_idx = req_idx;
+    a.R = R;
+    a.Hkv = c->Hkv;
+    a.num_blocks = c->num_blocks;
+    a.T_cap = T_cap;
+    a.row_tiles = row_tiles;
+    a.red_out = red_out;
+    a.sticky = c->ws.sticky;
+    return zp::launch_gram_redundancy(a, c->d, static_cast<int>(units),
+                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ZP_OK
+               : ZP_ERR_CUDA;
+}
+
 zp_status zp_cache_status(zp_cache *c, void *stream, int32_t *out_status)
 {
     if (!c || !out_status)

@@ -22,6 +22,22 @@ struct GlobalRedArgs {
 
 cudaError_t launch_global_redundancy(const GlobalRedArgs &a, int d, int units, cudaStream_t s);
 
+// The same score from the dense Gram of every unit (zp_redundancy_gram.cu).
+struct GramRedArgs {
+    const CUtensorMap *kmaps;  // [L] the K pool maps (128-byte swizzle, box {64, 16})
+    const int32_t *tables;
+    int32_t stride, num_rows;
+    const int32_t *lengths;
+    const int32_t *req_idx;
+    int32_t R, Hkv, num_blocks, T_cap;
+    int32_t row_tiles;  // CTAs per unit: ceil(T_cap / 256)
+    float *red_out;     // [units][T_cap]
+    int32_t *sticky;
+};
+
+int gram_row_tiles(int T_cap);
+cudaError_t launch_gram_redundancy(const GramRedArgs &a, int d, int units, cudaStream_t s);
+
 cudaError_t launch_alloc_rows(const Workspace &ws, int32_t *block_tables, int32_t bt_stride,
                               int32_t num_rows, int32_t *lengths, const int32_t *req_idx,
                               int32_t R, const int32_t *counts, int32_t num_blocks,

@@ -1,0 +1,392 @@
+// zp_redundancy_gram.cu -- the all-keys redundancy of every key computed the
+// way the original score pays for it: from the dense T x T Gram matrix of
+// each (request, layer, kv head) unit, O(T^2 d), on the 5th-generation tensor
+// cores.  The Lightning Redundancy Score of the compression kernels replaces
+// this O(N^2 b^2) score by an O(N b^2) one (Zipage, gist.science: Dutch
+// "Methodologie" §5, Korean "방법론" E); zp_redundancy_global.cu computes the
+// same quantity in O(T d) through the sum of the normalised keys.  Result:
+// red_t = mean over the other keys k of the unit of cos(K_t, K_k), a zero key
+// having cosine 0 with every key.
+//
+// One CTA per (unit, 256 keys t): A = those 256 key rows as two halves of
+// 128, B = the unit's keys 128 at a time, D_g = A_g B^T (128 x 128 fp32 per
+// half, two buffers: all 512 tensor-memory columns), and
+//   sum_t = sum_k D[t][k] / |K_k|,   red_t = (sum_t / |K_t| - 1) / (T - 1)
+// (the k = t term is the 1 removed; columns past T are skipped).  Each B tile
+// feeds both halves: 256 rows of products per byte staged.  Ten warps:
+//   warp 0     TMA producer: A once, B through four stages (the K pool maps,
+//              128-byte swizzle, one 16-row box per cache block and 64 dims);
+//   warp 1     allocates the tensor memory, one lane issues tcgen05.mma
+//              (kind::f16, bf16 x bf16 -> fp32, M 128, N 128, K 16) for both
+//              halves and commits to mbarriers;
+//   warps 2-9  the inverse norms of each B stage's keys (one key each) from
+//              shared memory, then tcgen05.ld of their 32 lanes of one
+//              accumulator (warps 2-5 the first half, 6-9 the second) and
+//              weighted row sums in registers.
+// The accumulators alternate between two buffers, so the products of one B
+// tile overlap the reduction of the previous one.
+// Every wait is bounded; on a timeout the CTA records ZP_ERR_TIMEOUT, skips
+// its remaining work and still frees its tensor memory.
+#include "zp_aux.cuh"
+
+namespace zp {
+
+namespace {
+
+constexpr int kGramH = 128;                // keys t per accumulator (tensor-memory lanes)
+constexpr int kGramM = 2 * kGramH;         // keys t per CTA
+constexpr int kGramN = 128;                // keys k per product (accumulator columns)
+constexpr int kGramNS = 4;                 // B stages
+constexpr int kGramEW = 8;                 // reducing warps: 4 per accumulator half
+constexpr int kGramThreads = (2 + kGramEW) * 32;
+constexpr int kTmemCols = 4 * kGramN;      // [buffer][half] accumulators
+
+template <int D>
+struct GramSmem {
+    static constexpr int PANELS = D / 64;                 // 128-byte rows per key
+    static constexpr int A_PANEL = kGramH * 128;          // bytes of one half, one panel
+    static constexpr int B_PANEL = kGramN * 128;
+    static constexpr int A_BYTES = 2 * PANELS * A_PANEL;
+    static constexpr int B_STAGE = PANELS * B_PANEL;
+    static constexpr int off_a = 0;                       // [half][panel]
+    static constexpr int off_b = off_a + A_BYTES;         // kGramNS stages
+    static constexpr int off_inv = off_b + kGramNS * B_STAGE;  // float [kGramNS][kGramN]
+    static constexpr int off_bar = off_inv + kGramNS * kGramN * 4;
+    // fullA, fullB[NS], emptyB[NS], accFull[2], accEmpty[2]
+    static constexpr int NBAR = 1 + 2 * kGramNS + 4;
+    static constexpr int off_tmem = off_bar + NBAR * 8;   // u32: tensor-memory base
+    static constexpr int BYTES = off_tmem + 16;
+    static constexpr int ALLOC = BYTES + 1024;            // room to align the base to 1024 B
+};
+
+// Shared-memory matrix descriptor of a K-major operand stored as 128-byte
+// rows with the 128-byte swizzle (8-row groups 1024 bytes apart).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3ffffu) >> 4);       // start address
+    d |= static_cast<uint64_t>(16 >> 4) << 16;                 // leading byte offset (unused)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;               // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                       // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                       // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::f16 with bf16 A and B, fp32 accumulator,
+// both operands K-major, M = 128, N = 128.
+constexpr uint32_t kGramIdesc = (1u << 4)                       // D fp32
+                                | (1u << 7)                     // A bf16
+                                | (1u << 10)                    // B bf16
+                                | (static_cast<uint32_t>(kGramN >> 3) << 17)
+                                | (static_cast<uint32_t>(kGramH >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kGramIdesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives once on `bar` when every tcgen05.mma this thread issued before is done.
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's accumulator lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+        "[%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+// Sum of squares of the key row `row` of a staged operand (its 128-byte
+// rows; the swizzle permutes 16-byte chunks within a row, which a sum over
+// the row does not see).  The chunks are visited starting at row % 8, so
+// that neighbouring threads (neighbouring rows, 128 bytes apart) read
+// different banks.
+template <int PANELS>
+__device__ __forceinline__ float row_sq(const uint8_t *base, int panel_bytes, int row)
+{
+    float s = 0.f;
+#pragma unroll
+    for (int p = 0; p < PANELS; ++p) {
+        const uint32_t a = smem_u32(base + p * panel_bytes + row * 128);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint4 v = ld_shared_v4(a + ((j + row) & 7) * 16);
+            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(h[i]);
+                s = fmaf(f.x, f.x, s);
+                s = fmaf(f.y, f.y, s);
+            }
+        }
+    }
+    return s;
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(const GramRedArgs a)
+{
+    using S = GramSmem<D>;
+    constexpr int PANELS = S::PANELS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sA = sm + S::off_a;
+    uint8_t *sB = sm + S::off_b;
+    float *sInv = reinterpret_cast<float *>(sm + S::off_inv);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::off_bar);
+    uint64_t *fullA = bars, *fullB = bars + 1, *emptyB = bars + 1 + kGramNS,
+             *accFull = bars + 1 + 2 * kGramNS, *accEmpty = accFull + 2;
+    uint32_t *sTmem = reinterpret_cast<uint32_t *>(sm + S::off_tmem);
+
+    const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
+    const int u = static_cast<int>(blockIdx.x) / a.row_tiles;
+    const int h = u % a.Hkv, r = (u / a.Hkv) % a.R, l = u / (a.Hkv * a.R);
+    const int t0 = (static_cast<int>(blockIdx.x) - u * a.row_tiles) * kGramM;
+    int row = a.req_idx ? a.req_idx[r] : r;
+    const bool row_ok = row >= 0 && row < a.num_rows;
+    const int T = row_ok ? a.lengths[row] : 0;
+    if (!row_ok || T < 0 || T > a.stride * kBlk) {
+        if (tid == 0 && t0 == 0)
+            set_error(a.sticky, row_ok ? ZP_ERR_DEVICE_CHECK : ZP_ERR_INVALID_ARG);
+        return;  // uniform: before any barrier or tensor-memory allocation
+    }
+    if (t0 >= T)
+        return;
+    const int nblk = (T + kBlk - 1) / kBlk;  // cache blocks holding the unit's keys
+    const int n_tiles = (T + kGramN - 1) / kGramN;
+    const int32_t *trow = a.tables + (size_t)row * a.stride;
+    const CUtensorMap *kmap = a.kmaps + l;
+
+    if (tid == 0) {
+        mbar_init(fullA, 1);
+        for (int s = 0; s < kGramNS; ++s) {
+            mbar_init(&fullB[s], 1);
+            mbar_init(&emptyB[s], 2);  // the products' commit and the norms' arrival
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accFull[b], 1);
+            mbar_init(&accEmpty[b], kGramEW);  // one arrival per reducing warp
+        }
+        fence_mbar_init();
+    }
+    if (wi == 1) {  // the whole warp: allocation is warp-wide
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(sTmem)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    const uint32_t tmem = *sTmem;
+    bool bad = false;
+
+    // the y coordinate (pool row) of cache block q of the unit, or a negative
+    // one past the unit's blocks (the load then fills zeros)
+    auto block_y = [&](int q) {
+        if (q >= nblk)
+            return -kBlk;
+        const int blk = trow[q];
+        if (blk < 0 || blk >= a.num_blocks) {
+            set_error(a.sticky, ZP_ERR_DEVICE_CHECK);
+            return -kBlk;
+        }
+        return (blk * a.Hkv + h) * kBlk;
+    };
+
+    if (wi == 0) {
+        // ------------------------------------------------------- producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(fullA, S::A_BYTES);
+            for (int q = 0; q < kGramM / kBlk; ++q) {
+                const int y = block_y(t0 / kBlk + q);
+                const int g = q / (kGramH / kBlk), qq = q % (kGramH / kBlk);
+                for (int p = 0; p < PANELS; ++p)
+                    tma_load_2d(sA + (g * PANELS + p) * S::A_PANEL + qq * kBlk * 128, kmap,
+                                p * 64, y, fullA);
+            }
+            for (int t = 0; t < n_tiles; ++t) {
+                const int s = t % kGramNS;
+                if (t >= kGramNS)
+                    bad |= !mbar_wait(&emptyB[s], ((t / kGramNS) - 1) & 1);
+                mbar_arrive_expect_tx(&fullB[s], S::B_STAGE);
+                uint8_t *dst = sB + s * S::B_STAGE;
+                for (int q = 0; q < kGramN / kBlk; ++q) {
+                    const int y = block_y(t * (kGramN / kBlk) + q);
+                    for (int p = 0; p < PANELS; ++p)
+                        tma_load_2d(dst + p * S::B_PANEL + q * kBlk * 128, kmap, p * 64, y,
+                                    &fullB[s]);
+                }
+            }
+        }
+    } else if (wi == 1) {
+        // ------------------------------------------------------- products
+        if (lane == 0) {
+            bad |= !mbar_wait(fullA, 0);
+            for (int t = 0; t < n_tiles; ++t) {
+                const int s = t % kGramNS, b = t & 1;
+                bool ok = mbar_wait(&fullB[s], (t / kGramNS) & 1);
+                if (t >= 2)
+                    ok &= mbar_wait(&accEmpty[b], ((t >> 1) - 1) & 1);
+                bad |= !ok;
+                tmem_fence_after();
+                if (!bad) {
+                    const uint32_t bBase = smem_u32(sB + s * S::B_STAGE);
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t koff = (ks & 3) * 32u;  // 16 dims within a 128-byte row
+                        const uint64_t bd = sw128_desc(bBase + (ks >> 2) * S::B_PANEL + koff);
+#pragma unroll
+                        for (int g = 0; g < 2; ++g) {
+                            const uint64_t ad = sw128_desc(
+                                smem_u32(sA + (g * PANELS + (ks >> 2)) * S::A_PANEL) + koff);
+                            umma_bf16(tmem + static_cast<uint32_t>((b * 2 + g) * kGramN), ad, bd,
+                                      ks > 0);
+                        }
+                    }
+                }
+                umma_commit(&emptyB[s]);    // this stage's operands are read
+                umma_commit(&accFull[b]);  // both halves of buffer b are complete
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- reduction
+        constexpr int NR = kGramEW * 32;
+        const int e = tid - 64;              // 0 .. NR-1 = 0 .. 255
+        const int quarter = wi & 3;          // tensor-memory lanes 32*quarter ..
+        const int g = (wi - 2) >> 2;         // accumulator (half of the CTA's keys)
+        const int tr = quarter * 32 + lane;  // this thread's key t0 + g*128 + tr
+        bad |= !mbar_wait(fullA, 0);
+        float sum = 0.f;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int s = t % kGramNS, b = t & 1;
+            bad |= !mbar_wait(&fullB[s], (t / kGramNS) & 1);
+            if (e < kGramN) {  // inverse norm of this stage's key e
+                const int k = t * kGramN + e;
+                const float sq = row_sq<PANELS>(sB + s * S::B_STAGE, S::B_PANEL, e);
+                sInv[s * kGramN + e] = (k < T && sq > 0.f) ? rsqrtf(sq) : 0.f;
+            }
+            named_sync(NR);
+            if (e == 0)
+                mbar_arrive(&emptyB[s]);
+            bad |= !mbar_wait(&accFull[b], (t >> 1) & 1);
+            tmem_fence_after();
+            bad = __any_sync(0xffffffffu, bad);  // tcgen05.ld is warp-collective
+            if (!bad) {
+                const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>((b * 2 + g) * kGramN);
+                const float4 *inv = reinterpret_cast<const float4 *>(sInv + s * kGramN);
+                const int lim = T - t * kGramN;  // columns at and past it are not keys
+#pragma unroll 1
+                for (int ch = 0; ch < kGramN / 32; ++ch) {
+                    float v[32];
+                    tmem_ld32(tbase + ch * 32, v);
+                    if (ch * 32 + 32 <= lim) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 w = inv[ch * 8 + i];
+                            sum = fmaf(v[4 * i], w.x, sum);
+                            sum = fmaf(v[4 * i + 1], w.y, sum);
+                            sum = fmaf(v[4 * i + 2], w.z, sum);
+                            sum = fmaf(v[4 * i + 3], w.w, sum);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (ch * 32 + i < lim)
+                                sum = fmaf(v[i], sInv[s * kGramN + ch * 32 + i], sum);
+                    }
+                }
+            }
+            tmem_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&accEmpty[b]);
+        }
+        const int tt = t0 + g * kGramH + tr;
+        if (tt < T && !bad) {
+            const float sq_t = row_sq<PANELS>(sA + g * PANELS * S::A_PANEL, S::A_PANEL, tr);
+            const float inv_t = sq_t > 0.f ? rsqrtf(sq_t) : 0.f;
+            const float pairs = T > 1 ? 1.0f / static_cast<float>(T - 1) : 0.f;
+            a.red_out[(size_t)u * a.T_cap + tt] =
+                inv_t > 0.f ? (sum * inv_t - 1.0f) * pairs : 0.f;
+        }
+    }
+    if (bad)
+        set_error(a.sticky, ZP_ERR_TIMEOUT);
+    tmem_fence_before();
+    __syncthreads();
+    if (wi == 1) {
+        tmem_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+template <int D>
+static cudaError_t launch_gram_t(const GramRedArgs &a, long long ctas, cudaStream_t s)
+{
+    using S = GramSmem<D>;
+    auto kern = zp_gram_redundancy_kernel<D>;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               S::ALLOC);
+    if (e != cudaSuccess)
+        return e;
+    kern<<<static_cast<unsigned>(ctas), kGramThreads, S::ALLOC, s>>>(a);
+    return cudaGetLastError();
+}
+
+int gram_row_tiles(int T_cap) { return (T_cap + kGramM - 1) / kGramM; }
+
+cudaError_t launch_gram_redundancy(const GramRedArgs &a, int d, int units, cudaStream_t s)
+{
+    const long long ctas = static_cast<long long>(units) * a.row_tiles;
+    if (ctas >= (1ll << 31))
+        return cudaErrorInvalidValue;
+    if (d == 64)
+        return launch_gram_t<64>(a, ctas, s);
+    if (d == 128)
+        return launch_gram_t<128>(a, ctas, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace zp

@@ -6,6 +6,7 @@ every call raises.
 The functions keep the C names (``zp_cache_create``, ``zp_compress``,
 ``zp_paged_decode_attn``, ``zp_append_slots``, ``zp_append_kv``,
 ``zp_compress_prefill``, ``zp_compress_prefill_workspace_size``, ``zp_global_redundancy``,
+``zp_global_redundancy_gram``,
 ``zp_alloc_rows``, ``zp_release_rows``, ``zp_fork_rows``,
 ``zp_cache_status``, ``zp_cache_destroy``, ``zp_status_string``) and take raw integers (device pointers, a cudaStream_t
 as an int).  ``Cache`` wraps them for torch tensors: it reads ``data_ptr()``
@@ -98,6 +99,8 @@ def lib():
         L.zp_fork_rows.restype = I32
         L.zp_global_redundancy.argtypes = [P, P, I32, I32, P, P, I32, P, P]
         L.zp_global_redundancy.restype = I32
+        L.zp_global_redundancy_gram.argtypes = [P, P, I32, I32, P, P, I32, P, P]
+        L.zp_global_redundancy_gram.restype = I32
         L.zp_cache_status.argtypes = [P, P, ctypes.POINTER(I32)]
         L.zp_cache_status.restype = I32
         L.zp_status_string.argtypes = [I32]
@@ -211,6 +214,13 @@ def zp_global_redundancy(handle, block_tables, bt_stride, num_rows, lengths, req
     return lib().zp_global_redundancy(P(handle), P(block_tables), bt_stride, num_rows,
                                       P(lengths), P(req_idx or None), R, P(red_out),
                                       P(stream or None))
+
+
+def zp_global_redundancy_gram(handle, block_tables, bt_stride, num_rows, lengths, req_idx, R,
+                              red_out, stream) -> int:
+    return lib().zp_global_redundancy_gram(P(handle), P(block_tables), bt_stride, num_rows,
+                                           P(lengths), P(req_idx or None), R, P(red_out),
+                                           P(stream or None))
 
 
 def zp_cache_status(handle, stream) -> tuple[int, int]:
@@ -364,14 +374,17 @@ class Cache:
         return st
 
     def global_redundancy(self, block_tables, lengths, red_out, req_idx=None, R=None,
-                          stream=None, check=True):
+                          stream=None, check=True, gram=False):
+        """gram=False: zp_global_redundancy (O(T d)); gram=True:
+        zp_global_redundancy_gram (the dense Gram on the tensor cores)."""
         if R is None:
             R = req_idx.numel() if req_idx is not None else block_tables.shape[0]
-        st = zp_global_redundancy(self.handle, block_tables.data_ptr(), block_tables.shape[1],
-                                  block_tables.shape[0], lengths.data_ptr(), _ptr(req_idx), R,
-                                  red_out.data_ptr(), _stream(stream))
+        fn = zp_global_redundancy_gram if gram else zp_global_redundancy
+        st = fn(self.handle, block_tables.data_ptr(), block_tables.shape[1],
+                block_tables.shape[0], lengths.data_ptr(), _ptr(req_idx), R,
+                red_out.data_ptr(), _stream(stream))
         if check and st != OK:
-            raise ZpError(st, "zp_global_redundancy")
+            raise ZpError(st, fn.__name__)
         return st
 
     def status(self, stream=None) -> int:

@@ -377,6 +377,18 @@ zp_status zp_global_redundancy(zp_cache *cache, const int32_t *block_tables, int
                                int32_t num_rows, const int32_t *lengths, const int32_t *req_idx,
                                int32_t R, float *red_out, void *stream);
 
+/* The same score as zp_global_redundancy, computed the way the original
+ * O(N^2 b^2) method pays for it: the dense T_i x T_i Gram matrix of every
+ * unit on the tensor cores (tcgen05, bf16 products, fp32 accumulation in
+ * tensor memory), red[t] = (sum_k cos(K_t, K_k) - 1) / (T_i - 1) from its
+ * rows.  For comparison only; O(T^2 d) work per unit.  Arguments, output
+ * layout and error reporting as zp_global_redundancy; a wait that runs out
+ * records ZP_ERR_TIMEOUT. */
+zp_status zp_global_redundancy_gram(zp_cache *cache, const int32_t *block_tables,
+                                    int32_t bt_stride, int32_t num_rows, const int32_t *lengths,
+                                    const int32_t *req_idx, int32_t R, float *red_out,
+                                    void *stream);
+
 /* Synchronises `stream`, returns the handle's sticky device status in
  * *out_status (ZP_OK or the first device-detected error since the last
  * read) and clears it.  Returns ZP_ERR_CUDA if the stream reports an error. */

@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
     for n in ("zp_cache_create", "zp_cache_destroy", "zp_compress", "zp_paged_decode_attn",
               "zp_cache_status", "zp_status_string", "zp_append_slots", "zp_append_kv",
               "zp_compress_prefill", "zp_compress_prefill_workspace_size",
-              "zp_global_redundancy", "zp_alloc_rows", "zp_release_rows",
+              "zp_global_redundancy", "zp_global_redundancy_gram", "zp_alloc_rows",
+              "zp_release_rows",
               "zp_fork_rows"):
         assert n in names
 

@@ -1,7 +1,8 @@
-"""GPU parity of the all-keys redundancy ablation (zp_global_redundancy)
-against the oracle's pair-by-pair definition: per unit, |r_gpu - r_orc| <=
-1e-4 * max(|r_orc|, mean |r_orc|) (fp32 sums of normalised keys against fp64
-pairwise cosines)."""
+"""GPU parity of the all-keys redundancy ablation against the oracle's
+pair-by-pair definition, for both kernels: zp_global_redundancy (sums of the
+normalised keys) and zp_global_redundancy_gram (the dense Gram of every unit
+on the tensor cores).  Per unit, |r_gpu - r_orc| <= 1e-4 * max(|r_orc|,
+mean |r_orc|) (fp32 against fp64 pairwise cosines)."""
 from __future__ import annotations
 
 import numpy as np
@@ -23,8 +24,10 @@ def gather(pool, table_row, T, h):
     return W.bf16_bits(x.reshape(n * 16, -1)[:T])
 
 
-@pytest.mark.parametrize("lens,d", [([2048, 1000, 17, 16, 1, 300], 128), ([700, 64, 5], 64)])
-def test_global_redundancy_matches_pairwise(orc, lens, d):
+@pytest.mark.parametrize("gram", [False, True], ids=["sum_of_keys", "dense_gram"])
+@pytest.mark.parametrize("lens,d", [([2048, 1000, 17, 16, 1, 300], 128), ([700, 64, 5], 64),
+                                    ([4096, 257, 255, 129, 128], 128)])
+def test_global_redundancy_matches_pairwise(orc, lens, d, gram):
     c = W.prefill_cache(500 + d, lens, 8, L=2, Hkv=2, Hq=4, d=d, w=4, device=DEV)
     # a few zero keys: cosine 0 with everything, redundancy 0
     c["k_pools"][0][c["tables"][1, 0], 0, 3] = 0
@@ -32,7 +35,7 @@ def test_global_redundancy_matches_pairwise(orc, lens, d):
     cache = zp.Cache(c["k_pools"], c["v_pools"], c["Hq"], max_requests=len(lens),
                      max_blocks_per_req=c["stride"])
     red = torch.full((2, len(lens), 2, c["stride"] * 16), float("nan"), device=DEV)
-    cache.global_redundancy(c["tables"], c["lengths"], red)
+    cache.global_redundancy(c["tables"], c["lengths"], red, gram=gram)
     assert cache.status() == zp.OK
     got = red.cpu().numpy()
     worst = 0.0
@@ -48,15 +51,37 @@ def test_global_redundancy_matches_pairwise(orc, lens, d):
                 assert np.all(np.isnan(got[l, r, h, T:])), "written past the length"
                 if T <= 16:  # one block: the block-local score
                     assert np.allclose(want, orc.redundancy(K, 16), atol=1e-12)
-    print(f"[parity] global redundancy: max rel err {worst:.2e}")
+    print(f"[parity] global redundancy ({'dense Gram' if gram else 'sum of keys'}): "
+          f"max rel err {worst:.2e}")
     assert worst <= RTOL
 
 
-def test_global_redundancy_bad_length_is_flagged():
+def test_dense_gram_agrees_with_sum_of_keys_at_scale():
+    """The two kernels on the bench workload's 512 units (T = 2048, d = 128)."""
+    wl = W.WORKLOADS["qwen3_1l"]
+    st = W.build_cache(wl, DEV, with_decode_q=False)
+    cache = zp.Cache(st.k_pools, st.v_pools, wl.Hq, max_requests=wl.R,
+                     max_blocks_per_req=st.block_tables.shape[1])
+    shape = (wl.L, wl.R, wl.Hkv, st.block_tables.shape[1] * 16)
+    a = torch.full(shape, float("nan"), device=DEV)
+    b = torch.full(shape, float("nan"), device=DEV)
+    cache.global_redundancy(st.block_tables, st.lengths, a)
+    cache.global_redundancy(st.block_tables, st.lengths, b, gram=True)
+    assert cache.status() == zp.OK
+    T = wl.T
+    x, y = a[..., :T].double(), b[..., :T].double()
+    scale = x.abs().mean(dim=-1, keepdim=True)
+    rel = ((x - y).abs() / torch.maximum(x.abs(), scale)).max().item()
+    print(f"[parity] dense Gram vs sum of keys, 512 units: max rel diff {rel:.2e}")
+    assert rel <= 2 * RTOL
+
+
+@pytest.mark.parametrize("gram", [False, True], ids=["sum_of_keys", "dense_gram"])
+def test_global_redundancy_bad_length_is_flagged(gram):
     c = W.prefill_cache(510, [100], 8, L=1, Hkv=2, Hq=2, d=64, w=1, device=DEV)
     c["lengths"][0] = c["stride"] * 16 + 1
     cache = zp.Cache(c["k_pools"], c["v_pools"], 2, max_requests=1, max_blocks_per_req=c["stride"])
     red = torch.zeros(1, 1, 2, c["stride"] * 16, device=DEV)
-    cache.global_redundancy(c["tables"], c["lengths"], red)
+    cache.global_redundancy(c["tables"], c["lengths"], red, gram=gram)
     assert cache.status() == zp.ERR_DEVICE_CHECK
     assert torch.count_nonzero(red) == 0
