@@ -13,7 +13,8 @@
 // producer warp.  The producer streams the chunk through a ring of NS
 // shared-memory stages with TMA in three passes:
 //   pass 1  K blocks (tensor maps, 128-byte swizzle, kept in L2 for the
-//           next passes): window logits and the b x b Gram of every block on
+//           next passes where the reuse distance allows it): window logits
+//           and the b x b Gram of every block on
 //           the tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate);
 //           online row max / sum per window row; Lightning Redundancy Score;
 //   pass 2  the same K blocks again, in reverse order so that they come from
@@ -345,13 +346,21 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                     // pass 1 read last (still in L2), and pass 3, forwards,
                     // starts on the blocks pass 2 read last
                     const int gg = pass == 0 ? g : n_score - 1 - g;
+                    // L2 priority by the distance to the next read of the block:
+                    // pass 1 -> pass 2 it is short for the last blocks, pass 2 ->
+                    // pass 3 short for the first ones.  The lines a read cannot
+                    // keep until then (the first quarter read in pass 1, the
+                    // first half read in pass 2) leave first and do not displace
+                    // those that can be kept.
+                    const uint64_t pol =
+                        (pass == 0 ? g < n_score / 4 : g < n_score / 2) ? once : keep;
                     for (int i = 0; i < kSScoreBlocks; ++i) {
                         const int blk = sSblk[gg * kSScoreBlocks + i];
                         const int y = (blk * a.Hkv + h) * kBlk;
 #pragma unroll
                         for (int hf = 0; hf < HALVES; ++hf)
                             tma_load_2d_hint(dst + i * SLAB + hf * 2048, kmap, hf * 64, y,
-                                             &full[s], keep);
+                                             &full[s], pol);
                     }
                 }
             }
