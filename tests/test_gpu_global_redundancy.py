@@ -32,6 +32,11 @@ def test_global_redundancy_matches_pairwise(orc, lens, d, gram):
     # a few zero keys: cosine 0 with everything, redundancy 0
     c["k_pools"][0][c["tables"][1, 0], 0, 3] = 0
     c["k_pools"][1][c["tables"][0, 2], 1, 0] = 0
+    # the slots past each length in its last block hold NaN bits: never keys
+    for r, T in enumerate(lens):
+        if T % 16:
+            for l in range(2):
+                c["k_pools"][l][c["tables"][r, T // 16], :, T % 16:] = float("nan")
     cache = zp.Cache(c["k_pools"], c["v_pools"], c["Hq"], max_requests=len(lens),
                      max_blocks_per_req=c["stride"])
     red = torch.full((2, len(lens), 2, c["stride"] * 16), float("nan"), device=DEV)
