@@ -136,6 +136,21 @@ __global__ void __launch_bounds__(kDecThreads, 2) zp_decode_kernel(const DecodeA
     for (int i = 0; i < my_n; ++i) {
         const int s = i % kDecStages;
         ok &= mbar_wait(&my_bar[s], (i / kDecStages) & 1);
+        const int tok0 = (first + i * kDecWarps) * kBlk;
+        if (len - tok0 < kBlk) {
+            // the slots past the length of a partial last block: their keys get
+            // probability 0, but 0 times a NaN or infinite V element (stale or
+            // never-written pool bytes) is NaN, so their V rows are cleared
+            uint8_t *vd = my_stage + s * S::STAGE_BYTES + S::KV_BYTES;
+            const int fill = len - tok0;  // >= 1: the block holds a token below len
+            constexpr int CPR2 = D / 8;   // 16-byte chunks per row (over the 64-dim panels)
+            for (int c = lane; c < (kBlk - fill) * CPR2; c += 32) {
+                const int rr = fill + c / CPR2, ch = c % CPR2;
+                st_shared_v4(smem_u32(vd + (ch >> 3) * kBlk * 128 + rr * 128 + (ch & 7) * 16),
+                             make_uint4(0u, 0u, 0u, 0u));
+            }
+            __syncwarp();
+        }
         const uint32_t kb_base = smem_u32(my_stage + s * S::STAGE_BYTES);
         const uint32_t vb_base = kb_base + S::KV_BYTES;
         const int mi = lane >> 3;
@@ -148,7 +163,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) zp_decode_kernel(const DecodeA
             mma_bf16(sacc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], kb[0], kb[1]);
             mma_bf16(sacc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], kb[2], kb[3]);
         }
-        const int tok0 = (first + i * kDecWarps) * kBlk;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll

@@ -300,6 +300,20 @@ def test_decode_ragged_lengths(orc, d, Hkv, Hq):
     H.check_decode(orc, st, 0, lengths=lens, scale=0.05)
 
 
+def test_decode_ignores_slots_past_the_length(orc):
+    """NaN bits in the K and V slots past each length in its last block: the
+    output stays finite and equal to the oracle's."""
+    wl = W.scaled(W.WORKLOADS["qwen3_1l"], name="nan_tail", N=20, R=9, spare_blocks=8)
+    st = W.build_cache(wl, DEV)
+    lens = torch.tensor([0, 1, 15, 16, 17, 100, 255, 319, 320], dtype=torch.int32, device=DEV)
+    for r, T in enumerate(lens.tolist()):
+        if T % 16:
+            blk = st.block_tables[r, T // 16]
+            st.k_pools[0][blk, :, T % 16:] = float("nan")
+            st.v_pools[0][blk, :, T % 16:] = float("inf")
+    H.check_decode(orc, st, 0, lengths=lens)
+
+
 def test_decode_bad_length_is_flagged(orc):
     wl = W.scaled(W.WORKLOADS["tiny"], name="badlen")
     st = W.build_cache(wl, DEV)

@@ -162,6 +162,20 @@ def test_prefill_parity(orc, case):
     check_prefill(orc, c)
 
 
+def test_prefill_ignores_slots_past_the_length(orc):
+    """NaN bits in the unfilled slots of each prompt's last block (K and V)
+    change nothing: those slots are neither keys nor moved rows."""
+    lens = [131, 150, 207, 300, 511]
+    c = W.prefill_cache(431, lens, 8, L=2, Hkv=2, d=128, w=8, Hq=8, device=DEV)
+    for r, T in enumerate(lens):
+        if T % 16:
+            for l in range(2):
+                blk = c["tables"][r, T // 16]
+                c["k_pools"][l][blk, :, T % 16:] = float("nan")
+                c["v_pools"][l][blk, :, T % 16:] = float("nan")
+    check_prefill(orc, c)
+
+
 def test_prefill_subset_of_rows_then_decode(orc):
     """Only some rows compress (req_idx, in shuffled order); decode attention
     of every row afterwards matches the oracle."""
