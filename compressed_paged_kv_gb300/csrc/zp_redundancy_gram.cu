@@ -13,16 +13,17 @@
 // half, two buffers: all 512 tensor-memory columns), and
 //   sum_t = sum_k D[t][k] / |K_k|,   red_t = (sum_t / |K_t| - 1) / (T - 1)
 // (the k = t term is the 1 removed; columns past T are skipped).  Each B tile
-// feeds both halves: 256 rows of products per byte staged.  Ten warps:
+// feeds both halves: 256 rows of products per byte staged.  Eighteen warps:
 //   warp 0     TMA producer: A once, B through four stages (the K pool maps,
 //              128-byte swizzle, one 16-row box per cache block and 64 dims);
 //   warp 1     allocates the tensor memory, one lane issues tcgen05.mma
 //              (kind::f16, bf16 x bf16 -> fp32, M 128, N 128, K 16) for both
 //              halves and commits to mbarriers;
-//   warps 2-9  the inverse norms of each B stage's keys (one key each) from
-//              shared memory, then tcgen05.ld of their 32 lanes of one
-//              accumulator (warps 2-5 the first half, 6-9 the second) and
-//              weighted row sums in registers.
+//   warps 2-17 two sets of 8 (one per accumulator buffer, so consecutive
+//              tiles are reduced at the same time): the inverse norms of the
+//              set's B stages (one key per thread) from shared memory, then
+//              tcgen05.ld of 32 lanes of one half and weighted row sums in
+//              registers, the two sets' sums added at the end.
 // The accumulators alternate between two buffers, so the products of one B
 // tile overlap the reduction of the previous one.
 // Every wait is bounded; on a timeout the CTA records ZP_ERR_TIMEOUT, skips
@@ -37,7 +38,7 @@ constexpr int kGramH = 128;                // keys t per accumulator (tensor-mem
 constexpr int kGramM = 2 * kGramH;         // keys t per CTA
 constexpr int kGramN = 128;                // keys k per product (accumulator columns)
 constexpr int kGramNS = 4;                 // B stages
-constexpr int kGramEW = 8;                 // reducing warps: 4 per accumulator half
+constexpr int kGramEW = 16;                // reducing warps: 2 sets (one per buffer) of 8
 constexpr int kGramThreads = (2 + kGramEW) * 32;
 constexpr int kTmemCols = 4 * kGramN;      // [buffer][half] accumulators
 
@@ -51,7 +52,8 @@ struct GramSmem {
     static constexpr int off_a = 0;                       // [half][panel]
     static constexpr int off_b = off_a + A_BYTES;         // kGramNS stages
     static constexpr int off_inv = off_b + kGramNS * B_STAGE;  // float [kGramNS][kGramN]
-    static constexpr int off_bar = off_inv + kGramNS * kGramN * 4;
+    static constexpr int off_part = off_inv + kGramNS * kGramN * 4;  // float [2][kGramM]
+    static constexpr int off_bar = off_part + 2 * kGramM * 4;
     // fullA, fullB[NS], emptyB[NS], accFull[2], accEmpty[2]
     static constexpr int NBAR = 1 + 2 * kGramNS + 4;
     static constexpr int off_tmem = off_bar + NBAR * 8;   // u32: tensor-memory base
@@ -98,6 +100,11 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
         : "memory");
+}
+
+__device__ __forceinline__ void named_sync_id(uint32_t id, uint32_t threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ void tmem_fence_before() {
@@ -201,7 +208,7 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accFull[b], 1);
-            mbar_init(&accEmpty[b], kGramEW);  // one arrival per reducing warp
+            mbar_init(&accEmpty[b], kGramEW / 2);  // one arrival per warp of its set
         }
         fence_mbar_init();
     }
@@ -233,27 +240,37 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
 
     if (wi == 0) {
         // ------------------------------------------------------- producer
-        if (lane == 0) {
+        // the whole warp: lane q reads the id of the q-th block of a tile (one
+        // round trip for all of them), lane 0 issues the loads
+        constexpr int QA = kGramM / kBlk, QB = kGramN / kBlk;  // blocks per A, per B tile
+        static_assert(QA <= 32 && QB <= 32, "one block id per lane");
+        const int ya = lane < QA ? block_y(t0 / kBlk + lane) : 0;
+        if (lane == 0)
             mbar_arrive_expect_tx(fullA, S::A_BYTES);
-            for (int q = 0; q < kGramM / kBlk; ++q) {
-                const int y = block_y(t0 / kBlk + q);
-                const int g = q / (kGramH / kBlk), qq = q % (kGramH / kBlk);
+        for (int q = 0; q < QA; ++q) {
+            const int y = __shfl_sync(0xffffffffu, ya, q);
+            const int g = q / (kGramH / kBlk), qq = q % (kGramH / kBlk);
+            if (lane == 0)
                 for (int p = 0; p < PANELS; ++p)
                     tma_load_2d(sA + (g * PANELS + p) * S::A_PANEL + qq * kBlk * 128, kmap,
                                 p * 64, y, fullA);
-            }
-            for (int t = 0; t < n_tiles; ++t) {
-                const int s = t % kGramNS;
+        }
+        for (int t = 0; t < n_tiles; ++t) {
+            const int s = t % kGramNS;
+            const int yb = lane < QB ? block_y(t * QB + lane) : 0;
+            if (lane == 0) {
                 if (t >= kGramNS)
                     bad |= !mbar_wait(&emptyB[s], ((t / kGramNS) - 1) & 1);
                 mbar_arrive_expect_tx(&fullB[s], S::B_STAGE);
-                uint8_t *dst = sB + s * S::B_STAGE;
-                for (int q = 0; q < kGramN / kBlk; ++q) {
-                    const int y = block_y(t * (kGramN / kBlk) + q);
+            }
+            __syncwarp();
+            uint8_t *dst = sB + s * S::B_STAGE;
+            for (int q = 0; q < QB; ++q) {
+                const int y = __shfl_sync(0xffffffffu, yb, q);
+                if (lane == 0)
                     for (int p = 0; p < PANELS; ++p)
                         tma_load_2d(dst + p * S::B_PANEL + q * kBlk * 128, kmap, p * 64, y,
                                     &fullB[s]);
-                }
             }
         }
     } else if (wi == 1) {
@@ -289,23 +306,28 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
         __syncwarp();
     } else {
         // ------------------------------------------------------- reduction
-        constexpr int NR = kGramEW * 32;
-        const int e = tid - 64;              // 0 .. NR-1 = 0 .. 255
-        const int quarter = wi & 3;          // tensor-memory lanes 32*quarter ..
-        const int g = (wi - 2) >> 2;         // accumulator (half of the CTA's keys)
-        const int tr = quarter * 32 + lane;  // this thread's key t0 + g*128 + tr
+        // two sets of 8 warps, set b reducing the tiles of accumulator buffer b
+        // (t = b, b + 2, ...), each warp 32 lanes of one 128-key half
+        constexpr int NSET = kGramEW / 2 * 32;   // threads per set
+        const int w2 = wi - 2;                   // 0 .. 15
+        const int set = w2 >> 3;
+        const int es = (w2 & 7) * 32 + lane;     // 0 .. 255 within the set
+        const int quarter = wi & 3;              // tensor-memory lanes 32*quarter ..
+        const int g = (w2 & 7) >> 2;             // accumulator half (of the CTA's keys)
+        const int tr = quarter * 32 + lane;      // this thread's key t0 + g*128 + tr
+        float *sPart = reinterpret_cast<float *>(sm + S::off_part);
         bad |= !mbar_wait(fullA, 0);
         float sum = 0.f;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int s = t % kGramNS, b = t & 1;
+        for (int t = set; t < n_tiles; t += 2) {
+            const int s = t % kGramNS, b = set;
             bad |= !mbar_wait(&fullB[s], (t / kGramNS) & 1);
-            if (e < kGramN) {  // inverse norm of this stage's key e
-                const int k = t * kGramN + e;
-                const float sq = row_sq<PANELS>(sB + s * S::B_STAGE, S::B_PANEL, e);
-                sInv[s * kGramN + e] = (k < T && sq > 0.f) ? rsqrtf(sq) : 0.f;
+            if (es < kGramN) {  // inverse norm of this stage's key es
+                const int k = t * kGramN + es;
+                const float sq = row_sq<PANELS>(sB + s * S::B_STAGE, S::B_PANEL, es);
+                sInv[s * kGramN + es] = (k < T && sq > 0.f) ? rsqrtf(sq) : 0.f;
             }
-            named_sync(NR);
-            if (e == 0)
+            named_sync_id(1 + set, NSET);
+            if (es == 0)
                 mbar_arrive(&emptyB[s]);
             bad |= !mbar_wait(&accFull[b], (t >> 1) & 1);
             tmem_fence_after();
@@ -341,13 +363,16 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
             if (lane == 0)
                 mbar_arrive(&accEmpty[b]);
         }
+        sPart[set * kGramM + g * kGramH + tr] = sum;
+        named_sync_id(3, 2 * NSET);
         const int tt = t0 + g * kGramH + tr;
-        if (tt < T && !bad) {
+        if (set == 0 && tt < T && !bad) {
+            const float tot = sPart[g * kGramH + tr] + sPart[kGramM + g * kGramH + tr];
             const float sq_t = row_sq<PANELS>(sA + g * PANELS * S::A_PANEL, S::A_PANEL, tr);
             const float inv_t = sq_t > 0.f ? rsqrtf(sq_t) : 0.f;
             const float pairs = T > 1 ? 1.0f / static_cast<float>(T - 1) : 0.f;
             a.red_out[(size_t)u * a.T_cap + tt] =
-                inv_t > 0.f ? (sum * inv_t - 1.0f) * pairs : 0.f;
+                inv_t > 0.f ? (tot * inv_t - 1.0f) * pairs : 0.f;
         }
     }
     if (bad)
