@@ -30,7 +30,8 @@ struct GramRedArgs {
     const int32_t *lengths;
     const int32_t *req_idx;
     int32_t R, Hkv, num_blocks, T_cap;
-    int32_t row_tiles;  // CTAs per unit: ceil(T_cap / 256)
+    int32_t row_tiles;  // work items per unit: ceil(T_cap / 256)
+    int32_t units;      // (request, layer, kv head) units; set by the launcher
     float *red_out;     // [units][T_cap]
     int32_t *sticky;
 };

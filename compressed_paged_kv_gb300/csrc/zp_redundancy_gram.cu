@@ -8,14 +8,21 @@
 // red_t = mean over the other keys k of the unit of cos(K_t, K_k), a zero key
 // having cosine 0 with every key.
 //
-// One CTA per (unit, 256 keys t): A = those 256 key rows as two halves of
+// Work items are (unit, 256 keys t): A = those 256 key rows as two halves of
 // 128, B = the unit's keys 128 at a time, D_g = A_g B^T (128 x 128 fp32 per
 // half, two buffers: all 512 tensor-memory columns), and
 //   sum_t = sum_k D[t][k] / |K_k|,   red_t = (sum_t / |K_t| - 1) / (T - 1)
 // (the k = t term is the 1 removed; columns past T are skipped).  Each B tile
-// feeds both halves: 256 rows of products per byte staged.  Eighteen warps:
-//   warp 0     TMA producer: A once, B through four stages (the K pool maps,
-//              128-byte swizzle, one 16-row box per cache block and 64 dims);
+// feeds both halves: 256 rows of products per byte staged.  The kernel is
+// persistent: one CTA per SM takes items blockIdx.x, + gridDim.x, ... (the
+// row tiles of a unit are neighbouring items, run at the same time by
+// neighbouring CTAs, so the unit's keys are read from HBM about once), keeps
+// its tensor memory for the whole launch and runs the pipelines below
+// continuously from one item into the next.  Eighteen warps:
+//   warp 0     TMA producer: each item's A once it is free (its last products
+//              done and its row norms taken), B through four stages (the K
+//              pool maps, 128-byte swizzle, one 16-row box per cache block
+//              and 64 dims);
 //   warp 1     allocates the tensor memory, one lane issues tcgen05.mma
 //              (kind::f16, bf16 x bf16 -> fp32, M 128, N 128, K 16) for both
 //              halves and commits to mbarriers;
@@ -23,11 +30,13 @@
 //              tiles are reduced at the same time): the inverse norms of the
 //              set's B stages (one key per thread) from shared memory, then
 //              tcgen05.ld of 32 lanes of one half and weighted row sums in
-//              registers, the two sets' sums added at the end.
+//              registers, the two sets' sums added at the end of the item.
 // The accumulators alternate between two buffers, so the products of one B
 // tile overlap the reduction of the previous one.
-// Every wait is bounded; on a timeout the CTA records ZP_ERR_TIMEOUT, skips
-// its remaining work and still frees its tensor memory.
+// Every wait is bounded; after a timeout a warp records ZP_ERR_TIMEOUT and
+// stops waiting (it still passes every barrier its set passes, doing no
+// work), the producer waits for its copies in flight and the MMA lane for its
+// products before the tensor memory is freed.
 #include "zp_aux.cuh"
 
 namespace zp {
@@ -52,10 +61,10 @@ struct GramSmem {
     static constexpr int off_a = 0;                       // [half][panel]
     static constexpr int off_b = off_a + A_BYTES;         // kGramNS stages
     static constexpr int off_inv = off_b + kGramNS * B_STAGE;  // float [kGramNS][kGramN]
-    static constexpr int off_part = off_inv + kGramNS * kGramN * 4;  // float [2][kGramM]
-    static constexpr int off_bar = off_part + 2 * kGramM * 4;
-    // fullA, fullB[NS], emptyB[NS], accFull[2], accEmpty[2]
-    static constexpr int NBAR = 1 + 2 * kGramNS + 4;
+    static constexpr int off_part = off_inv + kGramNS * kGramN * 4;  // float [2][2][kGramM]
+    static constexpr int off_bar = off_part + 4 * kGramM * 4;
+    // fullA, fullB[NS], emptyB[NS], accFull[2], accEmpty[2], emptyA, done
+    static constexpr int NBAR = 1 + 2 * kGramNS + 4 + 2;
     static constexpr int off_tmem = off_bar + NBAR * 8;   // u32: tensor-memory base
     static constexpr int BYTES = off_tmem + 16;
     static constexpr int ALLOC = BYTES + 1024;            // room to align the base to 1024 B
@@ -178,30 +187,17 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
     float *sInv = reinterpret_cast<float *>(sm + S::off_inv);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::off_bar);
     uint64_t *fullA = bars, *fullB = bars + 1, *emptyB = bars + 1 + kGramNS,
-             *accFull = bars + 1 + 2 * kGramNS, *accEmpty = accFull + 2;
+             *accFull = bars + 1 + 2 * kGramNS, *accEmpty = accFull + 2, *emptyA = accEmpty + 2,
+             *done = emptyA + 1;
     uint32_t *sTmem = reinterpret_cast<uint32_t *>(sm + S::off_tmem);
 
     const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
-    const int u = static_cast<int>(blockIdx.x) / a.row_tiles;
-    const int h = u % a.Hkv, r = (u / a.Hkv) % a.R, l = u / (a.Hkv * a.R);
-    const int t0 = (static_cast<int>(blockIdx.x) - u * a.row_tiles) * kGramM;
-    int row = a.req_idx ? a.req_idx[r] : r;
-    const bool row_ok = row >= 0 && row < a.num_rows;
-    const int T = row_ok ? a.lengths[row] : 0;
-    if (!row_ok || T < 0 || T > a.stride * kBlk) {
-        if (tid == 0 && t0 == 0)
-            set_error(a.sticky, row_ok ? ZP_ERR_DEVICE_CHECK : ZP_ERR_INVALID_ARG);
-        return;  // uniform: before any barrier or tensor-memory allocation
-    }
-    if (t0 >= T)
-        return;
-    const int nblk = (T + kBlk - 1) / kBlk;  // cache blocks holding the unit's keys
-    const int n_tiles = (T + kGramN - 1) / kGramN;
-    const int32_t *trow = a.tables + (size_t)row * a.stride;
-    const CUtensorMap *kmap = a.kmaps + l;
+    const int n_items = a.units * a.row_tiles;
 
     if (tid == 0) {
         mbar_init(fullA, 1);
+        mbar_init(emptyA, 2);  // the item's last products and its row norms taken
+        mbar_init(done, 1);
         for (int s = 0; s < kGramNS; ++s) {
             mbar_init(&fullB[s], 1);
             mbar_init(&emptyB[s], 2);  // the products' commit and the norms' arrival
@@ -225,17 +221,29 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
     const uint32_t tmem = *sTmem;
     bool bad = false;
 
-    // the y coordinate (pool row) of cache block q of the unit, or a negative
-    // one past the unit's blocks (the load then fills zeros)
-    auto block_y = [&](int q) {
-        if (q >= nblk)
-            return -kBlk;
-        const int blk = trow[q];
-        if (blk < 0 || blk >= a.num_blocks) {
-            set_error(a.sticky, ZP_ERR_DEVICE_CHECK);
-            return -kBlk;
-        }
-        return (blk * a.Hkv + h) * kBlk;
+    // Item w: unit u = w / row_tiles (h fastest, then the request, then the
+    // layer), keys t0 .. t0 + 255.  Every role walks the same items in the
+    // same order, so the pipeline counters agree without communication.
+    struct Item {
+        int u, h, l, t0, T, nblk, n_tiles;
+        const int32_t *trow;
+        int state;  // 0 work, 1 nothing to do (t0 >= T), 2 bad length, 3 bad request index
+    };
+    auto decode = [&](int w) {
+        Item it;
+        it.u = w / a.row_tiles;
+        it.h = it.u % a.Hkv;
+        const int r = (it.u / a.Hkv) % a.R;
+        it.l = it.u / (a.Hkv * a.R);
+        it.t0 = (w - it.u * a.row_tiles) * kGramM;
+        const int row = a.req_idx ? a.req_idx[r] : r;
+        const bool row_ok = row >= 0 && row < a.num_rows;
+        it.T = row_ok ? a.lengths[row] : 0;
+        it.trow = a.tables + (size_t)(row_ok ? row : 0) * a.stride;
+        it.nblk = (it.T + kBlk - 1) / kBlk;  // cache blocks holding the unit's keys
+        it.n_tiles = (it.T + kGramN - 1) / kGramN;
+        it.state = !row_ok ? 3 : (it.T < 0 || it.T > a.stride * kBlk) ? 2 : it.t0 >= it.T ? 1 : 0;
+        return it;
     };
 
     if (wi == 0) {
@@ -243,48 +251,97 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
         // the whole warp: lane q reads the id of the q-th block of a tile (one
         // round trip for all of them), lane 0 issues the loads
         constexpr int QA = kGramM / kBlk, QB = kGramN / kBlk;  // blocks per A, per B tile
-        static_assert(QA <= 32 && QB <= 32, "one block id per lane");
-        const int ya = lane < QA ? block_y(t0 / kBlk + lane) : 0;
-        if (lane == 0)
-            mbar_arrive_expect_tx(fullA, S::A_BYTES);
-        for (int q = 0; q < QA; ++q) {
-            const int y = __shfl_sync(0xffffffffu, ya, q);
-            const int g = q / (kGramH / kBlk), qq = q % (kGramH / kBlk);
-            if (lane == 0)
-                for (int p = 0; p < PANELS; ++p)
+        static_assert(QA * PANELS <= 32 && QB * PANELS <= 32, "one box per lane");
+        // the y coordinate (pool row) of cache block q of the item's unit, or
+        // a negative one past the unit's blocks (the load then fills zeros)
+        auto block_y = [&](const Item &it, int q) {
+            if (q >= it.nblk)
+                return -kBlk;
+            const int blk = it.trow[q];
+            if (blk < 0 || blk >= a.num_blocks) {
+                set_error(a.sticky, ZP_ERR_DEVICE_CHECK);
+                return -kBlk;
+            }
+            return (blk * a.Hkv + it.h) * kBlk;
+        };
+        uint32_t ia = 0, gt = 0;  // items loaded, B tiles loaded (over all items)
+        for (int w = blockIdx.x; w < n_items && !bad; w += gridDim.x) {
+            const Item it = decode(w);
+            if (it.state != 0) {
+                if (it.state >= 2 && it.t0 == 0 && lane == 0)
+                    set_error(a.sticky, it.state == 2 ? ZP_ERR_DEVICE_CHECK : ZP_ERR_INVALID_ARG);
+                continue;
+            }
+            const CUtensorMap *kmap = a.kmaps + it.l;
+            const int ya = lane < QA ? block_y(it, it.t0 / kBlk + lane) : 0;
+            if (lane == 0) {
+                bad = ia > 0 && !mbar_wait(emptyA, (ia - 1) & 1);
+                if (!bad)
+                    mbar_arrive_expect_tx(fullA, S::A_BYTES);
+            }
+            bad = __shfl_sync(0xffffffffu, bad, 0);
+            if (bad)
+                break;
+            {  // one box (a block's 16 rows, 64 dims) per lane
+                const int q = lane / PANELS, p = lane % PANELS;
+                const int y = __shfl_sync(0xffffffffu, ya, q & 31);
+                const int g = q / (kGramH / kBlk), qq = q % (kGramH / kBlk);
+                if (q < QA)
                     tma_load_2d(sA + (g * PANELS + p) * S::A_PANEL + qq * kBlk * 128, kmap,
                                 p * 64, y, fullA);
-        }
-        for (int t = 0; t < n_tiles; ++t) {
-            const int s = t % kGramNS;
-            const int yb = lane < QB ? block_y(t * QB + lane) : 0;
-            if (lane == 0) {
-                if (t >= kGramNS)
-                    bad |= !mbar_wait(&emptyB[s], ((t / kGramNS) - 1) & 1);
-                mbar_arrive_expect_tx(&fullB[s], S::B_STAGE);
             }
-            __syncwarp();
-            uint8_t *dst = sB + s * S::B_STAGE;
-            for (int q = 0; q < QB; ++q) {
-                const int y = __shfl_sync(0xffffffffu, yb, q);
-                if (lane == 0)
-                    for (int p = 0; p < PANELS; ++p)
+            ++ia;
+            for (int t = 0; t < it.n_tiles; ++t) {
+                const int s = gt % kGramNS;
+                const int yb = lane < QB ? block_y(it, t * QB + lane) : 0;
+                if (lane == 0) {
+                    bad = gt >= kGramNS && !mbar_wait(&emptyB[s], ((gt / kGramNS) - 1) & 1);
+                    if (!bad)
+                        mbar_arrive_expect_tx(&fullB[s], S::B_STAGE);
+                }
+                bad = __shfl_sync(0xffffffffu, bad, 0);
+                if (bad)
+                    break;
+                uint8_t *dst = sB + s * S::B_STAGE;
+                {  // one box per lane
+                    const int q = lane / PANELS, p = lane % PANELS;
+                    const int y = __shfl_sync(0xffffffffu, yb, q & 31);
+                    if (q < QB)
                         tma_load_2d(dst + p * S::B_PANEL + q * kBlk * 128, kmap, p * 64, y,
                                     &fullB[s]);
+                }
+                ++gt;
             }
+        }
+        // every copy issued has landed before the CTA may exit (immediate
+        // unless a consumer gave up)
+        if (lane == 0) {
+            bool ok = ia == 0 || mbar_wait(fullA, (ia - 1) & 1);
+            for (uint32_t j = gt > kGramNS ? gt - kGramNS : 0; j < gt; ++j)
+                ok &= mbar_wait(&fullB[j % kGramNS], (j / kGramNS) & 1);
+            bad |= !ok;
         }
     } else if (wi == 1) {
         // ------------------------------------------------------- products
         if (lane == 0) {
-            bad |= !mbar_wait(fullA, 0);
-            for (int t = 0; t < n_tiles; ++t) {
-                const int s = t % kGramNS, b = t & 1;
-                bool ok = mbar_wait(&fullB[s], (t / kGramNS) & 1);
-                if (t >= 2)
-                    ok &= mbar_wait(&accEmpty[b], ((t >> 1) - 1) & 1);
-                bad |= !ok;
-                tmem_fence_after();
-                if (!bad) {
+            uint32_t ia = 0, gt = 0, use[2] = {0u, 0u};
+            for (int w = blockIdx.x; w < n_items && !bad; w += gridDim.x) {
+                const Item it = decode(w);
+                if (it.state != 0)
+                    continue;
+                if (!mbar_wait(fullA, ia & 1)) {
+                    bad = true;
+                    break;
+                }
+                for (int t = 0; t < it.n_tiles; ++t, ++gt) {
+                    const int s = gt % kGramNS, b = t & 1;
+                    const uint32_t j = use[b]++;
+                    if (!mbar_wait(&fullB[s], (gt / kGramNS) & 1) ||
+                        (j > 0 && !mbar_wait(&accEmpty[b], (j - 1) & 1))) {
+                        bad = true;
+                        break;
+                    }
+                    tmem_fence_after();
                     const uint32_t bBase = smem_u32(sB + s * S::B_STAGE);
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
@@ -298,81 +355,121 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
                                       ks > 0);
                         }
                     }
+                    umma_commit(&emptyB[s]);    // this stage's operands are read
+                    umma_commit(&accFull[b]);  // both halves of buffer b are complete
                 }
-                umma_commit(&emptyB[s]);    // this stage's operands are read
-                umma_commit(&accFull[b]);  // both halves of buffer b are complete
+                if (bad)
+                    break;
+                umma_commit(emptyA);  // the item's products no longer read A
+                ++ia;
             }
+            // every product issued is done before the tensor memory is freed
+            umma_commit(done);
+            bad |= !mbar_wait(done, 0);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------- reduction
-        // two sets of 8 warps, set b reducing the tiles of accumulator buffer b
-        // (t = b, b + 2, ...), each warp 32 lanes of one 128-key half
+        // two sets of 8 warps, set b reducing the tiles t = b, b + 2, ... of
+        // each item (accumulator buffer b), each warp 32 lanes of one 128-key
+        // half.  The barriers a set passes depend only on the items, never on
+        // a timeout, so a warp that gave up still passes all of them.
         constexpr int NSET = kGramEW / 2 * 32;   // threads per set
         const int w2 = wi - 2;                   // 0 .. 15
         const int set = w2 >> 3;
         const int es = (w2 & 7) * 32 + lane;     // 0 .. 255 within the set
         const int quarter = wi & 3;              // tensor-memory lanes 32*quarter ..
-        const int g = (w2 & 7) >> 2;             // accumulator half (of the CTA's keys)
+        const int g = (w2 & 7) >> 2;             // accumulator half (of the item's keys)
         const int tr = quarter * 32 + lane;      // this thread's key t0 + g*128 + tr
         float *sPart = reinterpret_cast<float *>(sm + S::off_part);
-        bad |= !mbar_wait(fullA, 0);
-        float sum = 0.f;
-        for (int t = set; t < n_tiles; t += 2) {
-            const int s = t % kGramNS, b = set;
-            bad |= !mbar_wait(&fullB[s], (t / kGramNS) & 1);
-            if (es < kGramN) {  // inverse norm of this stage's key es
-                const int k = t * kGramN + es;
-                const float sq = row_sq<PANELS>(sB + s * S::B_STAGE, S::B_PANEL, es);
-                sInv[s * kGramN + es] = (k < T && sq > 0.f) ? rsqrtf(sq) : 0.f;
+        uint32_t ia = 0, gt = 0, use = 0, ic = 0;
+        for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+            const Item it = decode(w);
+            if (it.state != 0)
+                continue;
+            const int T = it.T;
+            float inv_t = 0.f;
+            if (set == 0) {
+                // the norm of this thread's key t, before A is released (only
+                // set 0 waits for A: its arrival gates the next load, so the
+                // phase it waits for cannot be overtaken)
+                if (!bad)
+                    bad = !mbar_wait(fullA, ia & 1);
+                ++ia;
+                if (!bad) {
+                    const float sq_t =
+                        row_sq<PANELS>(sA + g * PANELS * S::A_PANEL, S::A_PANEL, tr);
+                    inv_t = sq_t > 0.f ? rsqrtf(sq_t) : 0.f;
+                }
+                named_sync_id(1, NSET);
+                if (es == 0)
+                    mbar_arrive(emptyA);
             }
-            named_sync_id(1 + set, NSET);
-            if (es == 0)
-                mbar_arrive(&emptyB[s]);
-            bad |= !mbar_wait(&accFull[b], (t >> 1) & 1);
-            tmem_fence_after();
-            bad = __any_sync(0xffffffffu, bad);  // tcgen05.ld is warp-collective
-            if (!bad) {
-                const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       static_cast<uint32_t>((b * 2 + g) * kGramN);
-                const float4 *inv = reinterpret_cast<const float4 *>(sInv + s * kGramN);
-                const int lim = T - t * kGramN;  // columns at and past it are not keys
+            float sum = 0.f;
+            for (int t = 0; t < it.n_tiles; ++t, ++gt) {
+                if ((t & 1) != set)
+                    continue;
+                const int s = gt % kGramNS, b = set;
+                const uint32_t j = use++;
+                if (!bad)
+                    bad = !mbar_wait(&fullB[s], (gt / kGramNS) & 1);
+                if (es < kGramN) {  // inverse norm of this stage's key es
+                    const int k = t * kGramN + es;
+                    const float sq =
+                        bad ? 0.f : row_sq<PANELS>(sB + s * S::B_STAGE, S::B_PANEL, es);
+                    sInv[s * kGramN + es] = (k < T && sq > 0.f) ? rsqrtf(sq) : 0.f;
+                }
+                named_sync_id(1 + set, NSET);
+                if (es == 0)
+                    mbar_arrive(&emptyB[s]);
+                if (!bad)
+                    bad = !mbar_wait(&accFull[b], j & 1);
+                tmem_fence_after();
+                bad = __any_sync(0xffffffffu, bad);  // tcgen05.ld is warp-collective
+                if (!bad) {
+                    const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                           static_cast<uint32_t>((b * 2 + g) * kGramN);
+                    const float4 *inv = reinterpret_cast<const float4 *>(sInv + s * kGramN);
+                    const int lim = T - t * kGramN;  // columns at and past it are not keys
 #pragma unroll 1
-                for (int ch = 0; ch < kGramN / 32; ++ch) {
-                    float v[32];
-                    tmem_ld32(tbase + ch * 32, v);
-                    if (ch * 32 + 32 <= lim) {
+                    for (int ch = 0; ch < kGramN / 32; ++ch) {
+                        float v[32];
+                        tmem_ld32(tbase + ch * 32, v);
+                        if (ch * 32 + 32 <= lim) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float4 w = inv[ch * 8 + i];
-                            sum = fmaf(v[4 * i], w.x, sum);
-                            sum = fmaf(v[4 * i + 1], w.y, sum);
-                            sum = fmaf(v[4 * i + 2], w.z, sum);
-                            sum = fmaf(v[4 * i + 3], w.w, sum);
+                            for (int i = 0; i < 8; ++i) {
+                                const float4 wv = inv[ch * 8 + i];
+                                sum = fmaf(v[4 * i], wv.x, sum);
+                                sum = fmaf(v[4 * i + 1], wv.y, sum);
+                                sum = fmaf(v[4 * i + 2], wv.z, sum);
+                                sum = fmaf(v[4 * i + 3], wv.w, sum);
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (ch * 32 + i < lim)
+                                    sum = fmaf(v[i], sInv[s * kGramN + ch * 32 + i], sum);
                         }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (ch * 32 + i < lim)
-                                sum = fmaf(v[i], sInv[s * kGramN + ch * 32 + i], sum);
                     }
                 }
+                tmem_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&accEmpty[b]);
             }
-            tmem_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&accEmpty[b]);
-        }
-        sPart[set * kGramM + g * kGramH + tr] = sum;
-        named_sync_id(3, 2 * NSET);
-        const int tt = t0 + g * kGramH + tr;
-        if (set == 0 && tt < T && !bad) {
-            const float tot = sPart[g * kGramH + tr] + sPart[kGramM + g * kGramH + tr];
-            const float sq_t = row_sq<PANELS>(sA + g * PANELS * S::A_PANEL, S::A_PANEL, tr);
-            const float inv_t = sq_t > 0.f ? rsqrtf(sq_t) : 0.f;
-            const float pairs = T > 1 ? 1.0f / static_cast<float>(T - 1) : 0.f;
-            a.red_out[(size_t)u * a.T_cap + tt] =
-                inv_t > 0.f ? (tot * inv_t - 1.0f) * pairs : 0.f;
+            // the two sets' partial sums, double-buffered by item: a set can
+            // be at most one item ahead of the other at this barrier
+            float *part = sPart + (ic & 1) * 2 * kGramM;
+            part[set * kGramM + g * kGramH + tr] = sum;
+            named_sync_id(3, 2 * NSET);
+            const int tt = it.t0 + g * kGramH + tr;
+            if (set == 0 && tt < T && !bad) {
+                const float tot = part[g * kGramH + tr] + part[kGramM + g * kGramH + tr];
+                const float pairs = T > 1 ? 1.0f / static_cast<float>(T - 1) : 0.f;
+                a.red_out[(size_t)it.u * a.T_cap + tt] =
+                    inv_t > 0.f ? (tot * inv_t - 1.0f) * pairs : 0.f;
+            }
+            ++ic;
         }
     }
     if (bad)
@@ -388,7 +485,7 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
 }
 
 template <int D>
-static cudaError_t launch_gram_t(const GramRedArgs &a, long long ctas, cudaStream_t s)
+static cudaError_t launch_gram_t(const GramRedArgs &a, int ctas, cudaStream_t s)
 {
     using S = GramSmem<D>;
     auto kern = zp_gram_redundancy_kernel<D>;
@@ -404,13 +501,24 @@ int gram_row_tiles(int T_cap) { return (T_cap + kGramM - 1) / kGramM; }
 
 cudaError_t launch_gram_redundancy(const GramRedArgs &a, int d, int units, cudaStream_t s)
 {
-    const long long ctas = static_cast<long long>(units) * a.row_tiles;
-    if (ctas >= (1ll << 31))
+    const long long items = static_cast<long long>(units) * a.row_tiles;
+    if (items >= (1ll << 31))
         return cudaErrorInvalidValue;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return e;
+    GramRedArgs b = a;
+    b.units = units;
+    const int ctas = static_cast<int>(items < sms ? items : sms);  // one CTA per SM
+    if (ctas < 1)
+        return cudaSuccess;
     if (d == 64)
-        return launch_gram_t<64>(a, ctas, s);
+        return launch_gram_t<64>(b, ctas, s);
     if (d == 128)
-        return launch_gram_t<128>(a, ctas, s);
+        return launch_gram_t<128>(b, ctas, s);
     return cudaErrorInvalidValue;
 }
 

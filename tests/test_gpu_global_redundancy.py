@@ -90,3 +90,44 @@ def test_global_redundancy_bad_length_is_flagged(gram):
     cache.global_redundancy(c["tables"], c["lengths"], red, gram=gram)
     assert cache.status() == zp.ERR_DEVICE_CHECK
     assert torch.count_nonzero(red) == 0
+
+
+def test_dense_gram_many_items_per_cta(orc):
+    """Ragged lengths over more work items than the persistent kernel has CTAs
+    (384 units x 6 row tiles: about 15 items per CTA, items past a unit's
+    length skipped, odd tile counts): a seeded sample of units against the
+    oracle, every unit against the sum-of-keys kernel, nothing written past a
+    length."""
+    rng = np.random.default_rng(515)
+    lens = [int(x) for x in rng.integers(1, 1500, size=24)]
+    lens[0], lens[1] = 1500, 129
+    c = W.prefill_cache(515, lens, 8, L=2, Hkv=8, Hq=8, d=128, w=4, device=DEV)
+    cache = zp.Cache(c["k_pools"], c["v_pools"], c["Hq"], max_requests=len(lens),
+                     max_blocks_per_req=c["stride"])
+    shape = (2, len(lens), 8, c["stride"] * 16)
+    a = torch.full(shape, float("nan"), device=DEV)
+    b = torch.full(shape, float("nan"), device=DEV)
+    cache.global_redundancy(c["tables"], c["lengths"], a, gram=True)
+    cache.global_redundancy(c["tables"], c["lengths"], b)
+    assert cache.status() == zp.OK
+    worst = 0.0
+    for r, T in enumerate(lens):
+        x, y = a[:, r, :, :T].double(), b[:, r, :, :T].double()
+        scale = x.abs().mean(dim=-1, keepdim=True).clamp_min(1e-30)
+        worst = max(worst, ((x - y).abs() / torch.maximum(x.abs(), scale)).max().item())
+        assert torch.isnan(a[:, r, :, T:]).all(), "written past the length"
+    assert worst <= 2 * RTOL, worst
+    got = a.cpu().numpy()
+    picks = [(0, 0, 0), (1, 0, 7), (0, 1, 3)] + [
+        (int(rng.integers(2)), int(rng.integers(len(lens))), int(rng.integers(8)))
+        for _ in range(9)]
+    worst = 0.0
+    for l, r, h in picks:
+        T = lens[r]
+        K = gather(c["k_pools"][l], c["tables"][r], T, h)
+        want = orc.redundancy_global(K)
+        g = got[l, r, h, :T].astype(np.float64)
+        scale = max(float(np.mean(np.abs(want))), 1e-30)
+        worst = max(worst, float((np.abs(g - want) / np.maximum(np.abs(want), scale)).max()))
+    print(f"[parity] dense Gram, {len(lens) * 16} units ragged: max rel err {worst:.2e}")
+    assert worst <= RTOL
