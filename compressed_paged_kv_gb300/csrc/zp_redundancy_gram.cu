@@ -14,11 +14,12 @@
 //   sum_t = sum_k D[t][k] / |K_k|,   red_t = (sum_t / |K_t| - 1) / (T - 1)
 // (the k = t term is the 1 removed; columns past T are skipped).  Each B tile
 // feeds both halves: 256 rows of products per byte staged.  The kernel is
-// persistent: one CTA per SM takes items blockIdx.x, + gridDim.x, ... (the
-// row tiles of a unit are neighbouring items, run at the same time by
-// neighbouring CTAs, so the unit's keys are read from HBM about once), keeps
-// its tensor memory for the whole launch and runs the pipelines below
-// continuously from one item into the next.  Eighteen warps:
+// persistent: one CTA per SM takes a contiguous range of items, so a unit's
+// row tiles run back to back on one SM (its keys stay in L2 between them, and
+// the inverse norms of its keys, computed by its first item there, in shared
+// memory for the next ones); it keeps its tensor memory for the whole launch
+// and runs the pipelines below continuously from one item into the next.
+// Eighteen warps:
 //   warp 0     TMA producer: each item's A once it is free (its last products
 //              done and its row norms taken), B through four stages (the K
 //              pool maps, 128-byte swizzle, one 16-row box per cache block
@@ -28,9 +29,10 @@
 //              halves and commits to mbarriers;
 //   warps 2-17 two sets of 8 (one per accumulator buffer, so consecutive
 //              tiles are reduced at the same time): the inverse norms of the
-//              set's B stages (one key per thread) from shared memory, then
-//              tcgen05.ld of 32 lanes of one half and weighted row sums in
-//              registers, the two sets' sums added at the end of the item.
+//              set's B stages (one key per thread; for units of up to 4,096
+//              keys in a unit's first item only), then tcgen05.ld of 32 lanes
+//              of one half and weighted row sums in registers, the two sets'
+//              sums added at the end of the item.
 // The accumulators alternate between two buffers, so the products of one B
 // tile overlap the reduction of the previous one.
 // Every wait is bounded; after a timeout a warp records ZP_ERR_TIMEOUT and
@@ -50,6 +52,7 @@ constexpr int kGramNS = 4;                 // B stages
 constexpr int kGramEW = 16;                // reducing warps: 2 sets (one per buffer) of 8
 constexpr int kGramThreads = (2 + kGramEW) * 32;
 constexpr int kTmemCols = 4 * kGramN;      // [buffer][half] accumulators
+constexpr int kGramUMax = 4096;            // longest unit whose key norms stay in shared memory
 
 template <int D>
 struct GramSmem {
@@ -61,7 +64,8 @@ struct GramSmem {
     static constexpr int off_a = 0;                       // [half][panel]
     static constexpr int off_b = off_a + A_BYTES;         // kGramNS stages
     static constexpr int off_inv = off_b + kGramNS * B_STAGE;  // float [kGramNS][kGramN]
-    static constexpr int off_part = off_inv + kGramNS * kGramN * 4;  // float [2][2][kGramM]
+    static constexpr int off_invu = off_inv + kGramNS * kGramN * 4;  // float [kGramUMax]
+    static constexpr int off_part = off_invu + kGramUMax * 4;       // float [2][2][kGramM]
     static constexpr int off_bar = off_part + 4 * kGramM * 4;
     // fullA, fullB[NS], emptyB[NS], accFull[2], accEmpty[2], emptyA, done
     static constexpr int NBAR = 1 + 2 * kGramNS + 4 + 2;
@@ -193,6 +197,12 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
 
     const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
     const int n_items = a.units * a.row_tiles;
+    // a contiguous range of items per CTA: a unit's row tiles run back to back
+    // on one SM (its keys then stay in L2 between them, and their inverse
+    // norms in shared memory)
+    const int per = (n_items + gridDim.x - 1) / gridDim.x;
+    const int w_begin = min(n_items, static_cast<int>(blockIdx.x) * per);
+    const int w_end = min(n_items, w_begin + per);
 
     if (tid == 0) {
         mbar_init(fullA, 1);
@@ -265,7 +275,7 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
             return (blk * a.Hkv + it.h) * kBlk;
         };
         uint32_t ia = 0, gt = 0;  // items loaded, B tiles loaded (over all items)
-        for (int w = blockIdx.x; w < n_items && !bad; w += gridDim.x) {
+        for (int w = w_begin; w < w_end && !bad; ++w) {
             const Item it = decode(w);
             if (it.state != 0) {
                 if (it.state >= 2 && it.t0 == 0 && lane == 0)
@@ -325,7 +335,7 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
         // ------------------------------------------------------- products
         if (lane == 0) {
             uint32_t ia = 0, gt = 0, use[2] = {0u, 0u};
-            for (int w = blockIdx.x; w < n_items && !bad; w += gridDim.x) {
+            for (int w = w_begin; w < w_end && !bad; ++w) {
                 const Item it = decode(w);
                 if (it.state != 0)
                     continue;
@@ -382,12 +392,20 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
         const int g = (w2 & 7) >> 2;             // accumulator half (of the item's keys)
         const int tr = quarter * 32 + lane;      // this thread's key t0 + g*128 + tr
         float *sPart = reinterpret_cast<float *>(sm + S::off_part);
+        float *sInvU = reinterpret_cast<float *>(sm + S::off_invu);
         uint32_t ia = 0, gt = 0, use = 0, ic = 0;
-        for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+        int cur_u = -1;  // the unit whose key norms sInvU holds
+        for (int w = w_begin; w < w_end; ++w) {
             const Item it = decode(w);
             if (it.state != 0)
                 continue;
             const int T = it.T;
+            // a unit's first item here computes the inverse norms of all its
+            // keys (each set those of its tiles) into sInvU, the next ones
+            // read them; units too long for it take them per stage
+            const bool cached = T <= kGramUMax;
+            const bool fresh = !cached || it.u != cur_u;
+            cur_u = cached ? it.u : -1;
             float inv_t = 0.f;
             if (set == 0) {
                 // the norm of this thread's key t, before A is released (only
@@ -411,17 +429,27 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
                     continue;
                 const int s = gt % kGramNS, b = set;
                 const uint32_t j = use++;
-                if (!bad)
-                    bad = !mbar_wait(&fullB[s], (gt / kGramNS) & 1);
-                if (es < kGramN) {  // inverse norm of this stage's key es
-                    const int k = t * kGramN + es;
-                    const float sq =
-                        bad ? 0.f : row_sq<PANELS>(sB + s * S::B_STAGE, S::B_PANEL, es);
-                    sInv[s * kGramN + es] = (k < T && sq > 0.f) ? rsqrtf(sq) : 0.f;
-                }
-                named_sync_id(1 + set, NSET);
-                if (es == 0)
+                float *inv_row = cached ? sInvU + t * kGramN : sInv + s * kGramN;
+                if (fresh) {
+                    if (!bad)
+                        bad = !mbar_wait(&fullB[s], (gt / kGramNS) & 1);
+                    if (es < kGramN) {  // inverse norm of this stage's key es
+                        const int k = t * kGramN + es;
+                        const float sq =
+                            bad ? 0.f : row_sq<PANELS>(sB + s * S::B_STAGE, S::B_PANEL, es);
+                        inv_row[es] = (k < T && sq > 0.f) ? rsqrtf(sq) : 0.f;
+                    }
+                    named_sync_id(1 + set, NSET);
+                    if (es == 0)
+                        mbar_arrive(&emptyB[s]);
+                } else if (es == 0) {
+                    // nothing of the stage is read here: release it once it
+                    // holds this tile (an earlier arrival could close the
+                    // stage's previous phase)
+                    if (!bad)
+                        bad = !mbar_wait(&fullB[s], (gt / kGramNS) & 1);
                     mbar_arrive(&emptyB[s]);
+                }
                 if (!bad)
                     bad = !mbar_wait(&accFull[b], j & 1);
                 tmem_fence_after();
@@ -429,7 +457,7 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
                 if (!bad) {
                     const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                                            static_cast<uint32_t>((b * 2 + g) * kGramN);
-                    const float4 *inv = reinterpret_cast<const float4 *>(sInv + s * kGramN);
+                    const float4 *inv = reinterpret_cast<const float4 *>(inv_row);
                     const int lim = T - t * kGramN;  // columns at and past it are not keys
 #pragma unroll 1
                     for (int ch = 0; ch < kGramN / 32; ++ch) {
@@ -448,7 +476,7 @@ __global__ void __launch_bounds__(kGramThreads, 1) zp_gram_redundancy_kernel(con
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
                                 if (ch * 32 + i < lim)
-                                    sum = fmaf(v[i], sInv[s * kGramN + ch * 32 + i], sum);
+                                    sum = fmaf(v[i], inv_row[ch * 32 + i], sum);
                         }
                     }
                 }

@@ -26,7 +26,8 @@ def gather(pool, table_row, T, h):
 
 @pytest.mark.parametrize("gram", [False, True], ids=["sum_of_keys", "dense_gram"])
 @pytest.mark.parametrize("lens,d", [([2048, 1000, 17, 16, 1, 300], 128), ([700, 64, 5], 64),
-                                    ([4096, 257, 255, 129, 128], 128)])
+                                    ([4096, 257, 255, 129, 128], 128), ([4200, 130], 128),
+                                    ([4500, 4097, 200], 64)])
 def test_global_redundancy_matches_pairwise(orc, lens, d, gram):
     c = W.prefill_cache(500 + d, lens, 8, L=2, Hkv=2, Hq=4, d=d, w=4, device=DEV)
     # a few zero keys: cosine 0 with everything, redundancy 0
