@@ -22,12 +22,14 @@
 //       in shared memory) of the K_keep-th largest score; ties at the
 //       threshold go to the lower index; the kept positions in ascending
 //       order by block scans, then the window.
-//   zp_prefill_compact_kernel  one CTA per unit: destination rows in
-//       ascending chunks of 32; a chunk's source rows are read before any of
-//       its writes (one barrier), and every later chunk reads sources at or
-//       after its own first destination (kept[j] >= j), which no earlier
-//       chunk writes -- so compacting in place is safe, and the next chunk's
-//       rows can be loaded while this chunk's are stored.
+//   zp_prefill_compact_kernel  one CTA per unit: the source and destination
+//       pool rows of up to 2,048 destination rows resolved into shared memory
+//       first, then destination rows in ascending chunks of 32; a chunk's
+//       source rows are read before any of its writes (one barrier), and
+//       every later chunk reads sources at or after its own first destination
+//       (kept[j] >= j), which no earlier chunk writes -- so compacting in
+//       place is safe, and the next chunk's rows can be loaded while this
+//       chunk's are stored.
 #include "zp_internal.cuh"
 
 namespace zp {
@@ -40,6 +42,7 @@ constexpr int kPBlocks = kPChunk / kBlk;
 constexpr int kSelThreads = 1024;
 constexpr int kCmpThreads = 256;
 constexpr int kCmpRows = 32;                 // destination rows per compaction chunk
+constexpr int kCmpSeg = 2048;                // destination rows whose indices are staged at once
 
 template <int D, int MT>
 struct PrefillSmem {
@@ -461,6 +464,10 @@ __global__ void __launch_bounds__(kCmpThreads) zp_prefill_compact_kernel(const P
 {
     constexpr int VPR = D / 8;                                  // 16-byte vectors per row
     constexpr int ITEMS = kCmpRows * VPR * 2 / kCmpThreads;     // K and V
+    constexpr uint32_t kNone = 0xffffffffu;
+    // pool rows (block * Hkv + h) * b + slot of the source and the destination
+    // of each destination row of the segment, kNone: nothing to move
+    __shared__ uint32_t sSrc[kCmpSeg], sDst[kCmpSeg];
     if (*(volatile int32_t *)a.call != 0)
         return;
     const int u = blockIdx.x;
@@ -471,55 +478,67 @@ __global__ void __launch_bounds__(kCmpThreads) zp_prefill_compact_kernel(const P
     const int32_t *kept = a.kept + (size_t)u * KT;
     const int32_t *trow = a.tables + (size_t)row * a.stride;
     const int32_t *drow = a.dst_table + (size_t)r * a.stride;
-    uint4 *pools[2] = {static_cast<uint4 *>(a.kpools[l]), static_cast<uint4 *>(a.vpools[l])};
+    uint4 *const kpool = static_cast<uint4 *>(a.kpools[l]);
+    uint4 *const vpool = static_cast<uint4 *>(a.vpools[l]);
 
     // item `it` of a chunk: vector ch of row c0 + jj of K (kv 0) or V (kv 1)
     struct Chunk {
         uint4 v[ITEMS];
-        uint32_t dst[ITEMS];  // vector index into the pool, or ~0u: nothing to move
+        uint32_t dst[ITEMS];  // destination pool row, or kNone: nothing to move
     };
-    auto load = [&](int c0, Chunk &ck) {
-        const int n = min(kCmpRows, KT - c0);
+    auto load = [&](int n, int c0, Chunk &ck) {
 #pragma unroll
         for (int it = 0; it < ITEMS; ++it) {
             const int v = threadIdx.x + it * kCmpThreads;
             const int kv = v / (kCmpRows * VPR);
             const int rem = v - kv * kCmpRows * VPR;
-            const int jj = rem / VPR, ch = rem - jj * VPR;
-            ck.dst[it] = ~0u;
-            if (jj >= n)
+            const int jj = c0 + rem / VPR, ch = rem % VPR;
+            ck.dst[it] = kNone;
+            if (jj >= n || sSrc[jj] == kNone)
                 continue;
-            const int j = c0 + jj, src = kept[j];
-            if (src < j || src >= T) {  // kept[j] >= j holds for any valid selection
-                if (ch == 0 && kv == 0)
-                    set_error(a.sticky, ZP_ERR_DEVICE_CHECK);
-                continue;
-            }
-            const int sblk = trow[src / kBlk], dblk = drow[j / kBlk];
-            if (sblk == dblk && src % kBlk == j % kBlk)
-                continue;  // already in place
-            ck.v[it] = ld_global_nc_v4(pools[kv] +
-                                       (((size_t)sblk * a.Hkv + h) * kBlk + src % kBlk) * VPR + ch);
-            ck.dst[it] = static_cast<uint32_t>((((size_t)dblk * a.Hkv + h) * kBlk + j % kBlk) * VPR +
-                                               ch);
+            ck.v[it] = ld_global_nc_v4((kv ? vpool : kpool) + (size_t)sSrc[jj] * VPR + ch);
+            ck.dst[it] = sDst[jj];
         }
     };
     auto store = [&](const Chunk &ck) {
 #pragma unroll
         for (int it = 0; it < ITEMS; ++it) {
-            const int kv = (threadIdx.x + it * kCmpThreads) / (kCmpRows * VPR);
-            if (ck.dst[it] != ~0u)
-                pools[kv][ck.dst[it]] = ck.v[it];
+            const int v = threadIdx.x + it * kCmpThreads;
+            const int kv = v / (kCmpRows * VPR), ch = v % VPR;
+            if (ck.dst[it] != kNone)
+                (kv ? vpool : kpool)[(size_t)ck.dst[it] * VPR + ch] = ck.v[it];
         }
     };
-    Chunk cur, nxt;
-    load(0, cur);
-    for (int c0 = 0; c0 < KT; c0 += kCmpRows) {
-        __syncthreads();  // every source row of this chunk read before any of its writes
-        if (c0 + kCmpRows < KT)
-            load(c0 + kCmpRows, nxt);  // sources past this chunk: none written by it
-        store(cur);
-        cur = nxt;
+    for (int s0 = 0; s0 < KT; s0 += kCmpSeg) {
+        const int n = min(kCmpSeg, KT - s0);
+        __syncthreads();  // the previous segment's rows are stored
+        // every row's source and destination first, all rows in parallel (the
+        // copies below then wait on one load each, not on three in a row)
+        for (int jj = threadIdx.x; jj < n; jj += kCmpThreads) {
+            const int j = s0 + jj, src = kept[j];
+            uint32_t sr = kNone, dr = kNone;
+            if (src < j || src >= T) {  // kept[j] >= j holds for any valid selection
+                set_error(a.sticky, ZP_ERR_DEVICE_CHECK);
+            } else {
+                const int sblk = trow[src / kBlk], dblk = drow[j / kBlk];
+                if (!(sblk == dblk && src % kBlk == j % kBlk)) {  // else already in place
+                    sr = (static_cast<uint32_t>(sblk) * a.Hkv + h) * kBlk + src % kBlk;
+                    dr = (static_cast<uint32_t>(dblk) * a.Hkv + h) * kBlk + j % kBlk;
+                }
+            }
+            sSrc[jj] = sr;
+            sDst[jj] = dr;
+        }
+        __syncthreads();
+        Chunk cur, nxt;
+        load(n, 0, cur);
+        for (int c0 = 0; c0 < n; c0 += kCmpRows) {
+            __syncthreads();  // every source row of this chunk read before any of its writes
+            if (c0 + kCmpRows < n)
+                load(n, c0 + kCmpRows, nxt);  // sources past this chunk: none written by it
+            store(cur);
+            cur = nxt;
+        }
     }
 }
 
