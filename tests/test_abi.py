@@ -78,6 +78,68 @@ def test_descriptor_checks_need_no_gpu(lib):
     lib.zp_cache_destroy(None)
 
 
+def test_every_handle_entry_refuses_a_null_cache(lib):
+    """Each entry point that takes a cache handle returns ZP_ERR_INVALID_ARG
+    for a null one (and null arrays), before any CUDA call."""
+    from compressed_paged_kv_gb300 import zp
+    skip = {"zp_cache_create", "zp_cache_destroy", "zp_status_string",
+            "zp_paged_decode_attn_noalloc"}
+    checked = 0
+    for name in declared_functions():
+        if name in skip:
+            continue
+        fn = getattr(lib, name)
+        def zero(t):  # 0 for an integer, 0.0 for a float, NULL for a pointer
+            code = getattr(t, "_type_", None)
+            if code in ("f", "d"):
+                return 0.0
+            if isinstance(code, str) and code in "bBhHiIlLqQ?":
+                return 0
+            return None
+        args = [zero(t) for t in fn.argtypes]
+        assert fn(*args) == zp.ERR_INVALID_ARG, name
+        checked += 1
+    assert checked >= 12
+
+
+def test_descriptor_and_size_limits_need_no_gpu(lib):
+    """Pool alignment and the 2^31-row limit of cache creation, and the checks
+    of the handle-free decode entry point, all answered on the host."""
+    from compressed_paged_kv_gb300 import zp
+    P = ctypes.c_void_p
+
+    def create(ptr=256, **kw):
+        base = dict(num_layers=1, num_kv_heads=2, num_q_heads=4, head_dim=64, block_size=16,
+                    num_blocks=8, max_requests=2, max_blocks_per_req=8)
+        base.update(kw)
+        pools = (P * 1)(P(ptr))
+        d = zp.zp_cache_desc(base["num_layers"], base["num_kv_heads"], base["num_q_heads"],
+                             base["head_dim"], base["block_size"], base["num_blocks"],
+                             base["max_requests"], base["max_blocks_per_req"], pools, pools)
+        return lib.zp_cache_create(ctypes.byref(d), ctypes.byref(P()))
+
+    assert create(ptr=264) == zp.ERR_INVALID_ARG          # pool not 16-byte aligned
+    assert create(num_blocks=1 << 26) == zp.ERR_UNSUPPORTED  # 2^31 pool rows per layer
+
+    buf = P(4096)
+
+    def noalloc(R=1, Hkv=2, Hq=4, d=64, stride=8, scale=0.125, num_blocks=8):
+        return lib.zp_paged_decode_attn_noalloc(buf, buf, num_blocks, Hkv, Hq, d, buf, buf,
+                                                stride, 4, buf, None, R, scale, buf, None, None)
+
+    assert noalloc(d=96) == zp.ERR_UNSUPPORTED
+    assert noalloc(Hq=5) == zp.ERR_INVALID_ARG
+    assert noalloc(scale=float("nan")) == zp.ERR_INVALID_ARG
+    assert noalloc(num_blocks=0) == zp.ERR_INVALID_ARG
+    assert noalloc(R=-1) == zp.ERR_INVALID_ARG
+    assert noalloc(R=1 << 14, Hq=4) == zp.ERR_UNSUPPORTED  # more (request, head) pairs than slots
+    assert noalloc(stride=1 << 27) == zp.ERR_UNSUPPORTED
+    assert noalloc(R=0) == zp.OK                           # nothing to do, nothing launched
+    assert lib.zp_paged_decode_attn_noalloc(None, buf, 8, 2, 4, 64, buf, buf, 8, 4, buf, None, 1,
+                                            0.125, buf, None, None) == zp.ERR_INVALID_ARG
+    assert zp.status_string(12345) == "unknown status"
+
+
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     from compressed_paged_kv_gb300 import zp
     monkeypatch.setattr(zp, "_lib", None)
