@@ -742,7 +742,7 @@ zp_status zp_global_redundancy_gram(zp_cache *c, const int32_t *block_tables,
     a.row_tiles = row_tiles;
     a.red_out = red_out;
     a.sticky = c->ws.sticky;
-    return zp::launch_gram_redundancy(a, c->d, static_cast<int>(units),
+    return zp::launch_gram_redundancy(a, c->d, static_cast<int>(units), c->num_sms,
                                       static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? ZP_OK
                : ZP_ERR_CUDA;

@@ -37,7 +37,8 @@ struct GramRedArgs {
 };
 
 int gram_row_tiles(int T_cap);
-cudaError_t launch_gram_redundancy(const GramRedArgs &a, int d, int units, cudaStream_t s);
+cudaError_t launch_gram_redundancy(const GramRedArgs &a, int d, int units, int sms,
+                                   cudaStream_t s);  // one CTA per SM (sms of them at most)
 
 cudaError_t launch_alloc_rows(const Workspace &ws, int32_t *block_tables, int32_t bt_stride,
                               int32_t num_rows, int32_t *lengths, const int32_t *req_idx,

@@ -527,17 +527,12 @@ static cudaError_t launch_gram_t(const GramRedArgs &a, int ctas, cudaStream_t s)
 
 int gram_row_tiles(int T_cap) { return (T_cap + kGramM - 1) / kGramM; }
 
-cudaError_t launch_gram_redundancy(const GramRedArgs &a, int d, int units, cudaStream_t s)
+cudaError_t launch_gram_redundancy(const GramRedArgs &a, int d, int units, int sms,
+                                   cudaStream_t s)
 {
     const long long items = static_cast<long long>(units) * a.row_tiles;
-    if (items >= (1ll << 31))
+    if (items >= (1ll << 31) || sms < 1)
         return cudaErrorInvalidValue;
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess)
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess)
-        return e;
     GramRedArgs b = a;
     b.units = units;
     const int ctas = static_cast<int>(items < sms ? items : sms);  // one CTA per SM
