@@ -746,7 +746,7 @@ def run_gpu(args, world, rank, local):
         "decode_frac_of_measured": dec_gbs / peak,
         "compress_frac_of_8tbs": comp_gbs / NOMINAL_HBM_GBS,
         "roofline": {
-            "kernel": "zp_compress_kernel (timed over its zp_compress call: plan + fused + "
+            "kernel": "zp_compress_stream_kernel (timed over its zp_compress call: plan + fused + "
                       "finalize launches)",
             "bound": "hbm",
             "achieved": comp_gbs,
