@@ -1,12 +1,13 @@
 // zp_noalloc.cu -- paged decode attention for callers that cannot allocate.
 //
-// Some callers cannot call cudaMalloc at all: code running inside a CUDA
-// graph being captured, an allocator or memory-pool callback, a plug-in
-// loaded into a host process that owns all device memory, or a real-time
-// path that must not block on the driver's allocator.  This entry point
-// needs no zp_cache handle (whose creation allocates) and allocates nothing:
-// its split-K partial results live in a fixed file-scope device array that
-// every GPU loading the library holds until the process exits.
+// Some callers cannot call cudaMalloc at all: an allocator or memory-pool
+// callback (allocating there would re-enter the allocator), a plug-in loaded
+// into a host process that owns all device memory, or a real-time path that
+// must not block on the driver's allocator.  This entry point needs no
+// zp_cache handle (whose creation allocates) and allocates nothing: its
+// split-K partial results live in a fixed file-scope device array, created
+// when the library's device code is loaded into a context (usually at the
+// first call there) and held until the process exits.
 //
 // The kernels here are a plain CUDA-core variant of the split-K decode
 // attention in zp_decode.cu: one CTA per (request, query head, split), a
@@ -136,27 +137,73 @@ __global__ void __launch_bounds__(D) na_decode_combine(const NaArgs a)
     a.out[(size_t)rh * D + c] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
 }
 
-// Device address of g_na_part, looked up once per device (with that device
-// current) and cached.
-std::mutex g_na_mu;
-float *g_na_addr[256];
-bool g_na_ready[256];
+// The device address of g_na_part belongs to a CUDA context: the module (and
+// with it the array) is loaded once per context, so another context on the
+// same device, or the new primary context after cudaDeviceReset, has its own
+// copy at its own address.  Outside a stream capture every call asks the
+// runtime for the current context's address (a host-side lookup) and records
+// it against the context; inside a capture, where the lookup could load the
+// module, only a recorded address is used.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
 
-cudaError_t na_scratch(int device, float **out)
+CtxGetCurrentFn ctx_get_current()
 {
-    if (device < 0 || device >= 256)
-        return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_na_mu);
-    if (!g_na_ready[device]) {
+    static CtxGetCurrentFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<CtxGetCurrentFn>(p);
+        return static_cast<CtxGetCurrentFn>(nullptr);
+    }();
+    return fn;
+}
+
+constexpr int kNaCtxSlots = 64;
+std::mutex g_na_mu;
+CUcontext g_na_ctx[kNaCtxSlots];
+float *g_na_addr[kNaCtxSlots];
+int g_na_used = 0;
+
+// ZP_OK with *out set, ZP_ERR_UNSUPPORTED when `stream` is being captured and
+// this context has no recorded address yet, ZP_ERR_CUDA on a runtime error.
+zp_status na_scratch(cudaStream_t stream, float **out)
+{
+    CtxGetCurrentFn get = ctx_get_current();
+    if (!get)
+        return ZP_ERR_CUDA;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess)
+        return ZP_ERR_CUDA;
+    if (cap == cudaStreamCaptureStatusNone) {
         void *ptr = nullptr;
-        const cudaError_t err = cudaGetSymbolAddress(&ptr, g_na_part);
-        if (err != cudaSuccess)
-            return err;
-        g_na_addr[device] = static_cast<float *>(ptr);
-        g_na_ready[device] = true;
+        if (cudaGetSymbolAddress(&ptr, g_na_part) != cudaSuccess)
+            return ZP_ERR_CUDA;
+        CUcontext ctx = nullptr;
+        if (get(&ctx) != CUDA_SUCCESS || !ctx)
+            return ZP_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(g_na_mu);
+        int i = 0;
+        while (i < g_na_used && g_na_ctx[i] != ctx)
+            ++i;
+        if (i == g_na_used && g_na_used < kNaCtxSlots)
+            g_na_ctx[g_na_used++] = ctx;
+        if (i < g_na_used)
+            g_na_addr[i] = static_cast<float *>(ptr);
+        *out = static_cast<float *>(ptr);
+        return ZP_OK;
     }
-    *out = g_na_addr[device];
-    return cudaSuccess;
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS || !ctx)
+        return ZP_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_na_mu);
+    for (int i = 0; i < g_na_used; ++i)
+        if (g_na_ctx[i] == ctx) {
+            *out = g_na_addr[i];
+            return ZP_OK;
+        }
+    return ZP_ERR_UNSUPPORTED;
 }
 
 }  // namespace
@@ -180,12 +227,14 @@ extern "C" zp_status zp_paged_decode_attn_noalloc(
         return ZP_ERR_UNSUPPORTED;
     if (R == 0)
         return ZP_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float *part = nullptr;
+    const zp_status scratch = na_scratch(s, &part);
+    if (scratch != ZP_OK)
+        return scratch;
     int device = 0, sms = 0;
     if (cudaGetDevice(&device) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
-        return ZP_ERR_CUDA;
-    float *part = nullptr;
-    if (na_scratch(device, &part) != cudaSuccess)
         return ZP_ERR_CUDA;
 
     // splits: about four CTAs per SM, bounded by the array and by 16
@@ -214,7 +263,6 @@ extern "C" zp_status zp_paged_decode_attn_noalloc(
     a.part = part;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.status = status;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid(static_cast<unsigned>(splits), static_cast<unsigned>(num_q_heads),
                     static_cast<unsigned>(R));
     if (head_dim == 64) {

@@ -187,12 +187,23 @@ class CacheState:
         return self.refcount.shape[0]
 
 
-def build_cache(wl: Workload, device="cpu", seed=None, with_decode_q=True) -> CacheState:
-    """Builds the cache of a workload: every request's K/V rows written through
-    its block table into per-layer pools, plus the queries of one step."""
-    master = wl.seed if seed is None else seed
-    b, N, d, Hkv, L = wl.b, wl.N, wl.d, wl.Hkv, wl.L
-    R = wl.R
+@dataclasses.dataclass
+class Layout:
+    """Lengths, block tables and block accounting of a workload (host)."""
+    lengths: torch.Tensor        # [R] int64
+    compress_rows: torch.Tensor  # [Rc] int64
+    decode_rows: torch.Tensor    # [Rd] int64
+    nblk: torch.Tensor           # [R] blocks held
+    tables: torch.Tensor         # [R][N] int32, -1 past a row's blocks
+    refcount: torch.Tensor       # [num_blocks] int32
+    free_list: torch.Tensor      # spare block ids, bottom of the stack first
+    num_blocks: int
+    pb: int                      # shared prefix blocks per group (0: none)
+    group: int
+
+
+def layout(wl: Workload, master: int) -> Layout:
+    b, N, R = wl.b, wl.N, wl.R
     gcpu = _gen("cpu", derive_seed(master, TENSOR_LEN))
     if wl.mixed:
         # decoding requests are never full (a full request is due for
@@ -237,65 +248,155 @@ def build_cache(wl: Workload, device="cpu", seed=None, with_decode_q=True) -> Ca
     for r in range(R):
         own = tables[r, pb:int(nblk[r].item())]
         refcount[own.long()] += 1
-    free_list = phys[used:].clone()
-    free_ids = torch.full((num_blocks,), -1, dtype=torch.int32)
-    free_ids[:free_list.numel()] = free_list
-    free_count = torch.tensor([free_list.numel()], dtype=torch.int32)
+    return Layout(lengths, compress_rows, decode_rows, nblk, tables, refcount,
+                  phys[used:].clone(), num_blocks, pb, group)
 
-    T = N * b
+
+def layer_kv(wl: Workload, master: int, l: int, pb: int, group: int, device, rows=None):
+    """K and V of layer l for every request (or the requests `rows`), token
+    order: two bf16 tensors [R'][Hkv][T][d].  The draws are always made for
+    all R requests (one generator per tensor and layer), so a subset holds
+    exactly the values of the full build."""
+    R, Hkv, T, d, b = wl.R, wl.Hkv, wl.T, wl.d, wl.b
+    eps = _normal((R, Hkv, T, d), device, derive_seed(master, TENSOR_K, l))
+    veps = _normal((R, Hkv, T, d), device, derive_seed(master, TENSOR_V, l))
+    u = None
+    if wl.hh_prob > 0:
+        u = torch.rand((R, Hkv, T), generator=_gen(device, derive_seed(master, TENSOR_HH, l)),
+                       device=device)
+    if pb:
+        # prefix tokens are generated once per group (from its first member)
+        P = pb * b
+        lead = (torch.arange(R, device=device) // group) * group
+        eps[:, :, :P] = eps[lead][:, :, :P]
+        veps[:, :, :P] = veps[lead][:, :, :P]
+        if u is not None:
+            u[:, :, :P] = u[lead][:, :, :P]
+    # the recursion runs over all requests even for a subset: its batched
+    # products could round differently for another batch size
+    K = _ar1(eps, wl.rho)
+    del eps
+    if rows is not None:
+        sel = torch.as_tensor(rows, device=device).long()
+        K, veps = K[sel], veps[sel]
+        u = u[sel] if u is not None else None
+    if u is not None:
+        K = torch.where((u < wl.hh_prob)[..., None], K * wl.hh_scale, K)
+    return K.to(torch.bfloat16), veps.to(torch.bfloat16)
+
+
+def layer_window_q(wl: Workload, master: int, l: int, Rc: int, device):
+    return _normal((Rc, wl.Hq, wl.w, wl.d), device,
+                   derive_seed(master, TENSOR_Q, l)).to(torch.bfloat16)
+
+
+def layer_decode_q(wl: Workload, master: int, l: int, device):
+    return _normal((wl.R, wl.Hq, wl.d), device,
+                   derive_seed(master, TENSOR_DQ, l)).to(torch.bfloat16)
+
+
+def build_cache(wl: Workload, device="cpu", seed=None, with_decode_q=True) -> CacheState:
+    """Builds the cache of a workload: every request's K/V rows written through
+    its block table into per-layer pools, plus the queries of one step."""
+    master = wl.seed if seed is None else seed
+    b, N, d, Hkv, L = wl.b, wl.N, wl.d, wl.Hkv, wl.L
+    R = wl.R
+    lay = layout(wl, master)
+    num_blocks, nblk, tables = lay.num_blocks, lay.nblk, lay.tables
+    free_ids = torch.full((num_blocks,), -1, dtype=torch.int32)
+    free_ids[:lay.free_list.numel()] = lay.free_list
+    free_count = torch.tensor([lay.free_list.numel()], dtype=torch.int32)
+
     k_pools, v_pools = [], []
     flat_tables = tables.to(device).long()
+    live = torch.arange(N, device=device)[None, :] < nblk.to(device)[:, None]
     for l in range(L):
-        eps = _normal((R, Hkv, T, d), device, derive_seed(master, TENSOR_K, l))
-        veps = _normal((R, Hkv, T, d), device, derive_seed(master, TENSOR_V, l))
-        if pb:
-            # prefix tokens are generated once per group (from its first member)
-            P = pb * b
-            lead = (torch.arange(R, device=device) // group) * group
-            eps[:, :, :P] = eps[lead][:, :, :P]
-            veps[:, :, :P] = veps[lead][:, :, :P]
-        K = _ar1(eps, wl.rho)
-        if wl.hh_prob > 0:
-            u = torch.rand((R, Hkv, T), generator=_gen(device, derive_seed(master, TENSOR_HH, l)),
-                           device=device)
-            if pb:
-                P = pb * b
-                lead = (torch.arange(R, device=device) // group) * group
-                u[:, :, :P] = u[lead][:, :, :P]
-            K = torch.where((u < wl.hh_prob)[..., None], K * wl.hh_scale, K)
-        kb = K.to(torch.bfloat16)
-        vb = veps.to(torch.bfloat16)
-        del K, eps, veps
+        kb, vb = layer_kv(wl, master, l, lay.pb, lay.group, device)
         kpool = torch.zeros((num_blocks, Hkv, b, d), dtype=torch.bfloat16, device=device)
         vpool = torch.zeros((num_blocks, Hkv, b, d), dtype=torch.bfloat16, device=device)
         # [R][Hkv][N][b][d] -> rows of blocks; only the live blocks are written
         kb = kb.view(R, Hkv, N, b, d).permute(0, 2, 1, 3, 4)
         vb = vb.view(R, Hkv, N, b, d).permute(0, 2, 1, 3, 4)
-        live = torch.arange(N, device=device)[None, :] < nblk.to(device)[:, None]
         kpool[flat_tables[live]] = kb[live]
         vpool[flat_tables[live]] = vb[live]
         del kb, vb
         k_pools.append(kpool)
         v_pools.append(vpool)
 
-    Rc = compress_rows.numel()
+    Rc = lay.compress_rows.numel()
     window_q = torch.empty((L, Rc, wl.Hq, wl.w, d), dtype=torch.bfloat16, device=device)
     for l in range(L):
-        window_q[l] = _normal((Rc, wl.Hq, wl.w, d), device,
-                              derive_seed(master, TENSOR_Q, l)).to(torch.bfloat16)
+        window_q[l] = layer_window_q(wl, master, l, Rc, device)
     if with_decode_q:
         decode_q = torch.empty((L, R, wl.Hq, d), dtype=torch.bfloat16, device=device)
         for l in range(L):
-            decode_q[l] = _normal((R, wl.Hq, d), device,
-                                  derive_seed(master, TENSOR_DQ, l)).to(torch.bfloat16)
+            decode_q[l] = layer_decode_q(wl, master, l, device)
     else:
         decode_q = torch.empty(0, dtype=torch.bfloat16, device=device)
     i32 = dict(dtype=torch.int32, device=device)
     return CacheState(
         wl=wl, k_pools=k_pools, v_pools=v_pools, block_tables=tables.to(**i32),
-        lengths=lengths.to(**i32), refcount=refcount.to(**i32), free_ids=free_ids.to(**i32),
-        free_count=free_count.to(**i32), window_q=window_q, decode_q=decode_q,
-        compress_rows=compress_rows.to(**i32), decode_rows=decode_rows.to(**i32))
+        lengths=lay.lengths.to(**i32), refcount=lay.refcount.to(**i32),
+        free_ids=free_ids.to(**i32), free_count=free_count.to(**i32), window_q=window_q,
+        decode_q=decode_q, compress_rows=lay.compress_rows.to(**i32),
+        decode_rows=lay.decode_rows.to(**i32))
+
+
+def sample_snapshot(wl: Workload, rows, layers, device="cpu", seed=None, spare=None) -> dict:
+    """Host snapshot (the format of `snapshot`) of a sample of a workload: the
+    requests `rows` (table rows) on the layers `layers`, with exactly the
+    values the full build gives them, without building the full pools.  The
+    sampled rows' blocks are renumbered 0..n-1 in ascending order of their
+    ids in the full build; their refcounts count the sampled rows only (equal
+    to the full ones when whole sharing groups are sampled); `spare` fresh
+    blocks (default: a full request's worth per sampled row) form the free
+    stack.  window_q / decode_q hold the sampled compressing rows' and all
+    sampled rows' queries; compress_rows / decode_rows index the sample."""
+    import numpy as np
+    master = wl.seed if seed is None else seed
+    rows = sorted(int(r) for r in rows)
+    lay = layout(wl, master)
+    tab = lay.tables[rows]
+    used = torch.unique(tab[tab >= 0])
+    remap = torch.full((lay.num_blocks,), -1, dtype=torch.int32)
+    remap[used.long()] = torch.arange(used.numel(), dtype=torch.int32)
+    spare = len(rows) * wl.N if spare is None else spare
+    nb = used.numel() + spare
+    new_tab = torch.where(tab >= 0, remap[tab.clamp(min=0).long()], tab)
+    refcount = torch.zeros(nb, dtype=torch.int32)
+    for r in range(len(rows)):
+        held = new_tab[r][new_tab[r] >= 0].long()
+        refcount[held] += 1
+    free_ids = torch.full((nb,), -1, dtype=torch.int32)
+    free_ids[:spare] = torch.arange(used.numel(), nb, dtype=torch.int32)
+    comp_full = lay.compress_rows.tolist()
+    pos_c = {r: i for i, r in enumerate(comp_full)}
+    crow = [i for i, r in enumerate(rows) if r in pos_c]
+    drow = [i for i, r in enumerate(rows) if r not in pos_c]
+    b, N, Hkv, d = wl.b, wl.N, wl.Hkv, wl.d
+    nblk = lay.nblk[rows]
+    kp, vp, wq, dq = [], [], [], []
+    live = torch.arange(N)[None, :] < nblk[:, None]
+    for l in layers:
+        kb, vb = layer_kv(wl, master, l, lay.pb, lay.group, device, rows=rows)
+        kb = kb.view(len(rows), Hkv, N, b, d).permute(0, 2, 1, 3, 4).cpu()
+        vb = vb.view(len(rows), Hkv, N, b, d).permute(0, 2, 1, 3, 4).cpu()
+        kpool = torch.zeros((nb, Hkv, b, d), dtype=torch.bfloat16)
+        vpool = torch.zeros((nb, Hkv, b, d), dtype=torch.bfloat16)
+        kpool[new_tab.long()[live]] = kb[live]
+        vpool[new_tab.long()[live]] = vb[live]
+        kp.append(bf16_bits(kpool))
+        vp.append(bf16_bits(vpool))
+        q = layer_window_q(wl, master, l, len(comp_full), device)
+        wq.append(bf16_bits(q[[pos_c[rows[i]] for i in crow]]))
+        dq.append(bf16_bits(layer_decode_q(wl, master, l, device)[rows]))
+    return dict(
+        k_pools=kp, v_pools=vp, block_tables=new_tab.numpy().copy(),
+        lengths=lay.lengths[rows].to(torch.int32).numpy().copy(),
+        refcount=refcount.numpy().copy(), free_ids=free_ids.numpy().copy(), free_count=spare,
+        window_q=np.stack(wq), decode_q=np.stack(dq),
+        compress_rows=np.asarray(crow, dtype=np.int32),
+        decode_rows=np.asarray(drow, dtype=np.int32), layers=list(layers), rows=rows)
 
 
 def fork_cache(seed: int, R: int, n_max: int, L: int = 2, Hkv: int = 2, d: int = 128,

@@ -17,8 +17,8 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Every call only enqueues work on `stream`: nothing
  *    synchronises except zp_cache_status, and nothing allocates after
- *    zp_cache_create, so every call but zp_cache_status can be captured into
- *    a CUDA graph and replayed.
+ *    zp_cache_create, so every call that takes a zp_cache handle, except
+ *    zp_cache_status, can be captured into a CUDA graph and replayed.
  *  - Argument errors that the host can see are returned synchronously,
  *    before anything is enqueued.  Errors that only the device can see (a
  *    length or block id read from device memory, an empty free stack) are
@@ -223,13 +223,15 @@ zp_status zp_paged_decode_attn(zp_cache *cache, int32_t layer, const void *q,
 
 /* Paged decode attention for callers that cannot allocate device memory.
  * The paper has no counterpart: this is a deployment variant of
- * zp_paged_decode_attn.  Callers that cannot call cudaMalloc (code inside a
- * CUDA graph being captured, an allocator or memory-pool callback, a plug-in
- * in a process that owns all device memory, a real-time path that must not
- * wait on the allocator) can still run decode attention: this call needs no
- * zp_cache handle and allocates nothing.  Its split-K partial results live in
- * one fixed device array compiled into the library (about 16.3 MiB, held on
- * every GPU that loads the library until the process exits).
+ * zp_paged_decode_attn.  Some callers cannot call cudaMalloc where they run
+ * decode attention: an allocator or memory-pool callback (allocating there
+ * would re-enter the allocator), a plug-in in a process whose host owns all
+ * device memory, a real-time path that must not wait on the allocator.  This
+ * call needs no zp_cache handle and allocates nothing.  Its split-K partial
+ * results live in one fixed device array compiled into the library (about
+ * 16.3 MiB), created when the library's device code is loaded into a CUDA
+ * context -- usually at the first call in that context -- and held until the
+ * process exits.
  *
  *  k_pool, v_pool  device bf16 pools of one layer, [num_blocks][num_kv_heads][16][head_dim]
  *  q, out          device bf16 [R][num_q_heads][head_dim]; other arguments as in
@@ -237,12 +239,19 @@ zp_status zp_paged_decode_attn(zp_cache *cache, int32_t layer, const void *q,
  *  status          nullable device int32: device-detected errors (a length or
  *                  block id out of range) are recorded there with atomicCAS from 0
  * Limits: head_dim 64 or 128, block size 16, R * num_q_heads <= 32768
- * (ZP_ERR_UNSUPPORTED beyond).  The first call on a device looks up the
- * array's device address (once per device, with that device current): make
- * that first call before any stream capture.  Every call shares the array and
- * each call overwrites the slots it reads, so nothing needs clearing between
- * calls; calls that overlap on the GPU (two streams, or two threads) race on
- * it and must be serialised by the caller. */
+ * (ZP_ERR_UNSUPPORTED beyond).
+ * The array's device address belongs to the current CUDA context (another
+ * context on the same device, or the primary context re-created after
+ * cudaDeviceReset, has its own copy).  A call made while `stream` is not
+ * being captured looks the address up in the current context (a host-side
+ * lookup) and records it; a call made while `stream` is being captured uses
+ * only an address recorded earlier in the same context and returns
+ * ZP_ERR_UNSUPPORTED, before any other CUDA call, when there is none.  So in
+ * each context make the first call before any stream capture (and again
+ * after cudaDeviceReset).
+ * Every call shares the array and each call overwrites the slots it reads,
+ * so nothing needs clearing between calls; calls that overlap on the GPU (two
+ * streams, or two threads) race on it and must be serialised by the caller. */
 zp_status zp_paged_decode_attn_noalloc(const void *k_pool, const void *v_pool, int32_t num_blocks,
                                        int32_t num_kv_heads, int32_t num_q_heads,
                                        int32_t head_dim, const void *q,

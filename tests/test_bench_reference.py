@@ -33,7 +33,9 @@ def test_reference_line_keeps_the_contract():
     assert d["higher_is_better"] is True
     assert d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 1
     assert d["value"] > 0 and d["ms_per_step"] > 0
-    assert d["config"]["workload"] == "tiny"
+    from compressed_paged_kv_gb300 import workloads as W
+    wl = W.WORKLOADS["tiny"]
+    assert d["config"] == bench.bench_config(wl, wl.R, 1)  # the GPU arm's config, key by key
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert cb["unit"] == d["unit"] and cb["sample"]
@@ -46,3 +48,30 @@ def test_reference_other_ranks_print_nothing():
     assert run_bench(rank=1, world=2) == []
     lines = run_bench(rank=0, world=2)
     assert len(lines) == 1 and json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_samples_of_the_oracle_legs():
+    """The CPU baseline of the shared-prefix workload times two whole sharing
+    groups on every layer (>= 1,024 units); a reference step is a bounded
+    slice (whole requests of one group, a subset of layers) that rotates."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from compressed_paged_kv_gb300 import workloads as W
+    wl = W.WORKLOADS["qwen3_36l"]
+    rows, layers = bench.baseline_sample(wl)
+    assert len(rows) == 2 * wl.group and layers == list(range(wl.L))
+    assert {r // wl.group for r in rows} == {0, wl.R // wl.group - 1}
+    assert len(rows) * len(layers) * wl.Hkv >= 1024
+    seen = set()
+    for i in range(8):
+        rows, layers = bench.reference_step_sample(wl, i)
+        assert len({r // wl.group for r in rows}) == 1 and len(rows) == wl.group
+        assert 0 < len(rows) * len(layers) * wl.Hkv <= 1024
+        seen.add((rows[0], tuple(layers)))
+    assert len(seen) == 8
+    for name in ("qwen3_1l", "long4k"):
+        wl = W.WORKLOADS[name]
+        rows, layers = bench.baseline_sample(wl)
+        assert len(rows) * len(layers) * wl.Hkv >= min(1024, wl.units())
+        rows, layers = bench.reference_step_sample(wl, 3)
+        assert len(rows) * len(layers) * wl.Hkv <= 1024

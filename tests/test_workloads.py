@@ -120,3 +120,31 @@ def test_inputs_are_determined_by_the_seed(seed_same):
     same = all(torch.equal(x, y) for x, y in zip(a.k_pools + a.v_pools + [a.window_q, a.decode_q],
                                                  b.k_pools + b.v_pools + [b.window_q, b.decode_q]))
     assert same == seed_same
+
+
+def test_sample_snapshot_equals_the_full_build():
+    """A sampled snapshot holds exactly the full build's rows, queries and
+    per-request block structure (shared prefixes included), renumbered."""
+    import numpy as np
+    wl = W.scaled(W.WORKLOADS["qwen3_36l"], name="sample", L=3, R=12, group=4, prefix_blocks=2,
+                  N=8, spare_blocks=10)
+    st = W.build_cache(wl, "cpu")
+    rows = [4, 5, 6, 7, 10]
+    snap = W.sample_snapshot(wl, rows, [0, 2], device="cpu")
+    tab = st.block_tables.numpy()
+    for j, r in enumerate(rows):
+        for li, l in enumerate([0, 2]):
+            full_k = W.bf16_bits(st.k_pools[l])[tab[r]]
+            full_v = W.bf16_bits(st.v_pools[l])[tab[r]]
+            assert np.array_equal(snap["k_pools"][li][snap["block_tables"][j]], full_k)
+            assert np.array_equal(snap["v_pools"][li][snap["block_tables"][j]], full_v)
+            assert np.array_equal(snap["window_q"][li][j], W.bf16_bits(st.window_q[l][r]))
+            assert np.array_equal(snap["decode_q"][li][j], W.bf16_bits(st.decode_q[l][r]))
+    # rows 4..7 form a whole sharing group: its prefix blocks keep refcount 4
+    pre = snap["block_tables"][0, :2]
+    assert (snap["refcount"][pre] == 4).all()
+    assert np.array_equal(snap["block_tables"][1, :2], pre)
+    assert snap["free_count"] == len(rows) * wl.N
+    used = np.unique(snap["block_tables"][snap["block_tables"] >= 0])
+    assert np.array_equal(used, np.arange(used.size))
+    assert snap["lengths"].tolist() == [wl.T] * len(rows)
