@@ -340,13 +340,14 @@ def test_overlapped_compress_and_decode_match_serial(orc):
         main = torch.cuda.current_stream()
         s_dec = torch.cuda.Stream(priority=-1) if overlap else main
         s_cmp = torch.cuda.Stream() if overlap else main
+        # the queries exist before the fork and live until the synchronisation
+        qs = [st.decode_q[l][drows.long()].contiguous() for l in range(wl.L)]
         ev = torch.cuda.Event()
         ev.record(main)
         s_dec.wait_event(ev)
         s_cmp.wait_event(ev)
         for l in range(wl.L):
-            q = st.decode_q[l][drows.long()].contiguous()
-            cache.decode(l, q, st.block_tables, st.lengths, 1.0 / math.sqrt(wl.d), outs[l],
+            cache.decode(l, qs[l], st.block_tables, st.lengths, 1.0 / math.sqrt(wl.d), outs[l],
                          req_idx=drows, stream=s_dec)
         cache.compress(st.block_tables, st.lengths, st.window_q, wl.N, wl.w, wl.lam,
                        st.free_ids, st.free_count, st.refcount, req_idx=st.compress_rows,

@@ -112,6 +112,10 @@ def _overlapped_step(st, cache, k_new, v_new, outs, compress):
     main = torch.cuda.current_stream()
     s_dec = torch.cuda.Stream(priority=-1)
     s_cmp = torch.cuda.Stream()
+    # every layer's queries exist before the streams fork and stay alive until
+    # the synchronisation below (a temporary freed on this stream while the
+    # decode stream still reads it could be handed to the next allocation)
+    qs = [st.decode_q[l][drows.long()].contiguous() for l in range(wl.L)]
     cache.append_slots(st.block_tables, st.lengths, wl.N, st.free_ids, st.free_count,
                        st.refcount, req_idx=drows, stream=main)
     ev = torch.cuda.Event()
@@ -120,13 +124,13 @@ def _overlapped_step(st, cache, k_new, v_new, outs, compress):
     s_cmp.wait_event(ev)
     scale = 1.0 / math.sqrt(wl.d)
     for l in range(wl.L):
-        q = st.decode_q[l][drows.long()].contiguous()
         cache.append_kv(l, k_new[l], v_new[l], st.block_tables, st.lengths, req_idx=drows,
                         stream=s_dec)
-        cache.decode(l, q, st.block_tables, st.lengths, scale, outs[l], req_idx=drows,
+        cache.decode(l, qs[l], st.block_tables, st.lengths, scale, outs[l], req_idx=drows,
                      stream=s_dec)
     compress(s_cmp)
     torch.cuda.synchronize()
+    del qs
     assert cache.status() == zp.OK
 
 
