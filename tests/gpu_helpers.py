@@ -272,8 +272,11 @@ def check_compress(orc, st: W.CacheState, sample_rows=None, sample_layers=None, 
     return chk.verify(threads)
 
 
-def check_decode(orc, st: W.CacheState, layer, rows=None, lengths=None, scale=None, cache=None):
-    """GPU decode attention for table rows `rows` (all when None) vs the oracle."""
+def check_decode(orc, st: W.CacheState, layer, rows=None, lengths=None, scale=None, cache=None,
+                 out_offset=0):
+    """GPU decode attention for table rows `rows` (all when None) vs the oracle.
+    out_offset: elements between a 16-byte boundary and the output (1 puts it
+    on a 2-byte boundary only)."""
     wl = st.wl
     dev = st.block_tables.device
     cache = cache or make_cache(st)
@@ -281,7 +284,8 @@ def check_decode(orc, st: W.CacheState, layer, rows=None, lengths=None, scale=No
     rows = torch.arange(nrows, device=dev, dtype=torch.int32) if rows is None else rows
     lens = st.lengths if lengths is None else lengths
     q = st.decode_q[layer][rows.long()].contiguous()
-    out = torch.full_like(q, float("nan"))
+    buf = torch.full((q.numel() + out_offset,), float("nan"), dtype=q.dtype, device=dev)
+    out = buf[out_offset:].view(q.shape)
     scale = 1.0 / math.sqrt(wl.d) if scale is None else scale
     cache.decode(layer, q, st.block_tables, lens, scale, out, req_idx=rows)
     assert cache.status() == zp.OK

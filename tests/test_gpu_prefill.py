@@ -153,6 +153,11 @@ def check_prefill(orc, c, req_idx=None, sample=None):
     dict(lens=[129, 140], n_max=8, d=128, w=1, Hq=2),                         # w 1, G 1
     dict(lens=[333, 700], n_max=8, d=128, w=16, Hq=8),                        # 64 window rows
     dict(lens=[2500, 4096, 3001], n_max=128, d=128, w=8, Hq=8),               # budget 2048
+    # prompts of the bench's admission workload: several 2048-token chunks
+    dict(lens=[7534, 4108], n_max=128, d=128, w=8, Hq=8),
+    dict(lens=[8192, 5000, 2049], n_max=128, d=128, w=8, Hq=8, group=3, prefix_blocks=6),
+    dict(lens=[8200, 9001], n_max=128, d=128, w=8, Hq=8),                     # 5 chunks
+    dict(lens=[3100, 4000], n_max=128, d=128, w=16, Hq=8),                    # 64 rows
 ])
 def test_prefill_parity(orc, case):
     case = dict(case)
