@@ -1,6 +1,7 @@
 // zp_api.cu -- the C ABI declared in include/zp.h: handle, argument checks,
 // TMA tensor maps, launches.  Host code only.
 #include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
+#include <nvtx3/nvToolsExt.h>  // header-only; the ranges cost a pointer test without a profiler
 
 #include <algorithm>
 #include <cmath>
@@ -17,6 +18,15 @@ using zp::Workspace;
 namespace {
 
 constexpr int kMaxSplits = 16;
+
+// NVTX range around one entry point (host side: the argument checks and the
+// launches it enqueues), named after it, for timeline profilers.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 struct Alloc {
     size_t off = 0;
@@ -93,6 +103,7 @@ const char *zp_status_string(zp_status s)
 
 zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
 {
+    NvtxRange nvtx("zp_cache_create");
     if (!desc || !out)
         return ZP_ERR_INVALID_ARG;
     const zp_cache_desc &D = *desc;
@@ -239,6 +250,7 @@ zp_status zp_compress(zp_cache *c, int32_t *block_tables, int32_t bt_stride, int
                       int32_t n_max, int32_t window, float lambda, const zp_block_pool *pool,
                       void *stream, float *scores_out, int32_t *kept_out)
 {
+    NvtxRange nvtx("zp_compress");
     if (!c || !block_tables || !lengths || !window_q || !pool || !pool->free_ids ||
         !pool->free_count || !pool->refcount)
         return ZP_ERR_INVALID_ARG;
@@ -357,6 +369,7 @@ zp_status zp_compress_prefill(zp_cache *c, int32_t *block_tables, int32_t bt_str
                               size_t workspace_bytes, void *stream, float *scores_out,
                               int32_t *kept_out)
 {
+    NvtxRange nvtx("zp_compress_prefill");
     if (!c || !block_tables || !lengths || !window_q || !pool || !pool->free_ids ||
         !pool->free_count || !pool->refcount)
         return ZP_ERR_INVALID_ARG;
@@ -468,6 +481,7 @@ zp_status zp_paged_decode_attn(zp_cache *c, int32_t layer, const void *q,
                                const int32_t *lengths, const int32_t *req_idx, int32_t R,
                                float scale, void *out, void *stream)
 {
+    NvtxRange nvtx("zp_paged_decode_attn");
     if (!c || !q || !block_tables || !lengths || !out)
         return ZP_ERR_INVALID_ARG;
     if (layer < 0 || layer >= c->L || R < 0 || R > c->max_requests || num_rows < 1 ||
@@ -521,6 +535,7 @@ zp_status zp_append_slots(zp_cache *c, int32_t *block_tables, int32_t bt_stride,
                           int32_t n_max, const zp_block_pool *pool, void *stream,
                           int32_t *trigger_rows, int32_t *trigger_count)
 {
+    NvtxRange nvtx("zp_append_slots");
     if (!c || !block_tables || !lengths || !pool || !pool->free_ids || !pool->free_count ||
         !pool->refcount)
         return ZP_ERR_INVALID_ARG;
@@ -566,6 +581,7 @@ zp_status zp_append_kv(zp_cache *c, int32_t layer, const void *k_new, const void
                        const int32_t *block_tables, int32_t bt_stride, int32_t num_rows,
                        const int32_t *lengths, const int32_t *req_idx, int32_t R, void *stream)
 {
+    NvtxRange nvtx("zp_append_kv");
     if (!c || !k_new || !v_new || !block_tables || !lengths)
         return ZP_ERR_INVALID_ARG;
     if (layer < 0 || layer >= c->L || R < 0 || R > c->max_requests || num_rows < 1 ||
@@ -617,6 +633,7 @@ zp_status zp_alloc_rows(zp_cache *c, int32_t *block_tables, int32_t bt_stride, i
                         int32_t *lengths, const int32_t *req_idx, int32_t R,
                         const int32_t *counts, const zp_block_pool *pool, void *stream)
 {
+    NvtxRange nvtx("zp_alloc_rows");
     zp_status st = rows_checks(c, block_tables, bt_stride, num_rows, lengths, R, pool);
     if (st != ZP_OK)
         return st;
@@ -637,6 +654,7 @@ zp_status zp_release_rows(zp_cache *c, int32_t *block_tables, int32_t bt_stride,
                           int32_t num_rows, int32_t *lengths, const int32_t *req_idx, int32_t R,
                           const zp_block_pool *pool, void *stream)
 {
+    NvtxRange nvtx("zp_release_rows");
     zp_status st = rows_checks(c, block_tables, bt_stride, num_rows, lengths, R, pool);
     if (st != ZP_OK)
         return st;
@@ -655,6 +673,7 @@ zp_status zp_fork_rows(zp_cache *c, int32_t *block_tables, int32_t bt_stride, in
                        int32_t *lengths, const int32_t *src_rows, const int32_t *dst_rows,
                        int32_t n, int32_t *refcount, void *stream)
 {
+    NvtxRange nvtx("zp_fork_rows");
     if (!c || !block_tables || !lengths || !refcount || (n > 0 && (!src_rows || !dst_rows)))
         return ZP_ERR_INVALID_ARG;
     if (n < 0 || num_rows < 1 || num_rows > c->max_requests || n > num_rows || bt_stride < 1)
@@ -676,6 +695,7 @@ zp_status zp_global_redundancy(zp_cache *c, const int32_t *block_tables, int32_t
                                int32_t num_rows, const int32_t *lengths, const int32_t *req_idx,
                                int32_t R, float *red_out, void *stream)
 {
+    NvtxRange nvtx("zp_global_redundancy");
     if (!c || !block_tables || !lengths || !red_out || !aligned(red_out, 4))
         return ZP_ERR_INVALID_ARG;
     if (R < 0 || R > c->max_requests || num_rows < 1 || bt_stride < 1)
@@ -713,6 +733,7 @@ zp_status zp_global_redundancy_gram(zp_cache *c, const int32_t *block_tables,
                                     const int32_t *req_idx, int32_t R, float *red_out,
                                     void *stream)
 {
+    NvtxRange nvtx("zp_global_redundancy_gram");
     if (!c || !block_tables || !lengths || !red_out || !aligned(red_out, 4))
         return ZP_ERR_INVALID_ARG;
     if (R < 0 || R > c->max_requests || num_rows < 1 || bt_stride < 1)
@@ -750,6 +771,7 @@ zp_status zp_global_redundancy_gram(zp_cache *c, const int32_t *block_tables,
 
 zp_status zp_cache_status(zp_cache *c, void *stream, int32_t *out_status)
 {
+    NvtxRange nvtx("zp_cache_status");
     if (!c || !out_status)
         return ZP_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
