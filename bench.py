@@ -838,6 +838,7 @@ def run_gpu(args, world, rank, local):
     E = args.e2e_steps or K
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    # (a) one step at a time: copies, compression, attention, copies back
     e2e_ms_total = 0.0
     for i in range(E + 3):
         restore()
@@ -858,7 +859,15 @@ def run_gpu(args, world, rank, local):
         e1.synchronize()
         if i >= 3:
             e2e_ms_total += e0.elapsed_time(e1)
-    e2e_ms = e2e_ms_total / E
+    e2e_serial_ms = e2e_ms_total / E
+    # (b) as a serving loop runs it: step i+1's inputs cross on a copy stream
+    # into the other of two device buffer sets while step i computes; every
+    # step's inputs and results still cross inside the timed region.  The
+    # pools stay resident (no restore between steps: each step compresses
+    # the cache the previous one left, its block state restored from that
+    # step's host inputs -- the same work on different bytes).
+    e2e_ms = pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_state,
+                           h_out, h_tab, h_len, req_idx, dec_rows, scale, E)
     status2 = cache.status()
 
     # ablation: the redundancy of every key against all keys of its unit (the
@@ -894,8 +903,8 @@ def run_gpu(args, world, rank, local):
         del red_all
 
     # max over ranks
-    step_ms, comp_avg, dec_avg, e2e_ms, t_wall, abl_ms, gram_ms = reduce_max(
-        [step_ms, comp_avg, dec_avg, e2e_ms, t_wall, abl_ms, gram_ms], world, dev)
+    step_ms, comp_avg, dec_avg, e2e_ms, e2e_serial_ms, t_wall, abl_ms, gram_ms = reduce_max(
+        [step_ms, comp_avg, dec_avg, e2e_ms, e2e_serial_ms, t_wall, abl_ms, gram_ms], world, dev)
 
     if rank != 0:
         if world > 1:
@@ -961,7 +970,13 @@ def run_gpu(args, world, rank, local):
                                     "plus q and out"},
         "e2e": {"value": world * req_tokens / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms,
+                "how": "C ABI calls; each step's inputs (window and decode queries, block state) "
+                       "cross from pinned host memory on a copy stream into one of two device "
+                       "buffer sets while the previous step computes, each step's outputs "
+                       "(attention, tables, lengths) cross back; the KV pools stay resident",
+                "serial_ms_per_step": e2e_serial_ms,
+                "serial_value": world * req_tokens / (e2e_serial_ms * 1e-3)},
         "gpu_launches": K * (3 + wl.L * (1 if cache_splits_one(wl, Rc, cache) else 2)),
         "wall_s_timed_loop": t_wall,
         "ablation_all_keys_redundancy": None if args.no_ablations else {
@@ -982,6 +997,67 @@ def run_gpu(args, world, rank, local):
     if world > 1:
         dist.destroy_process_group()
     return res
+
+
+def pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_state, h_out, h_tab,
+                  h_len, req_idx, dec_rows, scale, E):
+    """Steps through the C ABI with double-buffered host inputs: the copy
+    stream brings step i+1's inputs into one device buffer set while the
+    compute stream runs step i on the other; ms per step over E timed steps
+    (after 2 warm-up steps; the first timed step's inputs are not overlapped)."""
+    comp = torch.cuda.current_stream()
+    cp = torch.cuda.Stream()
+    d_wq = [torch.empty_like(st.window_q) for _ in range(2)]
+    d_q = [[torch.empty_like(x) for x in q] for _ in range(2)]
+    d_state = [[torch.empty_like(t) for t in pristine] for _ in range(2)]
+    ready = [torch.cuda.Event() for _ in range(2)]
+    free = [torch.cuda.Event() for _ in range(2)]
+
+    def bring(i):
+        b = i % 2
+        if i >= 2:
+            cp.wait_event(free[b])
+        with torch.cuda.stream(cp):
+            d_wq[b].copy_(h_wq, non_blocking=True)
+            for x, h in zip(d_q[b], h_q):
+                x.copy_(h, non_blocking=True)
+            for x, h in zip(d_state[b], h_state):
+                x.copy_(h, non_blocking=True)
+        ready[b].record(cp)
+
+    def run(i):
+        b = i % 2
+        comp.wait_event(ready[b])
+        for x, y in zip(live, d_state[b]):
+            x.copy_(y, non_blocking=True)
+        cache.compress(st.block_tables, st.lengths, d_wq[b], wl.N, wl.w, wl.lam, st.free_ids,
+                       st.free_count, st.refcount, req_idx=req_idx)
+        for l in range(wl.L):
+            cache.decode(l, d_q[b][l], st.block_tables, st.lengths, scale, out[l],
+                         req_idx=dec_rows)
+        for h, x in zip(h_out, out):
+            h.copy_(x, non_blocking=True)
+        h_tab.copy_(st.block_tables, non_blocking=True)
+        h_len.copy_(st.lengths, non_blocking=True)
+        free[b].record(comp)
+
+    def loop(steps):
+        bring(0)
+        for i in range(steps):
+            if i + 1 < steps:
+                bring(i + 1)
+            run(i)
+
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    loop(2)  # warm-up
+    torch.cuda.synchronize()
+    t0.record(comp)
+    cp.wait_event(t0)  # the first step's inputs too cross inside the timed region
+    loop(E)
+    t1.record(comp)
+    t1.synchronize()
+    return t0.elapsed_time(t1) / E
 
 
 def cache_splits_one(wl, R, cache):
