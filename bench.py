@@ -405,11 +405,77 @@ def run_mixed(args, world, rank, local):
         a1.synchronize()
         if i >= 2:
             e2e.append(a0.elapsed_time(a1))
-    e2e_ms = sum(e2e) / len(e2e)
+    e2e_serial_ms = sum(e2e) / len(e2e)
+    # as a serving loop runs it: the next step's inputs cross on a copy stream
+    # into the other of two device buffer sets while this step computes (the
+    # pools stay resident: no restore between steps)
+    cp = torch.cuda.Stream(device=dev)
+    d_wq = [torch.empty_like(st.window_q) for _ in range(2)]
+    d_in = [[torch.empty_like(x) for x in q + k_new + v_new] for _ in range(2)]
+    d_state = [[torch.empty_like(t) for t in pristine] for _ in range(2)]
+    ready = [torch.cuda.Event() for _ in range(2)]
+    free = [torch.cuda.Event() for _ in range(2)]
+    L = wl.L
+
+    def bring(i):
+        b = i % 2
+        if i >= 2:
+            cp.wait_event(free[b])
+        with torch.cuda.stream(cp):
+            d_wq[b].copy_(h_wq, non_blocking=True)
+            for x, h in zip(d_in[b] + d_state[b], h_q + h_kv + h_state):
+                x.copy_(h, non_blocking=True)
+        ready[b].record(cp)
+
+    def run(i):
+        b = i % 2
+        main.wait_event(ready[b])
+        for x, y in zip(live, d_state[b]):
+            x.copy_(y, non_blocking=True)
+        append_slots(main)
+        ea = ev()
+        ea.record(main)
+        s_dec.wait_event(ea)
+        s_cmp.wait_event(ea)
+        dq, dk, dv = d_in[b][:L], d_in[b][L:2 * L], d_in[b][2 * L:]
+        for l in range(L):
+            cache.append_kv(l, dk[l], dv[l], st.block_tables, st.lengths, req_idx=drows,
+                            stream=s_dec)
+            cache.decode(l, dq[l], st.block_tables, st.lengths, scale, out[l], req_idx=drows,
+                         stream=s_dec)
+        cache.compress(st.block_tables, st.lengths, d_wq[b], wl.N, wl.w, wl.lam, st.free_ids,
+                       st.free_count, st.refcount, req_idx=st.compress_rows, stream=s_cmp)
+        dd, cc = ev(), ev()
+        dd.record(s_dec)
+        cc.record(s_cmp)
+        main.wait_event(dd)
+        main.wait_event(cc)
+        for h, x in zip(h_out, out):
+            h.copy_(x, non_blocking=True)
+        h_tab.copy_(st.block_tables, non_blocking=True)
+        h_len.copy_(st.lengths, non_blocking=True)
+        free[b].record(main)
+
+    def loop(steps):
+        bring(0)
+        for i in range(steps):
+            if i + 1 < steps:
+                bring(i + 1)
+            run(i)
+
+    loop(2)
+    torch.cuda.synchronize()
+    p0, p1 = ev(), ev()
+    p0.record(main)
+    cp.wait_event(p0)
+    loop(E)
+    p1.record(main)
+    p1.synchronize()
+    e2e_ms = p0.elapsed_time(p1) / E
     assert cache.status() == zp.OK
 
-    ov, se, slot_ms, dec_ms, cmp_ms, e2e_ms = reduce_max(
-        [ov, se, slot_ms, dec_ms, cmp_ms, e2e_ms], world, dev)
+    ov, se, slot_ms, dec_ms, cmp_ms, e2e_ms, e2e_serial_ms = reduce_max(
+        [ov, se, slot_ms, dec_ms, cmp_ms, e2e_ms, e2e_serial_ms], world, dev)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -452,7 +518,14 @@ def run_mixed(args, world, rank, local):
         "step_frac_overlapped": step_bytes / (ov * 1e-3) / 1e9 / peak,
         "e2e": {"value": world * Rc * wl.T / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms,
+                "how": "C ABI calls, overlapped as above; each step's inputs (window queries, "
+                       "decode queries, new K/V rows, block state) cross from pinned host memory "
+                       "on a copy stream into one of two device buffer sets while the previous "
+                       "step computes, its outputs (attention, tables, lengths) cross back; the "
+                       "KV pools stay resident",
+                "serial_ms_per_step": e2e_serial_ms,
+                "serial_value": world * Rc * wl.T / (e2e_serial_ms * 1e-3)},
         "gpu_launches": 2 * K * (2 + 3 + wl.L * (
             2 if cache_splits_one(wl, drows.numel(), cache) else 3)),
         "clocks": clk.summary(),
