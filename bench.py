@@ -1144,7 +1144,7 @@ def cache_splits_one(wl, R, cache):
     import torch
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     pairs = R * wl.Hkv
-    splits = min(16, max(1, (4 * sms + pairs - 1) // pairs))
+    splits = min(16, max(1, (sms + pairs - 1) // pairs))
     splits = min(splits, max(1, wl.N // 4))
     bps = (wl.N + splits - 1) // splits
     return (wl.N + bps - 1) // bps == 1

@@ -496,10 +496,12 @@ zp_status zp_paged_decode_attn(zp_cache *c, int32_t layer, const void *q,
     if (!on_device(c))
         return ZP_ERR_INVALID_ARG;
 
-    // splits per (request, kv head): enough CTAs for ~4 per SM, at most
-    // kMaxSplits, never fewer than 4 blocks per split
+    // splits per (request, kv head): one split when the pairs alone give every
+    // SM a CTA (the hardware scheduler balances the waves; a split adds
+    // partials and a combine launch), else enough to give every SM one, at
+    // most kMaxSplits, never fewer than 4 blocks per split
     const int pairs = R * c->Hkv;
-    const int target = 4 * c->num_sms;
+    const int target = c->num_sms;
     int splits = std::min(kMaxSplits, std::max(1, (target + pairs - 1) / pairs));
     splits = std::min(splits, std::max(1, bt_stride / 4));
     const int bps = (bt_stride + splits - 1) / splits;

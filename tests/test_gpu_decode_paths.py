@@ -59,7 +59,7 @@ def test_small_calls(orc, lengths):
 
 
 def test_output_on_a_2_byte_boundary(orc):
-    st, lens = _ragged(24, 96, 3)  # 192 (request, kv head) pairs: several splits per pair
+    st, lens = _ragged(12, 96, 3)  # 96 (request, kv head) pairs: two splits per pair
     H.check_decode(orc, st, 0, lengths=lens, out_offset=1)
 
 
