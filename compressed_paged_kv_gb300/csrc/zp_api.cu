@@ -71,6 +71,25 @@ bool encode_pool_map(CUtensorMap *map, void *pool, int num_blocks, int hkv, int 
     return res == CUDA_SUCCESS;
 }
 
+// The same 2D view with a box of one whole row ({d columns, 1 row}) and no
+// swizzle: the compaction gathers four arbitrary pool rows per load
+// (tile::gather4, whose box is one row high) into a [16][d] destination slab.
+bool encode_row_map(CUtensorMap *map, void *pool, int num_blocks, int hkv, int d)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(d),
+                          static_cast<cuuint64_t>(num_blocks) * hkv * zp::kBlk};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(d), 1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
@@ -154,6 +173,8 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
     const size_t o_smw = A.take(4 * 3 * zp::kSmSlots);
     const size_t o_kmaps = A.take(sizeof(CUtensorMap) * D.num_layers, 128);
     const size_t o_vmaps = A.take(sizeof(CUtensorMap) * D.num_layers, 128);
+    const size_t o_krmaps = A.take(sizeof(CUtensorMap) * D.num_layers, 128);
+    const size_t o_vrmaps = A.take(sizeof(CUtensorMap) * D.num_layers, 128);
     const size_t o_kp = A.take(sizeof(void *) * D.num_layers);
     const size_t o_vp = A.take(sizeof(void *) * D.num_layers);
     const size_t o_dst = A.take(4 * entries);
@@ -184,6 +205,8 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
     ws.smwave = reinterpret_cast<uint32_t *>(b + o_smw);
     ws.kmaps = reinterpret_cast<CUtensorMap *>(b + o_kmaps);
     ws.vmaps = reinterpret_cast<CUtensorMap *>(b + o_vmaps);
+    ws.krmaps = reinterpret_cast<CUtensorMap *>(b + o_krmaps);
+    ws.vrmaps = reinterpret_cast<CUtensorMap *>(b + o_vrmaps);
     ws.kpools = reinterpret_cast<void **>(b + o_kp);
     ws.vpools = reinterpret_cast<void **>(b + o_vp);
     ws.dst_table = reinterpret_cast<int32_t *>(b + o_dst);
@@ -203,11 +226,14 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
     c->kpools.assign(D.k_pools, D.k_pools + D.num_layers);
     c->vpools.assign(D.v_pools, D.v_pools + D.num_layers);
 
-    std::vector<CUtensorMap> kmaps(D.num_layers), vmaps(D.num_layers);
+    std::vector<CUtensorMap> kmaps(D.num_layers), vmaps(D.num_layers), krmaps(D.num_layers),
+        vrmaps(D.num_layers);
     bool ok = true;
     for (int l = 0; l < D.num_layers && ok; ++l) {
         ok = encode_pool_map(&kmaps[l], D.k_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim) &&
-             encode_pool_map(&vmaps[l], D.v_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim);
+             encode_pool_map(&vmaps[l], D.v_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim) &&
+             encode_row_map(&krmaps[l], D.k_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim) &&
+             encode_row_map(&vrmaps[l], D.v_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim);
     }
     ok = ok && cudaMemset(c->base, 0, o_kmaps) == cudaSuccess &&
          cudaMemset(b + o_rowmark, 0, 4 * static_cast<size_t>(D.max_requests)) == cudaSuccess &&
@@ -215,6 +241,10 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
          cudaMemcpy(ws.kmaps, kmaps.data(), sizeof(CUtensorMap) * D.num_layers,
                     cudaMemcpyHostToDevice) == cudaSuccess &&
          cudaMemcpy(ws.vmaps, vmaps.data(), sizeof(CUtensorMap) * D.num_layers,
+                    cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(ws.krmaps, krmaps.data(), sizeof(CUtensorMap) * D.num_layers,
+                    cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(ws.vrmaps, vrmaps.data(), sizeof(CUtensorMap) * D.num_layers,
                     cudaMemcpyHostToDevice) == cudaSuccess &&
          cudaMemcpy(ws.kpools, D.k_pools, sizeof(void *) * D.num_layers,
                     cudaMemcpyHostToDevice) == cudaSuccess &&
@@ -426,6 +456,8 @@ zp_status zp_compress_prefill(zp_cache *c, int32_t *block_tables, int32_t bt_str
     const size_t U = static_cast<size_t>(units);
     zp::PrefillArgs a{};
     a.kmaps = c->ws.kmaps;
+    a.krmaps = c->ws.krmaps;
+    a.vrmaps = c->ws.vrmaps;
     a.kpools = c->ws.kpools;
     a.vpools = c->ws.vpools;
     a.tables = block_tables;

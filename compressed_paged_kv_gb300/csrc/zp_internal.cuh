@@ -31,6 +31,8 @@ struct Workspace {
                          //      zeroed by the finalize kernel
     CUtensorMap *kmaps;  // [L]  K pool maps, 128B swizzle, box {64, 16}
     CUtensorMap *vmaps;  // [L]  V pool maps, same
+    CUtensorMap *krmaps; // [L]  K pool maps, no swizzle, box {d, 1}: one pool row (row gathers)
+    CUtensorMap *vrmaps; // [L]  V pool maps, same
     void **kpools;       // [L]  device copies of the pool pointers
     void **vpools;       // [L]
     int32_t *dst_table;  // [max_requests * max_blocks] plan: destination blocks
@@ -138,6 +140,7 @@ struct PrefillArgs {
     float lambda;
     float inv_rows;
     float logit_scale;
+    const CUtensorMap *krmaps, *vrmaps;  // per layer: one pool row per box (row gathers)
 };
 
 struct AppendArgs {
@@ -306,6 +309,33 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+
+// TMA row gather: four rows y0..y3 (a box one row high) of a 2D tensor map,
+// columns from x, land one after the other at dst; completion counted on an
+// mbarrier.
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, int x, int y0,
+                                            int y1, int y2, int y3, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Waits until at most N committed bulk groups of this thread still read their
+// shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Waits until every committed bulk group of this thread is complete.
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Bulk (untiled) copy global -> shared; 16-byte aligned, size multiple of 16.

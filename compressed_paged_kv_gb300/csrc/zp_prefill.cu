@@ -22,14 +22,15 @@
 //       in shared memory) of the K_keep-th largest score; ties at the
 //       threshold go to the lower index; the kept positions in ascending
 //       order by block scans, then the window.
-//   zp_prefill_compact_kernel  one CTA per unit: the source and destination
-//       pool rows of up to 2,048 destination rows resolved into shared memory
-//       first, then destination rows in ascending chunks of 32; a chunk's
-//       source rows are read before any of its writes (one barrier), and
-//       every later chunk reads sources at or after its own first destination
-//       (kept[j] >= j), which no earlier chunk writes -- so compacting in
-//       place is safe, and the next chunk's rows can be loaded while this
-//       chunk's are stored.
+//   zp_prefill_gather_kernel  one CTA per unit: the source pool row of every
+//       destination row resolved into shared memory, then the destination
+//       blocks in ascending order through a ring of shared-memory stages:
+//       TMA row gathers (tile::gather4, four arbitrary pool rows per load)
+//       of each block's 16 K and 16 V rows, written back as the block's two
+//       contiguous slabs by bulk stores.  Every later block reads sources at
+//       or after its own position (kept[j] >= j), which no earlier block's
+//       store writes -- so compacting in place is safe with loads running
+//       ahead of the stores.
 #include "zp_internal.cuh"
 
 namespace zp {
@@ -40,8 +41,6 @@ constexpr int kPStages = 2;                  // TMA stages per warp
 constexpr int kPChunk = kPrefillChunk;       // tokens per scoring CTA
 constexpr int kPBlocks = kPChunk / kBlk;
 constexpr int kSelThreads = 1024;
-constexpr int kCmpThreads = 256;
-constexpr int kCmpRows = 32;                 // destination rows per compaction chunk
 constexpr int kCmpSeg = 2048;                // destination rows whose indices are staged at once
 
 template <int D, int MT>
@@ -459,15 +458,33 @@ __global__ void __launch_bounds__(kSelThreads) zp_prefill_select_kernel(const Pr
         set_error(a.sticky, ZP_ERR_DEVICE_CHECK);
 }
 
+// Compaction by TMA row gathers: one CTA per unit.  The source pool row of
+// every destination row is resolved into shared memory first (all threads);
+// then one thread streams the destination blocks in ascending order through
+// a ring of kGatStages shared-memory stages: a stage takes a destination
+// block's 16 K rows and 16 V rows with eight tile::gather4 loads (four
+// arbitrary pool rows each, one row per box) and leaves as two bulk stores,
+// the block's contiguous K and V slabs.  Loads run kGatAhead blocks ahead of
+// the store.  In place this is safe: the sources of destination block p lie
+// at positions >= 16 p (kept[j] >= j), so block p's slab is written only
+// after every load that reads it -- its own and all earlier blocks' -- has
+// landed, and the blocks loaded ahead read only later positions.  A block
+// whose 16 rows all stay where they are is skipped.
+constexpr int kGatThreads = 256;
+constexpr int kGatStages = 8;
+constexpr int kGatAhead = 5;
+static_assert(kGatAhead < kGatStages, "a stage is reused only after its store read it");
+
 template <int D>
-__global__ void __launch_bounds__(kCmpThreads) zp_prefill_compact_kernel(const PrefillArgs a)
+__global__ void __launch_bounds__(kGatThreads) zp_prefill_gather_kernel(const PrefillArgs a)
 {
-    constexpr int VPR = D / 8;                                  // 16-byte vectors per row
-    constexpr int ITEMS = kCmpRows * VPR * 2 / kCmpThreads;     // K and V
-    constexpr uint32_t kNone = 0xffffffffu;
-    // pool rows (block * Hkv + h) * b + slot of the source and the destination
-    // of each destination row of the segment, kNone: nothing to move
-    __shared__ uint32_t sSrc[kCmpSeg], sDst[kCmpSeg];
+    constexpr int SLAB = kBlk * D * 2;  // one (block, kv head) slab of K or of V
+    __shared__ uint32_t sSrc[kCmpSeg];               // source pool row of each destination row
+    __shared__ uint8_t sMove[kCmpSeg / kBlk];        // the destination block moves a row
+    __shared__ __align__(8) uint64_t full[kGatStages];
+    extern __shared__ uint8_t smem_raw[];            // [kGatStages][K slab, V slab]
+    uint8_t *stage = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
     if (*(volatile int32_t *)a.call != 0)
         return;
     const int u = blockIdx.x;
@@ -478,66 +495,90 @@ __global__ void __launch_bounds__(kCmpThreads) zp_prefill_compact_kernel(const P
     const int32_t *kept = a.kept + (size_t)u * KT;
     const int32_t *trow = a.tables + (size_t)row * a.stride;
     const int32_t *drow = a.dst_table + (size_t)r * a.stride;
-    uint4 *const kpool = static_cast<uint4 *>(a.kpools[l]);
-    uint4 *const vpool = static_cast<uint4 *>(a.vpools[l]);
-
-    // item `it` of a chunk: vector ch of row c0 + jj of K (kv 0) or V (kv 1)
-    struct Chunk {
-        uint4 v[ITEMS];
-        uint32_t dst[ITEMS];  // destination pool row, or kNone: nothing to move
-    };
-    auto load = [&](int n, int c0, Chunk &ck) {
-#pragma unroll
-        for (int it = 0; it < ITEMS; ++it) {
-            const int v = threadIdx.x + it * kCmpThreads;
-            const int kv = v / (kCmpRows * VPR);
-            const int rem = v - kv * kCmpRows * VPR;
-            const int jj = c0 + rem / VPR, ch = rem % VPR;
-            ck.dst[it] = kNone;
-            if (jj >= n || sSrc[jj] == kNone)
-                continue;
-            ck.v[it] = ld_global_nc_v4((kv ? vpool : kpool) + (size_t)sSrc[jj] * VPR + ch);
-            ck.dst[it] = sDst[jj];
-        }
-    };
-    auto store = [&](const Chunk &ck) {
-#pragma unroll
-        for (int it = 0; it < ITEMS; ++it) {
-            const int v = threadIdx.x + it * kCmpThreads;
-            const int kv = v / (kCmpRows * VPR), ch = v % VPR;
-            if (ck.dst[it] != kNone)
-                (kv ? vpool : kpool)[(size_t)ck.dst[it] * VPR + ch] = ck.v[it];
-        }
-    };
+    uint8_t *const kpool = static_cast<uint8_t *>(a.kpools[l]);
+    uint8_t *const vpool = static_cast<uint8_t *>(a.vpools[l]);
+    const CUtensorMap *kmap = a.krmaps + l, *vmap = a.vrmaps + l;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int s = 0; s < kGatStages; ++s)
+            mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    bool ok = true;
+    int g = 0;  // destination blocks streamed so far (all segments)
     for (int s0 = 0; s0 < KT; s0 += kCmpSeg) {
-        const int n = min(kCmpSeg, KT - s0);
-        __syncthreads();  // the previous segment's rows are stored
-        // every row's source and destination first, all rows in parallel (the
-        // copies below then wait on one load each, not on three in a row)
-        for (int jj = threadIdx.x; jj < n; jj += kCmpThreads) {
+        const int n = min(kCmpSeg, KT - s0);  // a multiple of 16
+        const int nb = n / kBlk;
+        __syncthreads();  // the previous segment's rows are issued
+        for (int q = tid; q < nb; q += kGatThreads)
+            sMove[q] = 0;
+        __syncthreads();
+        for (int jj = tid; jj < n; jj += kGatThreads) {
             const int j = s0 + jj, src = kept[j];
-            uint32_t sr = kNone, dr = kNone;
+            const uint32_t dr =
+                (static_cast<uint32_t>(drow[j / kBlk]) * a.Hkv + h) * kBlk + j % kBlk;
+            uint32_t sr = dr;  // a row that stays is gathered from where it is
             if (src < j || src >= T) {  // kept[j] >= j holds for any valid selection
                 set_error(a.sticky, ZP_ERR_DEVICE_CHECK);
             } else {
-                const int sblk = trow[src / kBlk], dblk = drow[j / kBlk];
-                if (!(sblk == dblk && src % kBlk == j % kBlk)) {  // else already in place
-                    sr = (static_cast<uint32_t>(sblk) * a.Hkv + h) * kBlk + src % kBlk;
-                    dr = (static_cast<uint32_t>(dblk) * a.Hkv + h) * kBlk + j % kBlk;
-                }
+                sr = (static_cast<uint32_t>(trow[src / kBlk]) * a.Hkv + h) * kBlk + src % kBlk;
             }
             sSrc[jj] = sr;
-            sDst[jj] = dr;
+            if (sr != dr)
+                sMove[jj / kBlk] = 1;
         }
         __syncthreads();
-        Chunk cur, nxt;
-        load(n, 0, cur);
-        for (int c0 = 0; c0 < n; c0 += kCmpRows) {
-            __syncthreads();  // every source row of this chunk read before any of its writes
-            if (c0 + kCmpRows < n)
-                load(n, c0 + kCmpRows, nxt);  // sources past this chunk: none written by it
-            store(cur);
-            cur = nxt;
+        if (tid == 0) {
+            if (s0 > 0)
+                bulk_wait_read<0>();  // stage reuse across segments: every earlier store read
+            int issued = 0, stored = 0;  // blocks of the segment loaded, stored
+            for (int step = 0; step < nb + kGatAhead && ok; ++step) {
+                const int pl = step, ps = step - kGatAhead;
+                if (pl < nb) {
+                    ++issued;
+                    const int gi = g + pl, st = gi % kGatStages;
+                    // the store that last read this stage was committed kGatStages -
+                    // kGatAhead steps ago: at most that many minus one groups may read on
+                    if (gi >= kGatStages)
+                        bulk_wait_read<kGatStages - kGatAhead - 1>();
+                    uint8_t *ks = stage + st * 2 * SLAB;
+                    if (sMove[pl]) {
+                        mbar_arrive_expect_tx(&full[st], 2 * SLAB);
+                        const uint32_t *rs = sSrc + pl * kBlk;
+#pragma unroll
+                        for (int i = 0; i < kBlk; i += 4) {
+                            tma_gather4(ks + i * D * 2, kmap, 0, rs[i], rs[i + 1], rs[i + 2],
+                                        rs[i + 3], &full[st]);
+                            tma_gather4(ks + SLAB + i * D * 2, vmap, 0, rs[i], rs[i + 1],
+                                        rs[i + 2], rs[i + 3], &full[st]);
+                        }
+                    } else {
+                        mbar_arrive_expect_tx(&full[st], 0);
+                    }
+                }
+                if (ps >= 0) {
+                    const int gi = g + ps, st = gi % kGatStages;
+                    ok &= mbar_wait(&full[st], (gi / kGatStages) & 1);
+                    if (ok && sMove[ps]) {
+                        const int p = s0 / kBlk + ps;
+                        const size_t off = ((static_cast<size_t>(drow[p]) * a.Hkv + h) * kBlk) *
+                                           (size_t)(D * 2);
+                        uint8_t *ks = stage + st * 2 * SLAB;
+                        bulk_s2g_hint(kpool + off, ks, SLAB, policy_evict_first());
+                        bulk_s2g_hint(vpool + off, ks + SLAB, SLAB, policy_evict_first());
+                    }
+                    bulk_commit();
+                    ++stored;
+                }
+            }
+            if (!ok) {
+                set_error(a.sticky, ZP_ERR_TIMEOUT);
+                // loads still in flight land before the stages go away
+                for (int pl = stored; pl < issued; ++pl)
+                    mbar_wait(&full[(g + pl) % kGatStages], ((g + pl) / kGatStages) & 1);
+            }
+            g += nb;
+            bulk_wait_all();
         }
     }
 }
@@ -573,7 +614,12 @@ static cudaError_t launch_for_d(const PrefillArgs &a, int mt, int units, cudaStr
     if (e != cudaSuccess)
         return e;
     zp_prefill_select_kernel<<<static_cast<unsigned>(units), kSelThreads, sel_smem, s>>>(a);
-    zp_prefill_compact_kernel<D><<<static_cast<unsigned>(units), kCmpThreads, 0, s>>>(a);
+    constexpr int gat_smem = kGatStages * 2 * kBlk * D * 2 + 128;
+    e = cudaFuncSetAttribute(zp_prefill_gather_kernel<D>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, gat_smem);
+    if (e != cudaSuccess)
+        return e;
+    zp_prefill_gather_kernel<D><<<static_cast<unsigned>(units), kGatThreads, gat_smem, s>>>(a);
     return cudaGetLastError();
 }
 
