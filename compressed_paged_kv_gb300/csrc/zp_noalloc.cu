@@ -10,9 +10,11 @@
 // first call there) and held until the process exits.
 //
 // The kernels here are a plain CUDA-core variant of the split-K decode
-// attention in zp_decode.cu: one CTA per (request, query head, split), a
-// warp per token at a time with a shuffle-reduced dot product, an online
-// softmax per warp, then a log-sum-exp combine.
+// attention in zp_decode.cu: one CTA per (request, query head, split); a warp
+// takes 32 / (d / 8) tokens at a time, d / 8 lanes per token row reading 16
+// bytes each, with a shuffle-reduced dot product and an online softmax per
+// token group, merged within the warp and then across warps; a log-sum-exp
+// combine over the splits.
 #include <mutex>
 
 #include "zp_internal.cuh"
@@ -42,10 +44,12 @@ struct NaArgs {
 template <int D>
 __global__ void __launch_bounds__(kNaThreads) na_decode_split(const NaArgs a)
 {
-    constexpr int PER = D / 32;  // elements of a row per lane
+    constexpr int LPR = D / 8;     // lanes per row: 16 bytes (8 elements) each
+    constexpr int TPW = 32 / LPR;  // tokens a warp takes at a time
     __shared__ float s_m[kNaWarps], s_l[kNaWarps];
     __shared__ float s_o[kNaWarps][D];
     const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+    const int sub = lane / LPR, sl = lane % LPR;  // token of the warp's group, lane in the row
     const int split = blockIdx.x, hq = blockIdx.y, r = blockIdx.z;
     const int G = a.Hq / a.Hkv, h = hq / G;
     int row = a.req_idx ? a.req_idx[r] : r;
@@ -57,47 +61,82 @@ __global__ void __launch_bounds__(kNaThreads) na_decode_split(const NaArgs a)
         len = 0;
         row = 0;
     }
-    float qv[PER];
-    const __nv_bfloat16 *qrow = a.q + ((size_t)r * a.Hq + hq) * D;
+    float qv[8];
+    const __nv_bfloat16 *qrow = a.q + ((size_t)r * a.Hq + hq) * D + sl * 8;
 #pragma unroll
-    for (int i = 0; i < PER; ++i)
-        qv[i] = __bfloat162float(qrow[lane * PER + i]);
+    for (int i = 0; i < 8; ++i)
+        qv[i] = __bfloat162float(qrow[i]);
     const int t_begin = split * a.tps, t_end = min(len, t_begin + a.tps);
-    float m = -1e30f, l = 0.f, o[PER];
+    float m = -1e30f, l = 0.f, o[8];
 #pragma unroll
-    for (int i = 0; i < PER; ++i)
+    for (int i = 0; i < 8; ++i)
         o[i] = 0.f;
-    for (int t = t_begin + wi; t < t_end; t += kNaWarps) {
-        int blk = a.tables[(size_t)row * a.stride + t / zp::kBlk];
-        if (blk < 0 || blk >= a.num_blocks) {
-            if (lane == 0 && a.status)
-                atomicCAS(a.status, 0, ZP_ERR_DEVICE_CHECK);
-            continue;
+    // the warp takes TPW consecutive tokens at a time, LPR lanes per token
+    for (int t0 = t_begin + wi * TPW; t0 < t_end; t0 += kNaWarps * TPW) {
+        const int t = t0 + sub;
+        bool valid = t < t_end;
+        size_t off = 0;
+        if (valid) {
+            const int blk = a.tables[(size_t)row * a.stride + t / zp::kBlk];
+            if (blk < 0 || blk >= a.num_blocks) {
+                if (sl == 0 && a.status)
+                    atomicCAS(a.status, 0, ZP_ERR_DEVICE_CHECK);
+                valid = false;
+            } else {
+                off = (((size_t)blk * a.Hkv + h) * zp::kBlk + t % zp::kBlk) * D + sl * 8;
+            }
         }
-        const size_t off = (((size_t)blk * a.Hkv + h) * zp::kBlk + t % zp::kBlk) * D + lane * PER;
+        uint4 kr = make_uint4(0u, 0u, 0u, 0u), vr = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) {
+            kr = zp::ld_global_nc_v4(a.kpool + off);
+            vr = zp::ld_global_nc_v4(a.vpool + off);
+        }
+        const __nv_bfloat162 *kh = reinterpret_cast<const __nv_bfloat162 *>(&kr);
         float dot = 0.f;
 #pragma unroll
-        for (int i = 0; i < PER; ++i)
-            dot += qv[i] * __bfloat162float(a.kpool[off + i]);
+        for (int i = 0; i < 4; ++i) {
+            const float2 kf = __bfloat1622float2(kh[i]);
+            dot += qv[2 * i] * kf.x + qv[2 * i + 1] * kf.y;
+        }
 #pragma unroll
-        for (int s = 16; s > 0; s >>= 1)
+        for (int s = LPR / 2; s > 0; s >>= 1)
             dot += __shfl_xor_sync(0xffffffffu, dot, s);
-        const float x = dot * a.logit_scale;
+        const float x = valid ? dot * a.logit_scale : -INFINITY;
         const float m_new = fmaxf(m, x);
-        const float corr = exp2f(m - m_new), p = exp2f(x - m_new);
+        const float corr = exp2f(m - m_new), p = valid ? exp2f(x - m_new) : 0.f;
         l = l * corr + p;
+        const __nv_bfloat162 *vh = reinterpret_cast<const __nv_bfloat162 *>(&vr);
 #pragma unroll
-        for (int i = 0; i < PER; ++i)
-            o[i] = o[i] * corr + p * __bfloat162float(a.vpool[off + i]);
+        for (int i = 0; i < 4; ++i) {
+            const float2 vf = __bfloat1622float2(vh[i]);
+            o[2 * i] = o[2 * i] * corr + p * vf.x;
+            o[2 * i + 1] = o[2 * i + 1] * corr + p * vf.y;
+        }
         m = m_new;
+    }
+    // the warp's token groups merged: lanes sl of every group hold the same columns
+#pragma unroll
+    for (int s = LPR; s < 32; s <<= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, s);
+        const float l2 = __shfl_xor_sync(0xffffffffu, l, s);
+        const float mm = fmaxf(m, m2);
+        const float f1 = exp2f(m - mm), f2 = exp2f(m2 - mm);
+        l = l * f1 + l2 * f2;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float o2 = __shfl_xor_sync(0xffffffffu, o[i], s);
+            o[i] = o[i] * f1 + o2 * f2;
+        }
+        m = mm;
     }
     if (lane == 0) {
         s_m[wi] = m;
         s_l[wi] = l;
     }
+    if (sub == 0)
 #pragma unroll
-    for (int i = 0; i < PER; ++i)
-        s_o[wi][lane * PER + i] = o[i];
+        for (int i = 0; i < 8; ++i)
+            s_o[wi][sl * 8 + i] = o[i];
     __syncthreads();
     float *p = a.part + (((size_t)r * a.Hq + hq) * a.splits + split) * kNaSlotFloats;
     float M = -1e30f;
@@ -216,6 +255,8 @@ extern "C" zp_status zp_paged_decode_attn_noalloc(
 {
     if (!k_pool || !v_pool || !q || !block_tables || !lengths || !out)
         return ZP_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(k_pool) % 16 || reinterpret_cast<uintptr_t>(v_pool) % 16)
+        return ZP_ERR_INVALID_ARG;  // pool rows are read 16 bytes at a time
     if (num_blocks < 1 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads ||
         R < 0 || num_rows < 1 || bt_stride < 1 || !(scale == scale))
         return ZP_ERR_INVALID_ARG;

@@ -233,7 +233,8 @@ zp_status zp_paged_decode_attn(zp_cache *cache, int32_t layer, const void *q,
  * context -- usually at the first call in that context -- and held until the
  * process exits.
  *
- *  k_pool, v_pool  device bf16 pools of one layer, [num_blocks][num_kv_heads][16][head_dim]
+ *  k_pool, v_pool  device bf16 pools of one layer, [num_blocks][num_kv_heads][16][head_dim],
+ *                  16-byte aligned (ZP_ERR_INVALID_ARG otherwise)
  *  q, out          device bf16 [R][num_q_heads][head_dim]; other arguments as in
  *                  zp_paged_decode_attn
  *  status          nullable device int32: device-detected errors (a length or
