@@ -4,8 +4,10 @@
 A step = one zp_compress call over every request, layer and kv head of the
 workload (plan, fused score/select/compact kernel, finalize) followed by
 paged decode attention over the compacted tables, one call per layer.
-Default workload: Qwen3-8B-shaped single layer (8/32 heads, d 128, b 16,
-N_max 128, w 8, lambda 0.5, 64 requests at N_max, no sharing).
+Default workload: Qwen3-8B-shaped, 36 layers (8/32 heads, d 128, b 16,
+N_max 128, w 8, lambda 0.5), 256 requests at N_max in 32 groups of 8 sharing
+a 4-block prompt prefix (the shared blocks compress into fresh target
+blocks), K AR(1) rho 0.9 with 1% heavy hitters.
 
 Before each step (outside the timed events) the KV pools, block tables,
 lengths, refcounts and free stack are restored from a pristine device copy and
@@ -13,7 +15,8 @@ a 256 MiB buffer is written to flush L2, so every step compresses the
 workload's own data from HBM.
 
 `--impl reference` times the CPU oracle (plain fp64 C, all host cores) on
-the same workload instead.  Under torchrun each rank runs its own replica
+bounded slices of the same workload instead (the same config, steps and
+warm-up).  Under torchrun each rank runs its own replica
 (weak scaling, no collective on the data path); rank 0 prints one JSON line.
 """
 from __future__ import annotations
