@@ -75,3 +75,27 @@ def test_samples_of_the_oracle_legs():
         assert len(rows) * len(layers) * wl.Hkv >= min(1024, wl.units())
         rows, layers = bench.reference_step_sample(wl, 3)
         assert len(rows) * len(layers) * wl.Hkv <= 1024
+
+
+def test_moved_rows_count_of_the_algorithmic_bytes():
+    """The bench's algorithmic bytes count 3 row copies per moved row: a row
+    moves unless it keeps its position in the same physical block.  Hand-made
+    kept sets over N = 3 blocks of b = 4 (8 destination rows, 4 evicted)."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    from compressed_paged_kv_gb300 import workloads as W
+    wl = W.scaled(W.WORKLOADS["tiny"], b=4, N=3)
+    src = torch.tensor([[10, 11, 12], [20, 21, 22]], dtype=torch.int32)
+    kept = torch.tensor([[[[0, 1, 2, 3, 4, 5, 6, 7]],       # nothing evicted before row 8
+                          [[0, 2, 3, 5, 6, 8, 9, 11]]],     # shifts from row 1 on: 7 move
+                         ], dtype=torch.int32)
+    # request 0 compacts in place; request 1 into two fresh blocks: all 8 move
+    dst_in_place = src[:, :2].clone()
+    assert bench.count_moved(kept[:, :1], src[:1], dst_in_place[:1], wl) == 0
+    assert bench.count_moved(kept[:, 1:], src[1:], dst_in_place[1:], wl) == 7
+    fresh = torch.tensor([[10, 11], [30, 31]], dtype=torch.int32)
+    assert bench.count_moved(kept, src, fresh, wl) == 0 + 8
+    # a row kept at its position but in a different destination block moves
+    half = torch.tensor([[10, 99], [20, 21]], dtype=torch.int32)
+    assert bench.count_moved(kept[:, :1], src[:1], half[:1], wl) == 4
