@@ -1076,6 +1076,7 @@ def run_gpu(args, world, rank, local):
     res["clocks"] = clk.summary()
     if world == 1 and not args.no_cpu_baseline and not args.layers:
         res["cpu_baseline"] = cpu_baseline(wl, replica_seed(wl, rank), dev)
+        res["speedup_vs_oracle"] = res["value"] / res["cpu_baseline"]["value"]
     if world > 1:
         dist.destroy_process_group()
     return res
@@ -1241,6 +1242,7 @@ def cpu_baseline(wl, seed, device):
     v = toks / secs
     full_s = wl.R * wl.T / v
     return {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "units_per_s": units / secs, "full_step_s_extrapolated": full_s,
             "sample": f"{units} of {wl.units()} units of {wl.name} ({len(rows)} whole requests"
                       f"{' = 2 whole sharing groups' if wl.group > 1 and units < wl.units() else ''}"
                       f", {len(layers)} layers, compression + decode of the compacted requests),"
