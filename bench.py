@@ -1075,8 +1075,20 @@ def run_gpu(args, world, rank, local):
     }
     res["clocks"] = clk.summary()
     if world == 1 and not args.no_cpu_baseline and not args.layers:
-        res["cpu_baseline"] = cpu_baseline(wl, replica_seed(wl, rank), dev)
+        # one untimed call exactly as timed, from the pristine state, for the
+        # oracle's comparison on its sample
+        restore()
+        compress()
+        torch.cuda.synchronize()
+        assert cache.status() == zp.OK
+
+        def gpu_rows(r, l):
+            tab = st.block_tables[r, :wl.N - 1].long()
+            return W.bf16_bits(st.k_pools[l][tab]), W.bf16_bits(st.v_pools[l][tab])
+
+        res["cpu_baseline"] = cpu_baseline(wl, replica_seed(wl, rank), dev, gpu_rows)
         res["speedup_vs_oracle"] = res["value"] / res["cpu_baseline"]["value"]
+        res["parity"] = res["cpu_baseline"].pop("parity")
     if world > 1:
         dist.destroy_process_group()
     return res
@@ -1196,7 +1208,7 @@ def oracle_step(orc, wl, snap, nthreads):
     its compressing requests on its layers, then decode attention of the
     compacted requests on each of those layers.  Returns (seconds,
     request-tokens: compressing requests x T x the fraction of the model's
-    layers the snapshot holds)."""
+    layers the snapshot holds, the oracle's compacted state)."""
     layers = snap.get("layers", list(range(wl.L)))
     req = snap["compress_rows"] if (wl.mixed or "rows" in snap) else None
     t0 = time.perf_counter()
@@ -1214,7 +1226,7 @@ def oracle_step(orc, wl, snap, nthreads):
                                    1.0 / math.sqrt(wl.d))
         assert st == 0
     secs = time.perf_counter() - t0
-    return secs, len(rows) * wl.T * len(layers) / wl.L
+    return secs, len(rows) * wl.T * len(layers) / wl.L, res
 
 
 def _oracle_q(wl, n):
@@ -1229,7 +1241,32 @@ def _gen_device():
     return "cuda" if torch.cuda.is_available() else "cpu"
 
 
-def cpu_baseline(wl, seed, device):
+def compacted_parity(wl, snap, res, gpu_rows, check_layers):
+    """Compares, unit by unit, the compacted K and V rows of the oracle's run on
+    a sample (`res`, its tables over the sample's renumbered blocks) with the
+    GPU's (`gpu_rows(row, layer)` -> ([N-1][Hkv][b][d], same for V) as uint16,
+    through the GPU's own tables).  Returns the counts of units compared and of
+    units whose rows are byte-identical (a unit that differs is a near-tie or
+    a fault: the parity tests decide which)."""
+    import numpy as np
+    rows = snap["rows"]
+    layers = snap["layers"]
+    n, same = 0, 0
+    for l in check_layers:
+        li = layers.index(l)
+        for i in snap["compress_rows"]:
+            tab = res["tables"][i][:wl.N - 1]
+            ko, vo = res["kpools"][li][tab], res["vpools"][li][tab]
+            kg, vg = gpu_rows(rows[i], l)
+            for h in range(wl.Hkv):
+                n += 1
+                same += bool(np.array_equal(ko[:, h], kg[:, h]) and np.array_equal(vo[:, h], vg[:, h]))
+    return {"units": n, "byte_identical": same, "layers": list(check_layers),
+            "what": "compacted K/V rows of the sampled units, the bench's own call (no debug "
+                    "outputs) against the oracle on the same inputs"}
+
+
+def cpu_baseline(wl, seed, device, gpu_rows=None):
     import oracle
     from compressed_paged_kv_gb300 import workloads as W
     orc = oracle.load()
@@ -1237,12 +1274,16 @@ def cpu_baseline(wl, seed, device):
     rows, layers = baseline_sample(wl)
     snap = W.sample_snapshot(wl, rows, layers, device=device, seed=seed,
                              spare=len(rows) * (wl.prefix_blocks + 2))
-    secs, toks = oracle_step(orc, wl, snap, cores)
+    secs, toks, ores = oracle_step(orc, wl, snap, cores)
+    parity = None
+    if gpu_rows is not None:
+        check = sorted({layers[0], layers[len(layers) // 2], layers[-1]})
+        parity = compacted_parity(wl, snap, ores, gpu_rows, check)
     units = len(snap["compress_rows"]) * len(layers) * wl.Hkv
     v = toks / secs
     full_s = wl.R * wl.T / v
     return {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "units_per_s": units / secs, "full_step_s_extrapolated": full_s,
+            "units_per_s": units / secs, "full_step_s_extrapolated": full_s, "parity": parity,
             "sample": f"{units} of {wl.units()} units of {wl.name} ({len(rows)} whole requests"
                       f"{' = 2 whole sharing groups' if wl.group > 1 and units < wl.units() else ''}"
                       f", {len(layers)} layers, compression + decode of the compacted requests),"
@@ -1294,7 +1335,7 @@ def run_reference(args, world, rank):
     secs, toks, units = 0.0, 0.0, 0
     for i in range(args.steps):
         snap = sample(args.warmup + i)
-        s_, t_ = oracle_step(orc, wl, snap, cores)
+        s_, t_, _ = oracle_step(orc, wl, snap, cores)
         secs += s_
         toks += t_
         units += len(snap["compress_rows"]) * len(snap["layers"]) * wl.Hkv

@@ -99,3 +99,43 @@ def test_moved_rows_count_of_the_algorithmic_bytes():
     # a row kept at its position but in a different destination block moves
     half = torch.tensor([[10, 99], [20, 21]], dtype=torch.int32)
     assert bench.count_moved(kept[:, :1], src[:1], half[:1], wl) == 4
+
+
+def test_bench_parity_leg_matches_units_through_both_tables():
+    """The bench's parity leg compares the oracle's compaction of a sampled
+    snapshot (blocks renumbered) with a compaction of the full cache through
+    that cache's own tables.  Here both sides are the oracle, so every unit
+    must be byte-identical; a corrupted row must be counted as different."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    from compressed_paged_kv_gb300 import workloads as W
+    orc = oracle.load()
+    wl = W.scaled(W.WORKLOADS["qwen3_36l"], name="parity_leg", L=2, R=8, group=4,
+                  prefix_blocks=2, N=6, spare_blocks=24)
+    st = W.build_cache(wl, "cpu")
+    full = W.snapshot(st)
+    fres = orc.compress(full["k_pools"], full["v_pools"], full["block_tables"], full["lengths"],
+                        full["window_q"], wl.N, wl.w, wl.lam, full["free_ids"], full["free_count"],
+                        full["refcount"], Hq=wl.Hq, want_scores=False, want_kept=False)
+    assert fres["status"] == 0
+
+    def rows_of(r, l):
+        tab = fres["tables"][r, :wl.N - 1]
+        return fres["kpools"][l][tab], fres["vpools"][l][tab]
+
+    snap = W.sample_snapshot(wl, [0, 1, 2, 3], [0, 1], device="cpu", spare=16)
+    _, _, sres = bench.oracle_step(orc, wl, snap, 2)
+    par = bench.compacted_parity(wl, snap, sres, rows_of, [0, 1])
+    assert par["units"] == 4 * 2 * wl.Hkv and par["byte_identical"] == par["units"]
+
+    def corrupted(r, l):
+        k, v = rows_of(r, l)
+        k = k.copy()
+        if r == 2 and l == 1:
+            k[3, 1, 5, 0] ^= np.uint16(1)
+        return k, v
+
+    par = bench.compacted_parity(wl, snap, sres, corrupted, [0, 1])
+    assert par["byte_identical"] == par["units"] - 1
