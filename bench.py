@@ -11,8 +11,10 @@ blocks), K AR(1) rho 0.9 with 1% heavy hitters.
 
 Before each step (outside the timed events) the KV pools, block tables,
 lengths, refcounts and free stack are restored from a pristine device copy and
-a 256 MiB buffer is written to flush L2, so every step compresses the
-workload's own data from HBM.
+a 256 MiB buffer is written and another read to flush L2, so every step
+compresses the workload's own data from HBM (the read leaves L2 holding clean
+lines: the write-back of the written buffer's lines is not timed as part of
+the step).
 
 `--impl reference` times the CPU oracle (plain fp64 C, all host cores) on
 bounded slices of the same workload instead (the same config, steps and
@@ -40,6 +42,22 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+class L2Flush:
+    """Evicts the workload's data from L2 between steps: a buffer twice its
+    size is written, then another one read, so L2 ends up holding clean lines
+    of the second (nothing of the flush is written back inside the next timed
+    region)."""
+
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.torch.sum(self.r)
 
 
 def parse_args():
@@ -243,7 +261,7 @@ def run_mixed(args, world, rank, local):
     scale = 1.0 / math.sqrt(wl.d)
     live = [st.block_tables, st.lengths, st.refcount, st.free_ids, st.free_count]
     pristine = [t.clone() for t in live]
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     drows = st.decode_rows
     q = [st.decode_q[l][drows.long()].contiguous() for l in range(wl.L)]
     out = [torch.empty_like(x) for x in q]
@@ -286,7 +304,7 @@ def run_mixed(args, world, rank, local):
 
     def step(overlap):
         restore()
-        flush.zero_()
+        flush()
         t = {k: ev() for k in ("e0", "ea", "d0", "d1", "c0", "c1", "e1")}
         t["e0"].record(main)
         # slot reservation and compression both update the free stack and the
@@ -384,7 +402,7 @@ def run_mixed(args, world, rank, local):
     e2e = []
     for i in range(E + 2):
         restore()
-        flush.zero_()
+        flush()
         a0, a1 = ev(), ev()
         a0.record(main)
         st.window_q.copy_(h_wq, non_blocking=True)
@@ -502,7 +520,7 @@ def run_mixed(args, world, rank, local):
                                f"{Rc} requests at N_max={wl.N} compressing on a second stream",
                    "global_batch": world * wl.R, "seq_len": wl.T,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "flushed between steps (256 MiB write) after restoring the "
+                   "l2": "flushed between steps (256 MiB write, then 256 MiB read) after restoring the "
                          "compressed blocks"},
         "overlap_ms": ov, "serial_ms": se, "overlap_gain": se / ov,
         "slot_reservation_ms": slot_ms, "decode_ms": dec_ms, "compress_ms": cmp_ms,
@@ -659,7 +677,7 @@ def run_prefill(args, world, rank, local):
     pristine_pools = [t.clone() for t in pools]
     ws = torch.empty(cache.prefill_workspace_bytes(P["R"], c["stride"]), dtype=torch.uint8,
                      device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     units = P["R"] * P["L"] * P["Hkv"]
     KT = (P["N"] - 1) * 16
     kept = torch.empty(P["L"], P["R"], P["Hkv"], KT, dtype=torch.int32, device=dev)
@@ -676,7 +694,7 @@ def run_prefill(args, world, rank, local):
 
     for _ in range(args.warmup):
         restore()
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     assert cache.status() == zp.OK
@@ -688,7 +706,7 @@ def run_prefill(args, world, rank, local):
     with ClockSampler(device_index(torch)) as clk:
         for e0, e1 in evs:
             restore()
-            flush.zero_()
+            flush()
             e0.record()
             step()
             e1.record()
@@ -731,7 +749,7 @@ def run_prefill(args, world, rank, local):
                                f"N_max={P['N']} blocks (2032 tokens + reserved block)",
                    "global_batch": world * P["R"], "seq_len": max(lens),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "flushed between steps"},
+                   "l2": "flushed between steps (256 MiB write, then 256 MiB read)"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                      "frac": gbs / peak, "traffic": None, "peak_source": peak_src},
         "algorithmic_bytes": alg, "moved_rows": moved, "units": units,
@@ -836,7 +854,7 @@ def run_gpu(args, world, rank, local):
     live = [st.block_tables, st.lengths, st.refcount, st.free_ids, st.free_count]
     pristine_pools = [t.clone() for t in st.k_pools + st.v_pools]
     live_pools = st.k_pools + st.v_pools
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     q = [st.decode_q[l][dec_rows.long()].contiguous() for l in range(wl.L)]
     out = [torch.empty_like(x) for x in q]
 
@@ -860,7 +878,7 @@ def run_gpu(args, world, rank, local):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     for _ in range(Wm):
         restore()
-        flush.zero_()
+        flush()
         compress()
         decode()
     torch.cuda.synchronize()
@@ -873,7 +891,7 @@ def run_gpu(args, world, rank, local):
         t_wall0 = time.perf_counter()
         for i in range(K):
             restore()
-            flush.zero_()
+            flush()
             ev[i][0].record()
             compress()
             ev[i][1].record()
@@ -890,6 +908,20 @@ def run_gpu(args, world, rank, local):
     step_ms = sum(c + d for c, d in zip(comp_ms, dec_ms)) / K
     comp_avg = sum(comp_ms) / K
     dec_avg = sum(dec_ms) / K
+
+    # the attention alone, after a flush that leaves L2 clean: inside the step
+    # its interval also carries the write-back of the compression's last dirty
+    # L2 lines (up to the L2's size), which belongs to the step, not to decode
+    dec_alone = []
+    for i in range(K + 3):
+        flush()
+        ev[0][0].record()
+        decode()
+        ev[0][1].record()
+        ev[0][1].synchronize()
+        if i >= 3:
+            dec_alone.append(ev[0][0].elapsed_time(ev[0][1]))
+    dec_alone_ms = sum(dec_alone) / len(dec_alone)
 
     # moved rows of a step (from the kept indices), for the algorithmic bytes
     restore()
@@ -924,7 +956,7 @@ def run_gpu(args, world, rank, local):
     e2e_ms_total = 0.0
     for i in range(E + 3):
         restore()
-        flush.zero_()
+        flush()
         e0.record()
         st.window_q.copy_(h_wq, non_blocking=True)
         for a, b in zip(live, h_state):
@@ -960,7 +992,7 @@ def run_gpu(args, world, rank, local):
         red_all = torch.empty((wl.L, Rc, wl.Hkv, st.block_tables.shape[1] * wl.b), device=dev)
         abl = []
         for i in range(6):
-            flush.zero_()
+            flush()
             e0.record()
             cache.global_redundancy(st.block_tables, st.lengths, red_all, req_idx=req_idx, R=Rc)
             e1.record()
@@ -972,7 +1004,7 @@ def run_gpu(args, world, rank, local):
         # tensor cores (the cost of the original method)
         gram = []
         for i in range(6):
-            flush.zero_()
+            flush()
             e0.record()
             cache.global_redundancy(st.block_tables, st.lengths, red_all, req_idx=req_idx, R=Rc,
                                     gram=True)
@@ -985,8 +1017,9 @@ def run_gpu(args, world, rank, local):
         del red_all
 
     # max over ranks
-    step_ms, comp_avg, dec_avg, e2e_ms, e2e_serial_ms, t_wall, abl_ms, gram_ms = reduce_max(
-        [step_ms, comp_avg, dec_avg, e2e_ms, e2e_serial_ms, t_wall, abl_ms, gram_ms], world, dev)
+    (step_ms, comp_avg, dec_avg, e2e_ms, e2e_serial_ms, t_wall, abl_ms, gram_ms,
+     dec_alone_ms) = reduce_max([step_ms, comp_avg, dec_avg, e2e_ms, e2e_serial_ms, t_wall, abl_ms,
+                                 gram_ms, dec_alone_ms], world, dev)
 
     if rank != 0:
         if world > 1:
@@ -1049,7 +1082,14 @@ def run_gpu(args, world, rank, local):
                             "bound": "hbm", "achieved": dec_gbs, "peak": peak, "unit": "GB/s",
                             "frac": dec_gbs / peak, "bytes_per_step": dec_bytes,
                             "what": "every cached K and V row of the compacted requests, "
-                                    "plus q and out"},
+                                    "plus q and out",
+                            "alone": {"ms": dec_alone_ms,
+                                      "achieved": dec_bytes / (dec_alone_ms * 1e-3) / 1e9,
+                                      "frac": dec_bytes / (dec_alone_ms * 1e-3) / 1e9 / peak,
+                                      "what": "the same calls timed alone after an L2 flush that "
+                                              "leaves L2 clean (in the step, the decode "
+                                              "interval also carries the write-back of the "
+                                              "compression's dirty L2 lines)"}},
         "e2e": {"value": world * req_tokens / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": e2e_ms,
@@ -1305,7 +1345,7 @@ def bench_config(wl, Rc, world, layers=None):
         "global_batch": world * Rc,
         "seq_len": wl.T,
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-        "l2": "flushed between steps (256 MiB write) after restoring the pools",
+        "l2": "flushed between steps (256 MiB write, then 256 MiB read) after restoring the pools",
         "step": "zp_compress (all layers/heads) + zp_paged_decode_attn per layer",
     }
 
