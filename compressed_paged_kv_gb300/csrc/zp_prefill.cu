@@ -142,8 +142,11 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
     uint64_t *bar = bars + wi * kPStages;
     const int32_t *trow = a.tables + (size_t)row * a.stride;
     const CUtensorMap *kmap = a.kmaps + l;
-    auto issue = [&](int i) {
-        const int blk = trow[t0 / kBlk + wi + i * kPW];  // checked by the plan
+    // the block ids of this warp's blocks, one per lane, read once (the TMA
+    // issue of every block then waits on no global load)
+    static_assert(kPBlocks / kPW <= 32, "one block id per lane");
+    const int my_blk = lane < my_n ? trow[t0 / kBlk + wi + lane * kPW] : 0;  // checked by the plan
+    auto issue = [&](int i, int blk) {
         const int s = i % kPStages;
         mbar_arrive_expect_tx(&bar[s], SLAB);
         const int y = (blk * a.Hkv + h) * kBlk;
@@ -151,9 +154,12 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
         for (int hf = 0; hf < HALVES; ++hf)
             tma_load_2d(ring + s * SLAB + hf * kBlk * 128, kmap, hf * 64, y, &bar[s]);
     };
-    if (lane == 0)
-        for (int i = 0; i < my_n && i < kPStages; ++i)
-            issue(i);
+#pragma unroll
+    for (int i = 0; i < kPStages; ++i) {
+        const int blk = __shfl_sync(0xffffffffu, my_blk, i);
+        if (lane == 0 && i < my_n)
+            issue(i, blk);
+    }
 
     int slot_of[MT][2];
 #pragma unroll
@@ -174,9 +180,29 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
     const size_t ubase = (size_t)u * a.T_cap;
     const uint32_t qb = smem_u32(sQ);
     bool ok = true;
+    // scoring: the merged statistics of this thread's rows in registers, and
+    // the redundancy of each block's keys (lane j: slot j) read one block ahead
+    float gm[MT][2], ginv[MT][2];
+    float red_cur = 0.f;
+    auto red_of = [&](int i) {
+        const int key = t0 + (wi + i * kPW) * kBlk + (lane & 15);
+        return lane < kBlk && i < my_n && key < C ? a.red[ubase + key] : 0.f;
+    };
+    if (SCORE) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int rr = mt * 16 + (lane >> 2) + hh * 8;
+                gm[mt][hh] = sGm[rr];
+                ginv[mt][hh] = sGinv[rr];
+            }
+        red_cur = red_of(0);
+    }
 
     for (int i = 0; i < my_n; ++i) {
         const int s = i % kPStages;
+        const float red_nxt = SCORE ? red_of(i + 1) : 0.f;
         ok &= mbar_wait(&bar[s], (i / kPStages) & 1);
         const int key0 = t0 + (wi + i * kPW) * kBlk;  // token of the block's slot 0
         const uint32_t kb = smem_u32(ring + s * SLAB);
@@ -211,9 +237,12 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
             }
         }
         __syncwarp();
-        if (lane == 0 && i + kPStages < my_n) {
-            fence_proxy_async_smem();
-            issue(i + kPStages);
+        {
+            const int blk = __shfl_sync(0xffffffffu, my_blk, (i + kPStages) & 31);
+            if (lane == 0 && i + kPStages < my_n) {
+                fence_proxy_async_smem();
+                issue(i + kPStages, blk);
+            }
         }
         // base-2 logits; window row of slot i sees keys up to C + i, which
         // also hides the unfilled slots of a partial last block (only blocks
@@ -302,19 +331,18 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int rr = mt * 16 + (lane >> 2) + hh * 8;
-                            v += ex2_approx(acc[mt][nt][hh * 2 + ee] - sGm[rr]) * sGinv[rr];
-                        }
+                        for (int hh = 0; hh < 2; ++hh)
+                            v += ex2_approx(acc[mt][nt][hh * 2 + ee] - gm[mt][hh]) * ginv[mt][hh];
                     v += __shfl_xor_sync(0xffffffffu, v, 4);
                     v += __shfl_xor_sync(0xffffffffu, v, 8);
                     v += __shfl_xor_sync(0xffffffffu, v, 16);
+                    const float rd = __shfl_sync(0xffffffffu, red_cur, nt * 8 + (lane & 3) * 2 + ee);
                     const int key = key0 + nt * 8 + lane * 2 + ee;
                     if (lane < 4 && key < T)
-                        a.scores[ubase + key] =
-                            key < C ? v * a.inv_rows - a.lambda * a.red[ubase + key] : INFINITY;
+                        a.scores[ubase + key] = key < C ? v * a.inv_rows - a.lambda * rd : INFINITY;
                 }
         }
+        red_cur = red_nxt;
     }
     if (!ok && lane == 0)
         set_error(a.sticky, ZP_ERR_TIMEOUT);
