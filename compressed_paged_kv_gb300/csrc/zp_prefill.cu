@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
         }
     const size_t ubase = (size_t)u * a.T_cap;
     const uint32_t qb = smem_u32(sQ);
+    const float ls = a.logit_scale;  // base-2 logit scale
     bool ok = true;
     // scoring: the merged statistics of this thread's rows in registers, and
     // the redundancy of each block's keys (lane j: slot j) read one block ahead
@@ -244,25 +245,23 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
                 issue(i + kPStages, blk);
             }
         }
-        // base-2 logits; window row of slot i sees keys up to C + i, which
-        // also hides the unfilled slots of a partial last block (only blocks
-        // reaching past C hold such keys)
-        const bool masked_block = key0 + kBlk - 1 > C;
+        // window row of slot i sees keys up to C + i, which also hides the
+        // unfilled slots of a partial last block (only blocks reaching past C
+        // hold such keys); the logits stay unscaled here, the base-2 scale
+        // enters each exponent below
+        if (key0 + kBlk - 1 > C) {
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+                for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float v = acc[mt][nt][e] * a.logit_scale;
-                    if (masked_block) {
+                    for (int e = 0; e < 4; ++e) {
                         const int slot = slot_of[mt][e >> 1];
                         const int tok = key0 + nt * 8 + (lane & 3) * 2 + (e & 1);
                         if (slot >= 0 ? tok > C + slot : tok >= T)
-                            v = -INFINITY;
+                            acc[mt][nt][e] = -INFINITY;
                     }
-                    acc[mt][nt][e] = v;
-                }
+        }
 
         if (!SCORE) {
 #pragma unroll
@@ -272,15 +271,14 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
                     const float bm = fmaxf(fmaxf(acc[mt][0][hh * 2], acc[mt][0][hh * 2 + 1]),
                                            fmaxf(acc[mt][1][hh * 2], acc[mt][1][hh * 2 + 1]));
                     const float m_new = fmaxf(rm[mt][hh], bm);
-                    if (m_new == -INFINITY)
-                        continue;
-                    float sum = rm[mt][hh] == -INFINITY
-                                    ? 0.f
-                                    : rsum[mt][hh] * ex2_approx(rm[mt][hh] - m_new);
+                    // no branch: while every key so far is masked, any finite
+                    // reference gives exp2(-inf) = 0 for all of them
+                    const float mref = m_new == -INFINITY ? 0.f : m_new * ls;
+                    float sum = rsum[mt][hh] * ex2_approx(fmaf(rm[mt][hh], ls, -mref));
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
-                        sum += ex2_approx(acc[mt][nt][hh * 2] - m_new) +
-                               ex2_approx(acc[mt][nt][hh * 2 + 1] - m_new);
+                        sum += ex2_approx(fmaf(acc[mt][nt][hh * 2], ls, -mref)) +
+                               ex2_approx(fmaf(acc[mt][nt][hh * 2 + 1], ls, -mref));
                     rm[mt][hh] = m_new;
                     rsum[mt][hh] = sum;
                 }
@@ -299,10 +297,11 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
             __syncwarp();
             if (lane < kBlk) {
                 const float dj = inv[lane];
-                inv[lane] = lane < f && dj > 0.f ? 1.0f / sqrtf(dj) : 0.f;
+                inv[lane] = lane < f && dj > 0.f ? rsqrtf(dj) : 0.f;
             }
             __syncwarp();
             float rs[2] = {0.f, 0.f};
+            const float rf1 = f > 1 ? __frcp_rn(static_cast<float>(f - 1)) : 0.f;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -318,7 +317,7 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
                 v += __shfl_xor_sync(0xffffffffu, v, 2);
                 const int j = (lane >> 2) + hh * 8;
                 if ((lane & 3) == 0 && j < f)
-                    a.red[ubase + key0 + j] = f > 1 ? inv[j] * v / static_cast<float>(f - 1) : 0.f;
+                    a.red[ubase + key0 + j] = inv[j] * v * rf1;
             }
             __syncwarp();
         } else {
@@ -332,7 +331,7 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
                     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh)
-                            v += ex2_approx(acc[mt][nt][hh * 2 + ee] - gm[mt][hh]) * ginv[mt][hh];
+                            v += ex2_approx(fmaf(acc[mt][nt][hh * 2 + ee], ls, -gm[mt][hh])) * ginv[mt][hh];
                     v += __shfl_xor_sync(0xffffffffu, v, 4);
                     v += __shfl_xor_sync(0xffffffffu, v, 8);
                     v += __shfl_xor_sync(0xffffffffu, v, 16);
@@ -353,7 +352,7 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                float m = rm[mt][hh], s = rsum[mt][hh];
+                float m = rm[mt][hh] * ls, s = rsum[mt][hh];
 #pragma unroll
                 for (int o = 1; o <= 2; o <<= 1) {
                     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
