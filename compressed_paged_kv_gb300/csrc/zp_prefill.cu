@@ -105,38 +105,15 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::off_bar);
     const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5, mi = lane >> 3;
 
-    // window queries -> shared memory (swizzled, rows past w*G zero)
-    {
-        const __nv_bfloat16 *qsrc =
-            a.window_q + ((((size_t)l * a.R + r) * a.Hq + (size_t)h * G) * a.w) * D;
-        const uint32_t qb = smem_u32(sQ);
-        for (int c = tid; c < ROWS * CPR; c += kPThreads) {
-            const int rr = c / CPR, ch = c - rr * CPR;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (rr < a.rows)
-                v = ld_global_nc_v4(qsrc + (size_t)rr * D + ch * 8);
-            st_shared_v4(qb + swz(rr, ch, ROWS), v);
-        }
-    }
     if (tid < kPW * kPStages)
         mbar_init(&bars[tid], 1);
     if (tid == 0)
         fence_mbar_init();
-    if (SCORE && tid < ROWS) {
-        // statistics of all keys of the unit: merge the chunks
-        const int nc = (T + kPChunk - 1) / kPChunk;
-        const float2 *st = a.stats + (size_t)u * a.NC * kMaxRows + tid;
-        float m = -INFINITY, s = 0.f;
-        for (int c = 0; c < nc; ++c) {
-            const float2 v = st[(size_t)c * kMaxRows];
-            stat_merge(m, s, v.x, v.y);
-        }
-        sGm[tid] = m;
-        sGinv[tid] = tid < a.rows && s > 0.f ? 1.0f / s : 0.f;
-    }
     __syncthreads();
 
-    // this warp's blocks of the chunk: wi, wi + kPW, ...
+    // this warp's blocks of the chunk: wi, wi + kPW, ...; the first loads are
+    // issued before anything else, so the queries and statistics below are
+    // read while they are in flight
     const int my_n = wi < nblk ? (nblk - wi + kPW - 1) / kPW : 0;
     uint8_t *ring = sm + S::off_ring + wi * kPStages * SLAB;
     uint64_t *bar = bars + wi * kPStages;
@@ -160,6 +137,39 @@ __global__ void __launch_bounds__(kPThreads) zp_prefill_pass_kernel(const Prefil
         if (lane == 0 && i < my_n)
             issue(i, blk);
     }
+
+    // window queries -> shared memory (swizzled, rows past w*G zero)
+    {
+        const __nv_bfloat16 *qsrc =
+            a.window_q + ((((size_t)l * a.R + r) * a.Hq + (size_t)h * G) * a.w) * D;
+        const uint32_t qb = smem_u32(sQ);
+        for (int c = tid; c < ROWS * CPR; c += kPThreads) {
+            const int rr = c / CPR, ch = c - rr * CPR;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (rr < a.rows)
+                v = ld_global_nc_v4(qsrc + (size_t)rr * D + ch * 8);
+            st_shared_v4(qb + swz(rr, ch, ROWS), v);
+        }
+    }
+    if (SCORE && tid < ROWS) {
+        // statistics of all keys of the unit: merge the chunks (their loads
+        // four at a time, independent of one another)
+        const int nc = (T + kPChunk - 1) / kPChunk;
+        const float2 *st = a.stats + (size_t)u * a.NC * kMaxRows + tid;
+        float m = -INFINITY, s = 0.f;
+        for (int c0 = 0; c0 < nc; c0 += 4) {
+            float2 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                v[k] = c0 + k < nc ? st[(size_t)(c0 + k) * kMaxRows] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                stat_merge(m, s, v[k].x, v[k].y);
+        }
+        sGm[tid] = m;
+        sGinv[tid] = tid < a.rows && s > 0.f ? 1.0f / s : 0.f;
+    }
+    __syncthreads();
 
     int slot_of[MT][2];
 #pragma unroll
