@@ -1095,8 +1095,10 @@ def run_gpu(args, world, rank, local):
                 "ms_per_step": e2e_ms,
                 "how": "C ABI calls; each step's inputs (window and decode queries, block state) "
                        "cross from pinned host memory on a copy stream into one of two device "
-                       "buffer sets while the previous step computes, each step's outputs "
-                       "(attention, tables, lengths) cross back; the KV pools stay resident",
+                       "buffer sets while the previous step computes, and each step's outputs "
+                       "(attention, tables, lengths) cross back on it while the next step "
+                       "computes; every copy inside the timed region; the KV pools stay "
+                       "resident",
                 "serial_ms_per_step": e2e_serial_ms,
                 "serial_value": world * req_tokens / (e2e_serial_ms * 1e-3)},
         "gpu_launches": K * (3 + wl.L * (1 if cache_splits_one(wl, Rc, cache) else 2)),
@@ -1136,22 +1138,30 @@ def run_gpu(args, world, rank, local):
 
 def pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_state, h_out, h_tab,
                   h_len, req_idx, dec_rows, scale, E):
-    """Steps through the C ABI with double-buffered host inputs: the copy
-    stream brings step i+1's inputs into one device buffer set while the
-    compute stream runs step i on the other; ms per step over E timed steps
-    (after 2 warm-up steps; the first timed step's inputs are not overlapped)."""
+    """Steps through the C ABI as a serving loop runs them: a copy stream
+    brings step i+1's inputs into one of two device buffer sets while the
+    compute stream runs step i on the other, and takes step i's results (its
+    attention outputs, block tables and lengths, snapshotted on the compute
+    stream) back to the host while step i+1 computes.  ms per step over E
+    timed steps (after 2 warm-up steps; the first timed step's inputs and the
+    last one's results are not overlapped, and every copy is inside the timed
+    region)."""
     comp = torch.cuda.current_stream()
     cp = torch.cuda.Stream()
     d_wq = [torch.empty_like(st.window_q) for _ in range(2)]
     d_q = [[torch.empty_like(x) for x in q] for _ in range(2)]
     d_state = [[torch.empty_like(t) for t in pristine] for _ in range(2)]
-    ready = [torch.cuda.Event() for _ in range(2)]
-    free = [torch.cuda.Event() for _ in range(2)]
+    d_out = [out, [torch.empty_like(x) for x in out]]
+    d_tab = [torch.empty_like(st.block_tables) for _ in range(2)]
+    d_len = [torch.empty_like(st.lengths) for _ in range(2)]
+    ready = [torch.cuda.Event() for _ in range(2)]   # inputs of set b landed
+    done = [torch.cuda.Event() for _ in range(2)]    # step on set b computed
+    back = [torch.cuda.Event() for _ in range(2)]    # results of set b on the host
 
     def bring(i):
         b = i % 2
         if i >= 2:
-            cp.wait_event(free[b])
+            cp.wait_event(done[b])
         with torch.cuda.stream(cp):
             d_wq[b].copy_(h_wq, non_blocking=True)
             for x, h in zip(d_q[b], h_q):
@@ -1163,18 +1173,28 @@ def pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_sta
     def run(i):
         b = i % 2
         comp.wait_event(ready[b])
+        if i >= 2:
+            comp.wait_event(back[b])  # set b's previous results have left
         for x, y in zip(live, d_state[b]):
             x.copy_(y, non_blocking=True)
         cache.compress(st.block_tables, st.lengths, d_wq[b], wl.N, wl.w, wl.lam, st.free_ids,
                        st.free_count, st.refcount, req_idx=req_idx)
         for l in range(wl.L):
-            cache.decode(l, d_q[b][l], st.block_tables, st.lengths, scale, out[l],
+            cache.decode(l, d_q[b][l], st.block_tables, st.lengths, scale, d_out[b][l],
                          req_idx=dec_rows)
-        for h, x in zip(h_out, out):
-            h.copy_(x, non_blocking=True)
-        h_tab.copy_(st.block_tables, non_blocking=True)
-        h_len.copy_(st.lengths, non_blocking=True)
-        free[b].record(comp)
+        d_tab[b].copy_(st.block_tables, non_blocking=True)
+        d_len[b].copy_(st.lengths, non_blocking=True)
+        done[b].record(comp)
+
+    def take(i):
+        b = i % 2
+        cp.wait_event(done[b])
+        with torch.cuda.stream(cp):
+            for h, x in zip(h_out, d_out[b]):
+                h.copy_(x, non_blocking=True)
+            h_tab.copy_(d_tab[b], non_blocking=True)
+            h_len.copy_(d_len[b], non_blocking=True)
+        back[b].record(cp)
 
     def loop(steps):
         bring(0)
@@ -1182,6 +1202,7 @@ def pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_sta
             if i + 1 < steps:
                 bring(i + 1)
             run(i)
+            take(i)
 
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -1190,6 +1211,7 @@ def pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_sta
     t0.record(comp)
     cp.wait_event(t0)  # the first step's inputs too cross inside the timed region
     loop(E)
+    comp.wait_stream(cp)  # the last step's results have reached the host
     t1.record(comp)
     t1.synchronize()
     return t0.elapsed_time(t1) / E
