@@ -40,7 +40,8 @@ constexpr int kPThreads = kPW * 32;
 constexpr int kPStages = 2;                  // TMA stages per warp
 constexpr int kPChunk = kPrefillChunk;       // tokens per scoring CTA
 constexpr int kPBlocks = kPChunk / kBlk;
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 256;
+constexpr int kSelBins = 2048;                 // digits of the selection's widest pass
 constexpr int kCmpSeg = 2048;                // destination rows whose indices are staged at once
 
 template <int D, int MT>
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(kSelThreads) zp_prefill_select_kernel(const Pr
     if (*(volatile int32_t *)a.call != 0)
         return;
     extern __shared__ uint32_t sKey[];  // [T_cap] order images of the scores
-    __shared__ int hist[256];
+    __shared__ int hist[kSelBins];
     __shared__ int s_scan[kSelThreads / 32 + 1];
     __shared__ uint32_t s_prefix;
     __shared__ int s_need;
@@ -401,7 +402,7 @@ __global__ void __launch_bounds__(kSelThreads) zp_prefill_select_kernel(const Pr
     const int row = a.req_idx ? a.req_idx[r] : r;
     const int T = a.lengths[row];
     const int C = T - a.w;
-    const int KT = (a.N - 1) * kBlk, keep = KT - a.w;  // keep < C since T >= N*b
+    const int KT = (a.N - 1) * kBlk, keep = KT - a.w;  // 0 <= keep < C since T >= N*b
     const float *sc = a.scores + (size_t)u * a.T_cap;
     for (int j = tid; j < C; j += kSelThreads)
         sKey[j] = f32_order(sc[j]);
@@ -409,52 +410,44 @@ __global__ void __launch_bounds__(kSelThreads) zp_prefill_select_kernel(const Pr
         s_prefix = 0u;
         s_need = keep;
     }
-    __syncthreads();
 
-    // the keep-th largest order image, one 8-bit digit at a time from the top
+    // the keep-th largest order image, one digit at a time from the top:
+    // bits 31-21, 20-10, 9-0
     uint32_t mask = 0u;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += kSelThreads)
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
+        const int nb = pass == 2 ? 1024 : 2048;  // digits of this pass
+        for (int i = tid; i < nb; i += kSelThreads)
             hist[i] = 0;
         __syncthreads();
         const uint32_t prefix = s_prefix;
+        const int need = s_need;
         for (int j = tid; j < C; j += kSelThreads) {
             const uint32_t k = sKey[j];
             if ((k & mask) == prefix)
-                atomicAdd(&hist[(k >> shift) & 255u], 1);
+                atomicAdd(&hist[(k >> shift) & static_cast<uint32_t>(nb - 1)], 1);
         }
         __syncthreads();
-        if (tid < 32) {
-            // warp 0: the digit at which the count from the top reaches s_need
-            const int need = s_need;
-            int above = 0;  // keys with a larger digit, over the digits done
-            int digit = -1, before = 0;
-            for (int base = 255; base >= 0 && digit < 0; base -= 32) {
-                const int dg = base - tid;  // lane t takes digit base - t
-                const int c = hist[dg];
-                int incl = c;  // inclusive sum over lanes 0..t (larger digits first)
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (tid >= o)
-                        incl += y;
-                }
-                const unsigned hit = __ballot_sync(0xffffffffu, above + incl >= need);
-                if (hit) {
-                    const int t = __ffs(hit) - 1;
-                    const int excl = __shfl_sync(0xffffffffu, incl - c, t);
-                    digit = base - t;
-                    before = above + excl;
-                } else {
-                    above += __shfl_sync(0xffffffffu, incl, 31);
-                }
-            }
-            if (tid == 0) {
-                s_prefix = prefix | (static_cast<uint32_t>(digit) << shift);
-                s_need = need - before;
-            }
+        // thread t holds the digits hi, hi - 1, .., hi - bpt + 1 (larger
+        // digits at smaller t); the keys above its digits come from a scan
+        const int bpt = nb / kSelThreads;
+        const int hi = nb - 1 - tid * bpt;
+        int c = 0;
+        for (int i = 0; i < bpt; ++i)
+            c += hist[hi - i];
+        int total;
+        const int above = block_excl_scan<kSelThreads>(c, s_scan, total);
+        // the digit at which the count from the top reaches need (need <= 0
+        // only when nothing is kept: the top digit then, nothing above it)
+        if (need <= 0 ? tid == 0 : (above < need && need <= above + c)) {
+            int run = above, i = 0;
+            while (i < bpt - 1 && run + hist[hi - i] < need)
+                run += hist[hi - i++];
+            s_prefix = prefix | (static_cast<uint32_t>(hi - i) << shift);
+            s_need = need - run;
         }
-        mask |= 255u << shift;
+        mask |= static_cast<uint32_t>(nb - 1) << shift;
         __syncthreads();
     }
     const uint32_t thr = s_prefix;
