@@ -171,9 +171,12 @@ def test_prefill_parity(orc, case):
 
 @pytest.mark.parametrize("keys", ["equal", "zero", "eight_distinct"])
 def test_prefill_ties_keep_the_lower_indices(orc, keys):
-    """Scores that tie exactly (every key equal, every key zero, eight keys
-    repeated block after block): among equal scores the lower indices are kept,
-    so the kept sets must equal the oracle's exactly."""
+    """Tie-heavy scores.  Every key equal, or every key zero: all candidates
+    tie exactly on both sides, the lower indices are kept, and the kept sets
+    must equal the oracle's exactly.  Eight keys repeated block after block:
+    a key and its twin in the same block sum the same cosines in a different
+    order, so their scores differ by rounding on both sides and only the
+    near-tie rule applies."""
     c = W.prefill_cache(471, [1000, 2600, 333], 8, L=1, Hkv=2, device=DEV)
     k = c["k_pools"][0]
     if keys == "equal":
@@ -183,7 +186,7 @@ def test_prefill_ties_keep_the_lower_indices(orc, keys):
     else:
         base = k[:1, :, :8].clone()                # 8 key rows per kv head
         k.copy_(base.repeat(1, 1, 2, 1).expand_as(k))
-    check_prefill(orc, c, strict=True)
+    check_prefill(orc, c, strict=keys != "eight_distinct")
 
 
 def test_prefill_ignores_slots_past_the_length(orc):
