@@ -17,11 +17,13 @@
 //       every key (over the filled slots of its block) -> workspace.
 //   zp_prefill_pass_kernel<.., true>   same grid: the statistics of all
 //       chunks of the unit merged, logits again, importance and score.
-//   zp_prefill_select_kernel  one CTA per unit: radix select (four 8-bit
-//       digit passes over the order-preserving image of the fp32 scores held
-//       in shared memory) of the K_keep-th largest score; ties at the
-//       threshold go to the lower index; the kept positions in ascending
-//       order by block scans, then the window.
+//   zp_prefill_select_kernel  one CTA of 256 threads per unit: radix
+//       select (digit passes over bits 31-21, 20-10 and 9-0 of the
+//       order-preserving image of the fp32 scores held in shared memory,
+//       each digit found by a block-wide scan of the histogram) of the
+//       K_keep-th largest score; ties at the threshold go to the lower
+//       index; the kept positions in ascending order by block scans, then
+//       the window.
 //   zp_prefill_gather_kernel  one CTA per unit: the source pool row of every
 //       destination row resolved into shared memory, then the destination
 //       blocks in ascending order through a ring of shared-memory stages:
