@@ -418,6 +418,7 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
         const int mi = lane >> 3;
         const int grp = wi / kSGroupWarps, gw = wi % kSGroupWarps;  // group, warp in group
         const uint32_t qb_base = smem_u32(sQ);
+        const float ls = a.logit_scale;  // base-2 logit scale, applied in the exponents
         int slot_of[MT][2];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
@@ -428,7 +429,8 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
             }
 
         // logits of the window rows against the block of this warp in stage s
-        // (base 2, causal mask applied); optionally the block's Gram too
+        // (unscaled: the base-2 scale enters each exponent; causal mask
+        // applied); optionally the block's Gram too
         auto block_logits = [&](int s, int key0, float (&acc)[MT][2][4], float (&gram)[2][4],
                                 bool with_gram) {
 #pragma unroll
@@ -469,14 +471,12 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        float v = acc[mt][nt][e] * a.logit_scale;
                         if (masked_block) {
                             const int slot = slot_of[mt][e >> 1];
                             const int tok = t0 + key0 + nt * 8 + (lane & 3) * 2 + (e & 1);
                             if (slot >= 0 && tok > C + slot)
-                                v = -INFINITY;
+                                acc[mt][nt][e] = -INFINITY;
                         }
-                        acc[mt][nt][e] = v;
                     }
         };
 
@@ -507,14 +507,14 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                     const float bm = fmaxf(fmaxf(acc[mt][0][hh * 2], acc[mt][0][hh * 2 + 1]),
                                            fmaxf(acc[mt][1][hh * 2], acc[mt][1][hh * 2 + 1]));
                     const float m_new = fmaxf(rm[mt][hh], bm);
-                    if (m_new == -INFINITY)
-                        continue;
-                    float sum = rm[mt][hh] == -INFINITY ? 0.f
-                                                         : rsum[mt][hh] * ex2_approx(rm[mt][hh] - m_new);
+                    // no branch: while every key so far is masked, any finite
+                    // reference gives exp2(-inf) = 0 for all of them
+                    const float mref = m_new == -INFINITY ? 0.f : m_new * ls;
+                    float sum = rsum[mt][hh] * ex2_approx(fmaf(rm[mt][hh], ls, -mref));
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
-                        sum += ex2_approx(acc[mt][nt][hh * 2] - m_new) +
-                               ex2_approx(acc[mt][nt][hh * 2 + 1] - m_new);
+                        sum += ex2_approx(fmaf(acc[mt][nt][hh * 2], ls, -mref)) +
+                               ex2_approx(fmaf(acc[mt][nt][hh * 2 + 1], ls, -mref));
                     rm[mt][hh] = m_new;
                     rsum[mt][hh] = sum;
                 }
@@ -532,7 +532,7 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
             __syncwarp();
             if (lane < kBlk) {
                 const float dj = inv[lane];
-                inv[lane] = dj > 0.f ? 1.0f / sqrtf(dj) : 0.f;
+                inv[lane] = dj > 0.f ? rsqrtf(dj) : 0.f;
             }
             __syncwarp();
             float rs[2] = {0.f, 0.f};
@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                float m = rm[mt][hh], sum = rsum[mt][hh];
+                float m = rm[mt][hh] * ls, sum = rsum[mt][hh];
 #pragma unroll
                 for (int o = 1; o <= 2; o <<= 1) {
                     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(kSThreads, 2) zp_compress_stream_kernel(const 
                     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh)
-                            v += ex2_approx(acc[mt][nt][hh * 2 + ee] - gm[mt][hh]) * ginv[mt][hh];
+                            v += ex2_approx(fmaf(acc[mt][nt][hh * 2 + ee], ls, -gm[mt][hh])) * ginv[mt][hh];
                     v += __shfl_xor_sync(0xffffffffu, v, 4);
                     v += __shfl_xor_sync(0xffffffffu, v, 8);
                     v += __shfl_xor_sync(0xffffffffu, v, 16);
