@@ -137,5 +137,37 @@ def test_bench_parity_leg_matches_units_through_both_tables():
             k[3, 1, 5, 0] ^= np.uint16(1)
         return k, v
 
-    par = bench.compacted_parity(wl, snap, sres, corrupted, [0, 1])
+    par = bench.compacted_parity(wl, snap, sres, corrupted, [0, 1], orc)
     assert par["byte_identical"] == par["units"] - 1
+    assert par["near_ties"] == 0 and par["mismatches"] == 1
+
+
+def test_bench_parity_near_tie_rule():
+    """The bench's reading of a differing unit: the kept positions are read
+    back from the compacted rows, and the unit is a near-tie only when every
+    token in the symmetric difference scores within 1e-5 of the cut."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    rng = np.random.default_rng(5)
+    Ks = rng.integers(0, 1 << 16, (12, 4), dtype=np.uint16)
+    Vs = rng.integers(0, 1 << 16, (12, 4), dtype=np.uint16)
+    kept = np.array([0, 1, 3, 4, 6, 8, 9, 10, 11])
+    assert np.array_equal(bench.kept_of_rows(Ks, Vs, Ks[kept], Vs[kept]), kept)
+    Kg = Ks[kept].copy()
+    Kg[2, 1] ^= np.uint16(1)
+    assert bench.kept_of_rows(Ks, Vs, Kg, Vs[kept]) is None
+    # 10 candidates (w = 2), 3 evicted; the cut is the 3rd lowest score
+    s = np.array([0.5, 0.4, 0.1, 0.3, 0.9, 0.2, 0.8, 0.6, 0.7, 0.95])
+    imp, red = np.full(10, 0.1), np.full(12, 0.2)
+    s_tie = s.copy()
+    s_tie[3] = 0.3
+    s_tie[1] = 0.3 + 1e-9                                   # tokens 1 and 3 tie at the cut
+    # the oracle keeps 1 (higher), evicts 2, 5, 3; a GPU keeping 3 and evicting 1 differs
+    kept_o = np.array([0, 1, 4, 6, 7, 8, 9, 10, 11])
+    kept_g = np.array([0, 3, 4, 6, 7, 8, 9, 10, 11])
+    assert bench.near_tie(s_tie, imp, red, 0.5, kept_o, kept_g, 3)
+    s_far = s_tie.copy()
+    s_far[1] = 0.35                                         # far from the cut
+    assert not bench.near_tie(s_far, imp, red, 0.5, kept_o, kept_g, 3)
+    assert bench.near_tie(s_tie, imp, red, 0.5, kept_o, kept_o, 3)
