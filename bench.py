@@ -974,6 +974,18 @@ def run_gpu(args, world, rank, local):
         if i >= 3:
             e2e_ms_total += e0.elapsed_time(e1)
     e2e_serial_ms = e2e_ms_total / E
+    # the host link's rates on this machine (pinned buffers, one large copy each
+    # way: the window queries there and back, the same bytes), which set what
+    # the copies of a step cost
+    xfer = []
+    for src, dst in ((h_wq, st.window_q), (st.window_q, h_wq)):
+        dst.copy_(src, non_blocking=True)
+        e0.record()
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        xfer.append(3 * src.numel() * src.element_size() / (e0.elapsed_time(e1) * 1e-3) / 1e9)
     # (b) as a serving loop runs it: step i+1's inputs cross on a copy stream
     # into the other of two device buffer sets while step i computes; every
     # step's inputs and results still cross inside the timed region.  The
@@ -1100,7 +1112,10 @@ def run_gpu(args, world, rank, local):
                        "computes; every copy inside the timed region; the KV pools stay "
                        "resident",
                 "serial_ms_per_step": e2e_serial_ms,
-                "serial_value": world * req_tokens / (e2e_serial_ms * 1e-3)},
+                "serial_value": world * req_tokens / (e2e_serial_ms * 1e-3),
+                "host_link_gbs": {"h2d": xfer[0], "d2h": xfer[1],
+                                  "what": "pinned host <-> device copy rates measured beside "
+                                          "the e2e loop (one large copy each way)"}},
         "gpu_launches": K * (3 + wl.L * (1 if cache_splits_one(wl, Rc, cache) else 2)),
         "wall_s_timed_loop": t_wall,
         "ablation_all_keys_redundancy": None if args.no_ablations else {
