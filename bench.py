@@ -1155,9 +1155,11 @@ def pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_sta
                   h_len, req_idx, dec_rows, scale, E):
     """Steps through the C ABI as a serving loop runs them: a copy stream
     brings step i+1's inputs into one of two device buffer sets while the
-    compute stream runs step i on the other, and takes step i's results (its
-    attention outputs, block tables and lengths, snapshotted on the compute
-    stream) back to the host while step i+1 computes.  ms per step over E
+    compute stream runs step i's attention on the other (after its
+    compression, whose K re-reads through L2 the copies would churn), and
+    takes step i's results (its attention outputs, block tables and lengths,
+    snapshotted on the compute stream) back to the host while step i+1
+    computes.  ms per step over E
     timed steps (after 2 warm-up steps; the first timed step's inputs and the
     last one's results are not overlapped, and every copy is inside the timed
     region)."""
@@ -1172,11 +1174,16 @@ def pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_sta
     ready = [torch.cuda.Event() for _ in range(2)]   # inputs of set b landed
     done = [torch.cuda.Event() for _ in range(2)]    # step on set b computed
     back = [torch.cuda.Event() for _ in range(2)]    # results of set b on the host
+    cdone = [torch.cuda.Event() for _ in range(2)]   # compression of the step on set b done
 
     def bring(i):
         b = i % 2
         if i >= 2:
             cp.wait_event(done[b])
+        if i >= 1:
+            # the inputs cross while the previous step runs its attention: the
+            # compression re-reads K through L2, which the copies would churn
+            cp.wait_event(cdone[1 - b])
         with torch.cuda.stream(cp):
             d_wq[b].copy_(h_wq, non_blocking=True)
             for x, h in zip(d_q[b], h_q):
@@ -1194,6 +1201,7 @@ def pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_sta
             x.copy_(y, non_blocking=True)
         cache.compress(st.block_tables, st.lengths, d_wq[b], wl.N, wl.w, wl.lam, st.free_ids,
                        st.free_count, st.refcount, req_idx=req_idx)
+        cdone[b].record(comp)
         for l in range(wl.L):
             cache.decode(l, d_q[b][l], st.block_tables, st.lengths, scale, d_out[b][l],
                          req_idx=dec_rows)
@@ -1214,9 +1222,9 @@ def pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_sta
     def loop(steps):
         bring(0)
         for i in range(steps):
+            run(i)
             if i + 1 < steps:
                 bring(i + 1)
-            run(i)
             take(i)
 
     t0 = torch.cuda.Event(enable_timing=True)
