@@ -255,7 +255,10 @@ def run_mixed(args, world, rank, local):
     if args.layers:
         wl = W.scaled(wl, L=args.layers)
     seed = replica_seed(wl, rank)
-    st = W.build_cache(wl, dev, seed=seed)
+    # room for a fresh target block per block of every compressing request
+    # (the pipelined end-to-end loop below compresses into fresh targets)
+    st = W.build_cache(W.scaled(wl, spare_blocks=wl.spare_blocks + wl.mixed_compress * wl.N),
+                       dev, seed=seed)
     cache = zp.Cache(st.k_pools, st.v_pools, wl.Hq, max_requests=st.block_tables.shape[0],
                      max_blocks_per_req=st.block_tables.shape[1])
     scale = 1.0 / math.sqrt(wl.d)
@@ -434,12 +437,27 @@ def run_mixed(args, world, rank, local):
     # as a serving loop runs it: the next step's inputs cross on a copy stream
     # into the other of two device buffer sets while this step computes (the
     # pools stay resident: no restore between steps)
+    # Without a restore of the pools between its steps, each step would
+    # compress what the previous one compacted, the same window queries over
+    # data already thinned by them (the moved rows drift from ~1,900 to under
+    # 900 per unit).  So in the block state each step's inputs restore, every
+    # block of a compressing request is held twice (refcount 2): its
+    # compaction goes to fresh target blocks and leaves the sources as they
+    # were, and every step compresses the same data -- writing all (N_max-1)*b
+    # rows of a unit, more than the device-timed step's in-place compaction.
+    h_state_ft = [t.clone().pin_memory() for t in h_state]
+    crows_blk = pristine[0][st.compress_rows.long()].flatten().long()
+    h_state_ft[2][crows_blk.cpu()] += 1
     cp = torch.cuda.Stream(device=dev)
     d_wq = [torch.empty_like(st.window_q) for _ in range(2)]
     d_in = [[torch.empty_like(x) for x in q + k_new + v_new] for _ in range(2)]
     d_state = [[torch.empty_like(t) for t in pristine] for _ in range(2)]
-    ready = [torch.cuda.Event() for _ in range(2)]
-    free = [torch.cuda.Event() for _ in range(2)]
+    d_out = [out, [torch.empty_like(x) for x in out]]
+    d_tab = [torch.empty_like(st.block_tables) for _ in range(2)]
+    d_len = [torch.empty_like(st.lengths) for _ in range(2)]
+    ready = [torch.cuda.Event() for _ in range(2)]   # inputs of set b landed
+    free = [torch.cuda.Event() for _ in range(2)]    # step on set b computed
+    back = [torch.cuda.Event() for _ in range(2)]    # results of set b on the host
     L = wl.L
 
     def bring(i):
@@ -448,13 +466,15 @@ def run_mixed(args, world, rank, local):
             cp.wait_event(free[b])
         with torch.cuda.stream(cp):
             d_wq[b].copy_(h_wq, non_blocking=True)
-            for x, h in zip(d_in[b] + d_state[b], h_q + h_kv + h_state):
+            for x, h in zip(d_in[b] + d_state[b], h_q + h_kv + h_state_ft):
                 x.copy_(h, non_blocking=True)
         ready[b].record(cp)
 
     def run(i):
         b = i % 2
         main.wait_event(ready[b])
+        if i >= 2:
+            main.wait_event(back[b])  # set b's previous results have left
         for x, y in zip(live, d_state[b]):
             x.copy_(y, non_blocking=True)
         append_slots(main)
@@ -466,8 +486,8 @@ def run_mixed(args, world, rank, local):
         for l in range(L):
             cache.append_kv(l, dk[l], dv[l], st.block_tables, st.lengths, req_idx=drows,
                             stream=s_dec)
-            cache.decode(l, dq[l], st.block_tables, st.lengths, scale, out[l], req_idx=drows,
-                         stream=s_dec)
+            cache.decode(l, dq[l], st.block_tables, st.lengths, scale, d_out[b][l],
+                         req_idx=drows, stream=s_dec)
         cache.compress(st.block_tables, st.lengths, d_wq[b], wl.N, wl.w, wl.lam, st.free_ids,
                        st.free_count, st.refcount, req_idx=st.compress_rows, stream=s_cmp)
         dd, cc = ev(), ev()
@@ -475,11 +495,20 @@ def run_mixed(args, world, rank, local):
         cc.record(s_cmp)
         main.wait_event(dd)
         main.wait_event(cc)
-        for h, x in zip(h_out, out):
-            h.copy_(x, non_blocking=True)
-        h_tab.copy_(st.block_tables, non_blocking=True)
-        h_len.copy_(st.lengths, non_blocking=True)
+        d_tab[b].copy_(st.block_tables, non_blocking=True)
+        d_len[b].copy_(st.lengths, non_blocking=True)
         free[b].record(main)
+
+    def take(i):
+        # step i's results cross back on the copy stream while step i+1 runs
+        b = i % 2
+        cp.wait_event(free[b])
+        with torch.cuda.stream(cp):
+            for h, x in zip(h_out, d_out[b]):
+                h.copy_(x, non_blocking=True)
+            h_tab.copy_(d_tab[b], non_blocking=True)
+            h_len.copy_(d_len[b], non_blocking=True)
+        back[b].record(cp)
 
     def loop(steps):
         bring(0)
@@ -487,6 +516,7 @@ def run_mixed(args, world, rank, local):
             if i + 1 < steps:
                 bring(i + 1)
             run(i)
+            take(i)
 
     loop(2)
     torch.cuda.synchronize()
@@ -494,10 +524,19 @@ def run_mixed(args, world, rank, local):
     p0.record(main)
     cp.wait_event(p0)
     loop(E)
+    main.wait_stream(cp)  # the last step's results have reached the host
     p1.record(main)
     p1.synchronize()
     e2e_ms = p0.elapsed_time(p1) / E
     assert cache.status() == zp.OK
+    # the rows an end-to-end step moves (one untimed compression from the
+    # block state its inputs restore)
+    for a, b in zip(live, h_state_ft):
+        a.copy_(b)
+    append_slots(main)
+    compress(main, kept)
+    torch.cuda.synchronize()
+    e2e_moved = count_moved(kept, src_tab, st.block_tables[st.compress_rows.long(), :wl.N - 1], wl)
 
     ov, se, slot_ms, dec_ms, cmp_ms, e2e_ms, e2e_serial_ms = reduce_max(
         [ov, se, slot_ms, dec_ms, cmp_ms, e2e_ms, e2e_serial_ms], world, dev)
@@ -549,8 +588,16 @@ def run_mixed(args, world, rank, local):
                 "how": "C ABI calls, overlapped as above; each step's inputs (window queries, "
                        "decode queries, new K/V rows, block state) cross from pinned host memory "
                        "on a copy stream into one of two device buffer sets while the previous "
-                       "step computes, its outputs (attention, tables, lengths) cross back; the "
+                       "step computes, and its outputs (attention, tables, lengths) cross back on "
+                       "it while the next step computes; every copy inside the timed region; the "
                        "KV pools stay resident",
+                "moved_rows_per_unit": e2e_moved / cmp_units,
+                "device_step_moved_rows_per_unit": moved / cmp_units,
+                "work": "the pools are not restored between end-to-end steps; the block state "
+                        "each step's inputs restore holds every block of a compressing request "
+                        "twice, so its compaction goes to fresh targets and every step "
+                        "compresses the same data, moving all rows of a unit (above, against "
+                        "the device-timed step's in-place compaction)",
                 "serial_ms_per_step": e2e_serial_ms,
                 "serial_value": world * Rc * wl.T / (e2e_serial_ms * 1e-3)},
         "gpu_launches": 2 * K * (2 + 3 + wl.L * (
@@ -995,6 +1042,17 @@ def run_gpu(args, world, rank, local):
     e2e_ms = pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_state,
                            h_out, h_tab, h_len, req_idx, dec_rows, scale, E)
     status2 = cache.status()
+    # the work of an end-to-end step: its pools are not restored, so each step
+    # compresses what the previous one left; its moved rows, on the state the
+    # loop ended with (block state restored, one untimed compression)
+    restore(pools=False)
+    kept_dbg = torch.empty((wl.L, Rc, wl.Hkv, (wl.N - 1) * wl.b), dtype=torch.int32, device=dev)
+    src_tab = st.block_tables[st.compress_rows.long(), :wl.N].clone()
+    compress(None, kept_dbg)
+    torch.cuda.synchronize()
+    e2e_moved = count_moved(kept_dbg, src_tab, st.block_tables[st.compress_rows.long(), :wl.N - 1],
+                            wl)
+    del kept_dbg
 
     # ablation: the redundancy of every key against all keys of its unit (the
     # score the block-local one replaces), timed alone on the same units
@@ -1113,6 +1171,11 @@ def run_gpu(args, world, rank, local):
                        "resident",
                 "serial_ms_per_step": e2e_serial_ms,
                 "serial_value": world * req_tokens / (e2e_serial_ms * 1e-3),
+                "moved_rows_per_unit": e2e_moved / units,
+                "device_step_moved_rows_per_unit": moved / units,
+                "work": "the pools are not restored between end-to-end steps, so each compresses "
+                        "what the previous one left (the moved rows above, from one untimed "
+                        "compression of the final state, against the device-timed step's)",
                 "host_link_gbs": {"h2d": xfer[0], "d2h": xfer[1],
                                   "what": "pinned host <-> device copy rates measured beside "
                                           "the e2e loop (one large copy each way)"}},
