@@ -160,6 +160,9 @@ def check_prefill(orc, c, req_idx=None, sample=None, strict=False):
     dict(lens=[8200, 9001], n_max=128, d=128, w=8, Hq=8),                     # 5 chunks
     dict(lens=[3100, 4000], n_max=128, d=128, w=16, Hq=8),                    # 64 rows
     dict(lens=[40, 77, 200], n_max=2, d=128, w=16, Hq=8),                     # keep 0: window only
+    # prompts of 8.5 K (d 64) and 17 K tokens
+    dict(lens=[8500, 3000], n_max=128, d=64, w=8, Hq=8),
+    dict(lens=[17000, 5000], n_max=128, d=128, w=8, Hq=8),
 ])
 def test_prefill_parity(orc, case):
     case = dict(case)
