@@ -53,24 +53,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// 2D view [num_blocks * Hkv * b rows][d] of a pool, box {64 columns, b rows},
-// 128-byte swizzle: one (block, kv head) slab is loaded as d/64 boxes.
-bool encode_pool_map(CUtensorMap *map, void *pool, int num_blocks, int hkv, int d)
-{
-    auto fn = encode_fn();
-    if (!fn)
-        return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(d),
-                          static_cast<cuuint64_t>(num_blocks) * hkv * zp::kBlk};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(zp::kBlk)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool, dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return res == CUDA_SUCCESS;
-}
-
 // The same 2D view with a box of one whole row ({d columns, 1 row}) and no
 // swizzle: the compaction gathers four arbitrary pool rows per load
 // (tile::gather4, whose box is one row high) into a [16][d] destination slab.
@@ -93,6 +75,42 @@ bool encode_row_map(CUtensorMap *map, void *pool, int num_blocks, int hkv, int d
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
+
+namespace zp {
+
+// 2D view [num_blocks * Hkv * b rows][d] of a pool, box {64 columns, b rows},
+// 128-byte swizzle: one (block, kv head) slab is loaded as d/64 boxes.
+bool encode_pool_map(CUtensorMap *map, const void *pool, int num_blocks, int hkv, int d)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(d),
+                          static_cast<cuuint64_t>(num_blocks) * hkv * zp::kBlk};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(zp::kBlk)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
+// One split per pair whenever the pairs alone give every SM a CTA (the
+// hardware scheduler balances the waves; a split adds partials and a combine
+// launch), else enough to give every SM one, at most kMaxSplits, never fewer
+// than 4 blocks per split.
+int decode_splits(long long pairs, int bt_stride, int num_sms, int *bps)
+{
+    const long long target = num_sms;
+    int splits = static_cast<int>(
+        std::min<long long>(kMaxSplits, std::max<long long>(1, (target + pairs - 1) / pairs)));
+    splits = std::min(splits, std::max(1, bt_stride / 4));
+    *bps = (bt_stride + splits - 1) / splits;
+    return (bt_stride + *bps - 1) / *bps;
+}
+
+}  // namespace zp
 
 struct zp_cache {
     int device = 0;
@@ -230,8 +248,9 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
         vrmaps(D.num_layers);
     bool ok = true;
     for (int l = 0; l < D.num_layers && ok; ++l) {
-        ok = encode_pool_map(&kmaps[l], D.k_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim) &&
-             encode_pool_map(&vmaps[l], D.v_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim) &&
+        ok = zp::encode_pool_map(&kmaps[l], D.k_pools[l], D.num_blocks, D.num_kv_heads,
+                                 D.head_dim) &&
+             zp::encode_pool_map(&vmaps[l], D.v_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim) &&
              encode_row_map(&krmaps[l], D.k_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim) &&
              encode_row_map(&vrmaps[l], D.v_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim);
     }
@@ -528,16 +547,9 @@ zp_status zp_paged_decode_attn(zp_cache *c, int32_t layer, const void *q,
     if (!on_device(c))
         return ZP_ERR_INVALID_ARG;
 
-    // splits per (request, kv head): one split when the pairs alone give every
-    // SM a CTA (the hardware scheduler balances the waves; a split adds
-    // partials and a combine launch), else enough to give every SM one, at
-    // most kMaxSplits, never fewer than 4 blocks per split
-    const int pairs = R * c->Hkv;
-    const int target = c->num_sms;
-    int splits = std::min(kMaxSplits, std::max(1, (target + pairs - 1) / pairs));
-    splits = std::min(splits, std::max(1, bt_stride / 4));
-    const int bps = (bt_stride + splits - 1) / splits;
-    splits = (bt_stride + bps - 1) / bps;
+    int bps = 0;
+    const int splits = zp::decode_splits(static_cast<long long>(R) * c->Hkv, bt_stride,
+                                         c->num_sms, &bps);
 
     zp::DecodeArgs da{};
     // the per-layer maps live in device memory; kernels take their address

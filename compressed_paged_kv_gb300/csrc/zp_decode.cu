@@ -38,8 +38,10 @@ struct DecodeSmem {
     static constexpr int ALLOC = BYTES + 1024;
 };
 
-template <int D>
-__global__ void __launch_bounds__(kDecThreads, 2) zp_decode_kernel(const DecodeArgs a)
+// MAPV: the tensor maps come by value in the parameters (a.kmap_v, a.vmap_v)
+template <int D, bool MAPV>
+__global__ void __launch_bounds__(kDecThreads, 2)
+    zp_decode_kernel(const __grid_constant__ DecodeArgs a)
 {
     pdl_wait();  // launched early: everything of the kernels before it is visible from here
     using S = DecodeSmem<D>;
@@ -101,6 +103,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) zp_decode_kernel(const DecodeA
     uint8_t *my_stage = sm + S::off_stage + wi * kDecStages * S::STAGE_BYTES;
     uint64_t *my_bar = bars + wi * kDecStages;
     const int32_t *trow = a.tables + (size_t)row * a.stride;
+    const CUtensorMap *kmap = MAPV ? &a.kmap_v : a.kmap;
+    const CUtensorMap *vmap = MAPV ? &a.vmap_v : a.vmap;
 
     auto issue = [&](int i) {
         int blk = trow[first + i * kDecWarps];
@@ -115,8 +119,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) zp_decode_kernel(const DecodeA
         const int y = (blk * a.Hkv + h) * kBlk;
 #pragma unroll
         for (int hf = 0; hf < HALVES; ++hf) {
-            tma_load_2d(kd + hf * kBlk * 128, a.kmap, hf * 64, y, &my_bar[s]);
-            tma_load_2d(vd + hf * kBlk * 128, a.vmap, hf * 64, y, &my_bar[s]);
+            tma_load_2d(kd + hf * kBlk * 128, kmap, hf * 64, y, &my_bar[s]);
+            tma_load_2d(vd + hf * kBlk * 128, vmap, hf * 64, y, &my_bar[s]);
         }
     };
     if (lane == 0)
@@ -289,11 +293,11 @@ __global__ void __launch_bounds__(D) zp_decode_combine(const DecodeArgs a)
     a.out[(size_t)rh * D + c] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
 }
 
-template <int D>
+template <int D, bool MAPV>
 static cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t s)
 {
     using Sm = DecodeSmem<D>;
-    cudaError_t err = cudaFuncSetAttribute(zp_decode_kernel<D>,
+    cudaError_t err = cudaFuncSetAttribute(zp_decode_kernel<D, MAPV>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::ALLOC);
     if (err != cudaSuccess)
         return err;
@@ -309,7 +313,7 @@ static cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t s)
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, zp_decode_kernel<D>, a);
+    err = cudaLaunchKernelEx(&cfg, zp_decode_kernel<D, MAPV>, a);
     if (err != cudaSuccess || a.splits == 1)
         return err;
     cfg.gridDim = dim3(static_cast<unsigned>(a.R * a.Hq), 1, 1);
@@ -321,9 +325,18 @@ static cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t s)
 cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t s)
 {
     if (d == 64)
-        return launch_decode_t<64>(a, s);
+        return launch_decode_t<64, false>(a, s);
     if (d == 128)
-        return launch_decode_t<128>(a, s);
+        return launch_decode_t<128, false>(a, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_mapv(const DecodeArgs &a, int d, cudaStream_t s)
+{
+    if (d == 64)
+        return launch_decode_t<64, true>(a, s);
+    if (d == 128)
+        return launch_decode_t<128, true>(a, s);
     return cudaErrorInvalidValue;
 }
 

@@ -117,6 +117,10 @@ struct DecodeArgs {
     __nv_bfloat16 *out;
     float *part;          // [R][Hq][splits][2 + d] (m, l, o[d]) when splits > 1
     int32_t *sticky;
+    // launches that take the maps by value (launch_decode_mapv): the K and V
+    // tensor maps in the kernel's parameter space, for a caller with no
+    // device memory to hold them; kmap / vmap are then unused
+    CUtensorMap kmap_v, vmap_v;
 };
 
 // Compression at admission (zp_prefill.cu); units u = (l*R + r)*Hkv + h.
@@ -184,6 +188,13 @@ cudaError_t launch_compress(const CompressArgs &a, int d, int mt, int units, cud
 cudaError_t launch_compress_d64(const CompressArgs &a, int mt, int units, cudaStream_t s);
 cudaError_t launch_compress_d128(const CompressArgs &a, int mt, int units, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t s);
+cudaError_t launch_decode_mapv(const DecodeArgs &a, int d, cudaStream_t s);
+// Splits per (request, kv head) of a decode over `pairs` (request, kv head)
+// pairs and tables of bt_stride blocks on `num_sms` SMs; *bps: blocks per split.
+int decode_splits(long long pairs, int bt_stride, int num_sms, int *bps);
+// The swizzled 2D tensor map of a pool [num_blocks][hkv][b][d] that the
+// decode and compression kernels load (box: 64 columns x b rows).
+bool encode_pool_map(CUtensorMap *map, const void *pool, int num_blocks, int hkv, int d);
 
 // ------------------------------------------------------------ device helpers
 #ifdef __CUDACC__

@@ -227,20 +227,26 @@ zp_status zp_paged_decode_attn(zp_cache *cache, int32_t layer, const void *q,
  * decode attention: an allocator or memory-pool callback (allocating there
  * would re-enter the allocator), a plug-in in a process whose host owns all
  * device memory, a real-time path that must not wait on the allocator.  This
- * call needs no zp_cache handle and allocates nothing.  Its split-K partial
- * results live in one fixed device array compiled into the library (about
- * 16.3 MiB), created when the library's device code is loaded into a CUDA
- * context -- usually at the first call in that context -- and held until the
- * process exits.
+ * call needs no zp_cache handle and allocates nothing: it runs the same
+ * kernels as zp_paged_decode_attn, with the two pools' tensor maps encoded on
+ * the host and passed in the launch parameters, and with the same splits its
+ * results are those of zp_paged_decode_attn bit for bit.  Its split-K
+ * partial results live in one fixed device array compiled into the library
+ * (about 16.3 MiB), created when the library's device code is loaded into a
+ * CUDA context -- usually at the first call in that context -- and held until
+ * the process exits.
  *
  *  k_pool, v_pool  device bf16 pools of one layer, [num_blocks][num_kv_heads][16][head_dim],
  *                  16-byte aligned (ZP_ERR_INVALID_ARG otherwise)
- *  q, out          device bf16 [R][num_q_heads][head_dim]; other arguments as in
- *                  zp_paged_decode_attn
+ *  q, out          device bf16 [R][num_q_heads][head_dim], q 16-byte and out
+ *                  2-byte aligned (ZP_ERR_INVALID_ARG otherwise); other
+ *                  arguments as in zp_paged_decode_attn
  *  status          nullable device int32: device-detected errors (a length or
  *                  block id out of range) are recorded there with atomicCAS from 0
- * Limits: head_dim 64 or 128, block size 16, R * num_q_heads <= 32768
- * (ZP_ERR_UNSUPPORTED beyond).
+ *                  (with NULL they go to the array's last word and are not read)
+ * Limits: head_dim 64 or 128, block size 16, num_q_heads / num_kv_heads <= 16,
+ * R * num_q_heads <= 32768 (ZP_ERR_UNSUPPORTED beyond); fewer splits than
+ * zp_paged_decode_attn's where the array cannot hold their partials.
  * The array's device address belongs to the current CUDA context (another
  * context on the same device, or the primary context re-created after
  * cudaDeviceReset, has its own copy).  A call made while `stream` is not

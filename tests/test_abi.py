@@ -137,6 +137,9 @@ def test_descriptor_and_size_limits_need_no_gpu(lib):
     assert noalloc(R=0) == zp.OK                           # nothing to do, nothing launched
     assert lib.zp_paged_decode_attn_noalloc(None, buf, 8, 2, 4, 64, buf, buf, 8, 4, buf, None, 1,
                                             0.125, buf, None, None) == zp.ERR_INVALID_ARG
+    assert lib.zp_paged_decode_attn_noalloc(buf, buf, 8, 2, 4, 64, P(4096 + 8), buf, 8, 4, buf,
+                                            None, 1, 0.125, buf, None, None) == zp.ERR_INVALID_ARG
+    assert noalloc(Hkv=1, Hq=32) == zp.ERR_UNSUPPORTED    # 32 query heads on one kv head
     odd = P(4096 + 8)  # pools are read 16 bytes at a time
     assert lib.zp_paged_decode_attn_noalloc(odd, buf, 8, 2, 4, 64, buf, buf, 8, 4, buf, None, 1,
                                             0.125, buf, None, None) == zp.ERR_INVALID_ARG
