@@ -449,12 +449,28 @@ def run_mixed(args, world, rank, local):
     crows_blk = pristine[0][st.compress_rows.long()].flatten().long()
     h_state_ft[2][crows_blk.cpu()] += 1
     cp = torch.cuda.Stream(device=dev)
-    d_wq = [torch.empty_like(st.window_q) for _ in range(2)]
-    d_in = [[torch.empty_like(x) for x in q + k_new + v_new] for _ in range(2)]
-    d_state = [[torch.empty_like(t) for t in pristine] for _ in range(2)]
-    d_out = [out, [torch.empty_like(x) for x in out]]
-    d_tab = [torch.empty_like(st.block_tables) for _ in range(2)]
-    d_len = [torch.empty_like(st.lengths) for _ in range(2)]
+    # a step's inputs, and its results, each cross as one copy of one packed
+    # buffer (pinned on the host) rather than as one copy per tensor
+    h_src = [h_wq] + list(h_q) + list(h_kv) + list(h_state_ft)
+    h_inp, hv = packed(torch, h_src, "cpu", pin=True)
+    for v, t in zip(hv, h_src):
+        v.copy_(t)
+    nq = len(h_q) + len(h_kv)
+    d_flat, d_wq, d_in, d_state = [], [], [], []
+    for _ in range(2):
+        flat, views = packed(torch, hv, dev)
+        d_flat.append(flat)
+        d_wq.append(views[0])
+        d_in.append(views[1:1 + nq])
+        d_state.append(views[1 + nq:])
+    h_res, _ = packed(torch, list(h_out) + [h_tab, h_len], "cpu", pin=True)
+    d_res, d_out, d_tab, d_len = [], [], [], []
+    for _ in range(2):
+        flat, views = packed(torch, list(out) + [st.block_tables, st.lengths], dev)
+        d_res.append(flat)
+        d_out.append(views[:len(out)])
+        d_tab.append(views[len(out)])
+        d_len.append(views[len(out) + 1])
     ready = [torch.cuda.Event() for _ in range(2)]   # inputs of set b landed
     free = [torch.cuda.Event() for _ in range(2)]    # step on set b computed
     back = [torch.cuda.Event() for _ in range(2)]    # results of set b on the host
@@ -465,9 +481,7 @@ def run_mixed(args, world, rank, local):
         if i >= 2:
             cp.wait_event(free[b])
         with torch.cuda.stream(cp):
-            d_wq[b].copy_(h_wq, non_blocking=True)
-            for x, h in zip(d_in[b] + d_state[b], h_q + h_kv + h_state_ft):
-                x.copy_(h, non_blocking=True)
+            d_flat[b].copy_(h_inp, non_blocking=True)
         ready[b].record(cp)
 
     def run(i):
@@ -504,10 +518,7 @@ def run_mixed(args, world, rank, local):
         b = i % 2
         cp.wait_event(free[b])
         with torch.cuda.stream(cp):
-            for h, x in zip(h_out, d_out[b]):
-                h.copy_(x, non_blocking=True)
-            h_tab.copy_(d_tab[b], non_blocking=True)
-            h_len.copy_(d_len[b], non_blocking=True)
+            h_res.copy_(d_res[b], non_blocking=True)
         back[b].record(cp)
 
     def loop(steps):
@@ -1233,6 +1244,21 @@ def run_gpu(args, world, rank, local):
     return res
 
 
+def packed(torch, tensors, device, pin=False):
+    """One flat byte buffer with room for `tensors` (each at a 256-byte
+    aligned offset) and views of it shaped like them."""
+    offs, n = [], 0
+    for t in tensors:
+        offs.append(n)
+        n += (t.numel() * t.element_size() + 255) // 256 * 256
+    flat = torch.empty(n, dtype=torch.uint8, device=device)
+    if pin:
+        flat = flat.pin_memory()
+    views = [flat[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+             for o, t in zip(offs, tensors)]
+    return flat, views
+
+
 def pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_state, h_out, h_tab,
                   h_len, req_idx, dec_rows, scale, E):
     """Steps through the C ABI as a serving loop runs them: a copy stream
@@ -1247,12 +1273,27 @@ def pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_sta
     region)."""
     comp = torch.cuda.current_stream()
     cp = torch.cuda.Stream()
-    d_wq = [torch.empty_like(st.window_q) for _ in range(2)]
-    d_q = [[torch.empty_like(x) for x in q] for _ in range(2)]
-    d_state = [[torch.empty_like(t) for t in pristine] for _ in range(2)]
-    d_out = [out, [torch.empty_like(x) for x in out]]
-    d_tab = [torch.empty_like(st.block_tables) for _ in range(2)]
-    d_len = [torch.empty_like(st.lengths) for _ in range(2)]
+    L = wl.L
+    # a step's inputs, and its results, each cross as one copy of one packed
+    # buffer (pinned on the host) rather than as one copy per tensor
+    h_in, hv = packed(torch, [h_wq] + list(h_q) + list(h_state), "cpu", pin=True)
+    for v, t in zip(hv, [h_wq] + list(h_q) + list(h_state)):
+        v.copy_(t)
+    d_in, d_wq, d_q, d_state = [], [], [], []
+    for _ in range(2):
+        flat, views = packed(torch, hv, st.window_q.device)
+        d_in.append(flat)
+        d_wq.append(views[0])
+        d_q.append(views[1:1 + L])
+        d_state.append(views[1 + L:])
+    h_res, _ = packed(torch, list(h_out) + [h_tab, h_len], "cpu", pin=True)
+    d_res, d_out, d_tab, d_len = [], [], [], []
+    for _ in range(2):
+        flat, views = packed(torch, list(out) + [st.block_tables, st.lengths], st.window_q.device)
+        d_res.append(flat)
+        d_out.append(views[:L])
+        d_tab.append(views[L])
+        d_len.append(views[L + 1])
     ready = [torch.cuda.Event() for _ in range(2)]   # inputs of set b landed
     done = [torch.cuda.Event() for _ in range(2)]    # step on set b computed
     back = [torch.cuda.Event() for _ in range(2)]    # results of set b on the host
@@ -1267,11 +1308,7 @@ def pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_sta
             # compression re-reads K through L2, which the copies would churn
             cp.wait_event(cdone[1 - b])
         with torch.cuda.stream(cp):
-            d_wq[b].copy_(h_wq, non_blocking=True)
-            for x, h in zip(d_q[b], h_q):
-                x.copy_(h, non_blocking=True)
-            for x, h in zip(d_state[b], h_state):
-                x.copy_(h, non_blocking=True)
+            d_in[b].copy_(h_in, non_blocking=True)
         ready[b].record(cp)
 
     def run(i):
@@ -1295,10 +1332,7 @@ def pipelined_e2e(torch, cache, st, wl, q, out, pristine, live, h_wq, h_q, h_sta
         b = i % 2
         cp.wait_event(done[b])
         with torch.cuda.stream(cp):
-            for h, x in zip(h_out, d_out[b]):
-                h.copy_(x, non_blocking=True)
-            h_tab.copy_(d_tab[b], non_blocking=True)
-            h_len.copy_(d_len[b], non_blocking=True)
+            h_res.copy_(d_res[b], non_blocking=True)
         back[b].record(cp)
 
     def loop(steps):
