@@ -13,7 +13,9 @@
 // S = Q K^T and O += P V on the tensor cores (mma.sync bf16, fp32
 // accumulate, P rounded to bf16 for the second product).  Warps merge in
 // shared memory; with more than one split the CTA writes (m, l, o) partials
-// that zp_decode_combine merges with a log-sum-exp.
+// that zp_decode_combine merges with a log-sum-exp.  The two tensor maps come
+// from device memory (the handle's per-layer maps) or, for the allocation-
+// free entry point, by value in the launch parameters.
 #include "zp_internal.cuh"
 
 namespace zp {
