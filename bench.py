@@ -111,7 +111,7 @@ def peaks():
 # the files the compression kernel is compiled from: the recorded DRAM
 # traffic stays valid while none of them changes
 COMPRESS_KERNEL_SOURCES = ["zp_compress_stream.cuh", "zp_internal.cuh", "zp_compress_d64.cu",
-                           "zp_compress_d128.cu"]
+                           "zp_compress_d128.cu", "zp_tmap.cu"]
 
 
 def kernel_source_digest():

@@ -21,7 +21,7 @@ LIB = os.path.join(LIB_DIR, "libzp.so")
 
 SOURCES = ["zp_api.cu", "zp_compress.cu", "zp_compress_d64.cu", "zp_compress_d128.cu",
            "zp_decode.cu", "zp_noalloc.cu", "zp_append.cu", "zp_prefill.cu",
-           "zp_redundancy_global.cu", "zp_redundancy_gram.cu", "zp_blocks.cu"]
+           "zp_redundancy_global.cu", "zp_redundancy_gram.cu", "zp_blocks.cu", "zp_tmap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -1,6 +1,5 @@
 // zp_api.cu -- the C ABI declared in include/zp.h: handle, argument checks,
 // TMA tensor maps, launches.  Host code only.
-#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
 #include <nvtx3/nvToolsExt.h>  // header-only; the ranges cost a pointer test without a profiler
 
 #include <algorithm>
@@ -39,62 +38,11 @@ struct Alloc {
     }
 };
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// The same 2D view with a box of one whole row ({d columns, 1 row}) and no
-// swizzle: the compaction gathers four arbitrary pool rows per load
-// (tile::gather4, whose box is one row high) into a [16][d] destination slab.
-bool encode_row_map(CUtensorMap *map, void *pool, int num_blocks, int hkv, int d)
-{
-    auto fn = encode_fn();
-    if (!fn)
-        return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(d),
-                          static_cast<cuuint64_t>(num_blocks) * hkv * zp::kBlk};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(d), 1};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool, dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return res == CUDA_SUCCESS;
-}
-
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
 
 namespace zp {
-
-// 2D view [num_blocks * Hkv * b rows][d] of a pool, box {64 columns, b rows},
-// 128-byte swizzle: one (block, kv head) slab is loaded as d/64 boxes.
-bool encode_pool_map(CUtensorMap *map, const void *pool, int num_blocks, int hkv, int d)
-{
-    auto fn = encode_fn();
-    if (!fn)
-        return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(d),
-                          static_cast<cuuint64_t>(num_blocks) * hkv * zp::kBlk};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(zp::kBlk)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims,
-                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return res == CUDA_SUCCESS;
-}
 
 // One split per pair whenever the pairs alone give every SM a CTA (the
 // hardware scheduler balances the waves; a split adds partials and a combine
@@ -251,8 +199,8 @@ zp_status zp_cache_create(const zp_cache_desc *desc, zp_cache **out)
         ok = zp::encode_pool_map(&kmaps[l], D.k_pools[l], D.num_blocks, D.num_kv_heads,
                                  D.head_dim) &&
              zp::encode_pool_map(&vmaps[l], D.v_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim) &&
-             encode_row_map(&krmaps[l], D.k_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim) &&
-             encode_row_map(&vrmaps[l], D.v_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim);
+             zp::encode_row_map(&krmaps[l], D.k_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim) &&
+             zp::encode_row_map(&vrmaps[l], D.v_pools[l], D.num_blocks, D.num_kv_heads, D.head_dim);
     }
     ok = ok && cudaMemset(c->base, 0, o_kmaps) == cudaSuccess &&
          cudaMemset(b + o_rowmark, 0, 4 * static_cast<size_t>(D.max_requests)) == cudaSuccess &&

@@ -195,6 +195,8 @@ int decode_splits(long long pairs, int bt_stride, int num_sms, int *bps);
 // The swizzled 2D tensor map of a pool [num_blocks][hkv][b][d] that the
 // decode and compression kernels load (box: 64 columns x b rows).
 bool encode_pool_map(CUtensorMap *map, const void *pool, int num_blocks, int hkv, int d);
+// The same view with a box of one whole row and no swizzle (tile::gather4).
+bool encode_row_map(CUtensorMap *map, const void *pool, int num_blocks, int hkv, int d);
 
 // ------------------------------------------------------------ device helpers
 #ifdef __CUDACC__
