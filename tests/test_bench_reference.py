@@ -171,3 +171,20 @@ def test_bench_parity_near_tie_rule():
     s_far[1] = 0.35                                         # far from the cut
     assert not bench.near_tie(s_far, imp, red, 0.5, kept_o, kept_g, 3)
     assert bench.near_tie(s_tie, imp, red, 0.5, kept_o, kept_o, 3)
+
+
+def test_packed_buffers_hold_each_tensor_at_an_aligned_offset():
+    """The end-to-end loop's packed copies: one flat buffer, every tensor at a
+    256-byte aligned offset, views that read back what was written."""
+    sys.path.insert(0, ROOT)
+    import torch
+    import bench
+    ts = [torch.arange(7, dtype=torch.int32), torch.randn(3, 5).to(torch.bfloat16),
+          torch.arange(300, dtype=torch.int32).view(10, 30)]
+    flat, views = bench.packed(torch, ts, "cpu")
+    for v, t in zip(views, ts):
+        v.copy_(t)
+    for v, t in zip(views, ts):
+        assert torch.equal(v, t) and v.shape == t.shape and v.dtype == t.dtype
+        assert (v.data_ptr() - flat.data_ptr()) % 256 == 0
+    assert flat.numel() == 256 + 256 + 1280
